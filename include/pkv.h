@@ -1,0 +1,203 @@
+/*
+ * pkv.h -- C ABI of the paged KV-cache library for one NVIDIA GB300 (sm_103a).
+ *
+ * Two operations, as the course page "P09 · Paged KV 写入 + decode attention
+ * （参考实现）" (kuanzhou.online, nano-vllm-omni drills) defines them in its
+ * section 题面速览 and its two shape-trace tables (框架视角 · shape trace):
+ *
+ *   pkv_write             write_kv: cache[slot // bs, slot % bs] = k[i] (and v),
+ *                         in place; a negative slot is a padding token and is
+ *                         not written.
+ *   pkv_decode_attention  paged decode attention: each sequence's single query
+ *                         attends to the first context_lens[b] tokens of its
+ *                         paged context, gathered through block_tables[b, :nb]
+ *                         with nb = ceil(n / bs); query head h reads KV head
+ *                         h // (H / KVH); softmax(q . K^T * scale) . V with the
+ *                         softmax in fp32, output in q's dtype.
+ * Long contexts are split into partitions whose partial results are merged
+ * with a log-sum-exp rescale, the partitioned variant the interview note
+ * "PagedAttention kernel: paged KV cache 与 block table"
+ * (inference-learning-path.pages.dev), section 深入原理 ("v1 vs v2"),
+ * describes; the result equals the unsplit one up to rounding.
+ *
+ * Common rules
+ *   - Every pointer argument except the host-side ones named below is a
+ *     DEVICE pointer on the current CUDA device.  The caller owns all memory;
+ *     the library allocates nothing on the call path and keeps no pointer
+ *     after a call returns.
+ *   - All work is enqueued on `stream` (NULL = the legacy default stream);
+ *     calls return once the work is enqueued, before it runs.
+ *   - Argument errors that need no device data are caught on the host before
+ *     anything is enqueued and returned as a status.
+ *   - Errors that depend on device data (a slot past the pool, a table entry
+ *     outside [0, num_blocks), an over-long context) cannot be seen on the
+ *     host: the kernels skip the offending access and OR a PKV_FLAG_* bit into
+ *     *err_flags (a device int, may be NULL).  The caller reads it after the
+ *     stream has synchronised.  Nothing in the library traps or asserts on
+ *     the device.
+ *   - Cache layout: K and V are separate tensors
+ *     [num_blocks, block_size, num_kv_heads, head_dim], contiguous, one
+ *     token's row of num_kv_heads * head_dim elements contiguous.
+ */
+#ifndef PKV_H
+#define PKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define PKV_API __attribute__((visibility("default")))
+#else
+#define PKV_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* The same handle type as cudaStream_t (a CUstream). */
+typedef struct CUstream_st *pkv_stream_t;
+
+typedef enum pkv_status {
+  PKV_OK = 0,
+  PKV_ERR_INVALID_ARG = 1,   /* a size, pointer, alignment or count is not valid */
+  PKV_ERR_UNSUPPORTED = 2,   /* valid, but a shape/dtype this build does not handle */
+  PKV_ERR_CUDA = 3,          /* a CUDA runtime call or a kernel launch failed */
+  PKV_ERR_WORKSPACE = 4      /* the workspace is missing or smaller than needed */
+} pkv_status;
+
+typedef enum pkv_dtype {
+  PKV_F32 = 0,   /* float32 */
+  PKV_BF16 = 1,  /* bfloat16 */
+  PKV_F16 = 2    /* float16 */
+} pkv_dtype;
+
+/* Bits the kernels OR into *err_flags. */
+#define PKV_FLAG_SLOT_OUT_OF_RANGE 0x1   /* pkv_write: slot >= num_blocks * block_size; token skipped */
+#define PKV_FLAG_BLOCK_OUT_OF_RANGE 0x2  /* decode: an entry of block_tables[b, :nb] outside
+                                            [0, num_blocks); block 0 is read in its place and
+                                            that sequence's output is unspecified */
+#define PKV_FLAG_CONTEXT_TOO_LONG 0x4    /* decode: context_lens[b] > max_blocks * block_size;
+                                            clamped, output of that sequence unspecified */
+#define PKV_FLAG_CONTEXT_NEGATIVE 0x8    /* decode: context_lens[b] < 0; treated as 0 */
+#define PKV_FLAG_CONTEXT_OVER_HINT 0x10  /* decode: context_lens[b] > max_context_len (the host
+                                            hint sized the grid too small); output of that
+                                            sequence unspecified */
+#define PKV_FLAG_TIMEOUT 0x20            /* a bounded wait for an asynchronous copy ran out
+                                            (should never happen); outputs unspecified */
+
+/*
+ * pkv_write -- write_kv / reshape_and_cache.
+ * Definition: course page "P09 · Paged KV 写入 + decode attention（参考实现）",
+ * section 题面速览 ("写: cache[slot // bs, slot % bs] = k[i]") and the
+ * write_kv shape trace (keep = slot >= 0; blk = s // bs; off = s % bs;
+ * k_cache[blk, off] = k[keep]; same for v; in place, returns nothing).
+ *
+ *   k_cache, v_cache  [num_blocks, block_size, num_kv_heads, head_dim], dtype dt,
+ *                     written in place (only rows named by a kept slot change)
+ *   k, v              [num_tokens, num_kv_heads, head_dim]; token i starts at
+ *                     element i * k_token_stride (resp. v_token_stride);
+ *                     each token's num_kv_heads * head_dim elements contiguous
+ *   slot_mapping      [num_tokens] int64: flat slot block * block_size + offset;
+ *                     any negative value = padding, skipped silently
+ *   err_flags         device int or NULL: PKV_FLAG_SLOT_OUT_OF_RANGE
+ * The copy is bit-exact.  Two kept tokens with the same slot in one call
+ * race (which one lands is unspecified).  num_tokens == 0 enqueues nothing.
+ * Errors: PKV_ERR_INVALID_ARG for a NULL pointer with num_tokens > 0, a
+ * non-positive size, or a token stride smaller than one row;
+ * PKV_ERR_CUDA if the launch fails.
+ */
+PKV_API pkv_status pkv_write(void *k_cache, void *v_cache, const void *k, const void *v,
+                             const int64_t *slot_mapping, int64_t num_tokens,
+                             int64_t k_token_stride, int64_t v_token_stride,
+                             int64_t num_blocks, int block_size, int num_kv_heads,
+                             int head_dim, pkv_dtype dt, int *err_flags, pkv_stream_t stream);
+
+/*
+ * pkv_decode_workspace_size -- bytes of device workspace pkv_decode_attention
+ * needs for these sizes (host only, no CUDA call).  partition_size as in
+ * pkv_decode_attention (0 = automatic: the size covers every partition size
+ * the automatic choice can make).  max_context_len: the longest context the
+ * calls will see (0 = max_blocks * block_size).  Returns 0 for invalid sizes.
+ *
+ * The workspace holds per-partition partial results and one counter per
+ * (sequence, head group).  Before its FIRST use it must be zero-filled
+ * (e.g. cudaMemset); every call leaves the counters at zero again, so the
+ * same workspace can be reused by later calls on the same stream without
+ * clearing.  Calls that run concurrently need separate workspaces.
+ */
+PKV_API size_t pkv_decode_workspace_size(int B, int H, int num_kv_heads, int head_dim,
+                                         int block_size, int max_blocks, int max_context_len,
+                                         int partition_size);
+
+/*
+ * pkv_decode_attention -- paged decode attention (one query per sequence).
+ * Definition: course page "P09 · Paged KV 写入 + decode attention（参考实现）",
+ * section 题面速览 ("decode 读") and the paged_decode_attention shape trace:
+ * n = context_lens[b]; nb = ceil(n / bs); table = block_tables[b, :nb];
+ * gather k_cache[table] in table order; keep the first n rows; head h uses
+ * KV head h // (H / KVH); fp32 scores times scale, softmax over the n
+ * tokens in fp32, weighted sum of V, cast to q's dtype.
+ *
+ *   out           [B, H, head_dim], dtype dt (written; rows of sequences with
+ *                 context_lens[b] == 0 are set to zero)
+ *   q             [B, H, head_dim], dtype dt
+ *   k_cache, v_cache  [num_blocks, block_size, num_kv_heads, head_dim], dtype dt
+ *   block_tables  [B, max_blocks] int32; only the first ceil(n/bs) entries of
+ *                 row b are read -- the rest may hold anything (e.g. 99999)
+ *   context_lens  [B] int32
+ *   scale         multiplies q.K before the softmax (e.g. 1/sqrt(head_dim))
+ *   max_context_len  host-side upper bound on context_lens (sizes the grid;
+ *                 0 = max_blocks * block_size).  A longer context sets
+ *                 PKV_FLAG_CONTEXT_OVER_HINT.
+ *   partition_size   tokens per partition of the split-KV path, a positive
+ *                 multiple of 16 (or of block_size when that is not a multiple
+ *                 of 16); 0 = choose from the sizes and the SM count.  A
+ *                 context longer than one partition is processed by several
+ *                 CTAs whose (max, sum, weighted-V) partials are merged in the
+ *                 workspace with a log-sum-exp rescale.
+ *   workspace, workspace_bytes  device scratch of at least
+ *                 pkv_decode_workspace_size(...) bytes, zero-filled before
+ *                 first use (may be NULL/0 when no context is longer than one
+ *                 partition)
+ *   err_flags     device int or NULL (PKV_FLAG_BLOCK_OUT_OF_RANGE,
+ *                 PKV_FLAG_CONTEXT_*, PKV_FLAG_TIMEOUT)
+ * Supported: H % num_kv_heads == 0; head_dim a multiple of 8 in [8, 512] (fp32:
+ * a multiple of 4); block_size >= 1; q, out, caches 16-byte aligned.  bf16 /
+ * fp16 with head_dim in {64, 128, 192, 256} and block_size a multiple of 16
+ * run the tensor-core kernel; every other supported shape runs the
+ * CUDA-core kernel.
+ * Errors: PKV_ERR_INVALID_ARG, PKV_ERR_UNSUPPORTED, PKV_ERR_WORKSPACE,
+ * PKV_ERR_CUDA.  B == 0 enqueues nothing.
+ */
+PKV_API pkv_status pkv_decode_attention(void *out, const void *q, const void *k_cache,
+                                        const void *v_cache, const int32_t *block_tables,
+                                        const int32_t *context_lens, int B, int H,
+                                        int num_kv_heads, int head_dim, int block_size,
+                                        int max_blocks, int64_t num_blocks, float scale,
+                                        pkv_dtype dt, int max_context_len, int partition_size,
+                                        void *workspace, size_t workspace_bytes, int *err_flags,
+                                        pkv_stream_t stream);
+
+/*
+ * pkv_decode_plan -- the partition size and the partitions per sequence that
+ * pkv_decode_attention would use for these arguments on a GPU with
+ * num_sms SMs (host only, no CUDA call; for tests and tuning).  Returns the
+ * partition size in tokens (>= 16), or 0 for invalid sizes; *kernel is set to
+ * 1 for the tensor-core kernel, 0 for the CUDA-core kernel.
+ */
+PKV_API int pkv_decode_plan(int B, int H, int num_kv_heads, int head_dim, int block_size,
+                            int max_blocks, int max_context_len, int partition_size,
+                            pkv_dtype dt, int num_sms, int *max_partitions, int *kernel);
+
+/* A static, human-readable name for a status code. */
+PKV_API const char *pkv_status_string(pkv_status status);
+
+/* Version string of the library build. */
+PKV_API const char *pkv_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H */

@@ -70,7 +70,7 @@ def _declare(lib):
     lib.pkv_oracle_write.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, c_int]
     lib.pkv_oracle_write.restype = c_int
     lib.pkv_oracle_decode.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i64,
-                                      i64, ctypes.c_double, c_int, i64, i64]
+                                      i64, ctypes.c_double, c_int, i64, i64, i64, i64]
     lib.pkv_oracle_decode.restype = c_int
     lib.pkv_oracle_round.argtypes = [vp, vp, i64, c_int]
     lib.pkv_oracle_round.restype = c_int
@@ -117,11 +117,13 @@ def write(k_cache, v_cache, k, v, slot_mapping, lib=None) -> None:
 
 
 def decode(q, k_cache, v_cache, block_tables, context_lens, scale: float,
-           seqs: tuple[int, int] | None = None, out=None, lib=None):
+           seqs: tuple[int, int] | None = None, heads: tuple[int, int] | None = None,
+           out=None, lib=None):
     """Paged decode attention; returns out [B, H, D] in q.dtype.
 
-    ``seqs=(b0, b1)`` computes only sequences b0..b1-1 (the other rows of
-    ``out`` are left as they were)."""
+    ``seqs=(b0, b1)`` / ``heads=(h0, h1)`` restrict the work to sequences
+    b0..b1-1 and query heads h0..h1-1 (the other rows of ``out`` are left as
+    they were)."""
     lib = lib or load()
     B, H, D = q.shape
     nblk, bs, kvh, d2 = k_cache.shape
@@ -133,9 +135,11 @@ def decode(q, k_cache, v_cache, block_tables, context_lens, scale: float,
     if out is None:
         out = torch.zeros_like(q)
     b0, b1 = seqs if seqs is not None else (0, B)
+    h0, h1 = heads if heads is not None else (0, H)
     _check(lib.pkv_oracle_decode(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache),
                                  _ptr(block_tables), _ptr(context_lens), B, H, kvh, D, bs,
-                                 max_blocks, nblk, float(scale), _DTYPE_CODE[q.dtype], b0, b1))
+                                 max_blocks, nblk, float(scale), _DTYPE_CODE[q.dtype], b0, b1,
+                                 h0, h1))
     return out
 
 

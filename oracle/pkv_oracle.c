@@ -192,7 +192,8 @@ int pkv_oracle_write(void *k_cache, void *v_cache, const void *k, const void *v,
 /* ----------------------------------------------------------------- decode */
 
 /*
- * paged decode attention for the sequences b in [b_begin, b_end):
+ * paged decode attention for the sequences b in [b_begin, b_end) and the
+ * query heads h in [h_begin, h_end) (the whole batch: [0, B) x [0, H)):
  *   n    = context_lens[b]
  *   nb   = ceil(n / bs); only block_tables[b, 0:nb] is read
  *   for each query head h:  kvh = h / (H / KVH)
@@ -206,10 +207,12 @@ int pkv_oracle_decode(void *out, const void *q, const void *k_cache, const void 
                       const int32_t *block_tables, const int32_t *context_lens,
                       int64_t B, int64_t H, int64_t num_kv_heads, int64_t head_dim,
                       int64_t block_size, int64_t max_blocks, int64_t num_blocks,
-                      double scale, int dtype, int64_t b_begin, int64_t b_end) {
+                      double scale, int dtype, int64_t b_begin, int64_t b_end,
+                      int64_t h_begin, int64_t h_end) {
   if (B < 0 || H <= 0 || num_kv_heads <= 0 || H % num_kv_heads != 0 || head_dim <= 0 ||
       block_size <= 0 || max_blocks < 0 || num_blocks < 0 || dtype < ORC_F32 ||
-      dtype > ORC_F16 || b_begin < 0 || b_end > B || b_begin > b_end)
+      dtype > ORC_F16 || b_begin < 0 || b_end > B || b_begin > b_end || h_begin < 0 ||
+      h_end > H || h_begin > h_end)
     return ORC_ERR_ARG;
   const int64_t KVH = num_kv_heads, D = head_dim, bs = block_size;
   const int64_t group = H / KVH;
@@ -228,7 +231,7 @@ int pkv_oracle_decode(void *out, const void *q, const void *k_cache, const void 
     double *s = (double *)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1));
     if (!s) { rc = ORC_ERR_NOMEM; break; }
 
-    for (int64_t h = 0; h < H; ++h) {
+    for (int64_t h = h_begin; h < h_end; ++h) {
       const int64_t kvh = h / group;            /* GQA: repeat_interleave order */
       const int64_t qoff = (b * H + h) * D;
       if (n == 0) {                             /* empty context: zero output */

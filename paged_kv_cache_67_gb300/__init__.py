@@ -1,0 +1,29 @@
+"""Paged KV-cache write and paged decode attention for one GB300 (sm_103a).
+
+A thin Python binding over the C ABI of ``include/pkv.h`` (``libpkv.so``,
+built in-tree by ``paged_kv_cache_67_gb300.build``).  The functions carry the
+C names and only marshal torch tensors into pointers and sizes: every step of
+the computation runs in the library's CUDA kernels.  There is no CPU
+fallback; if the library is missing or a call fails, an exception is raised.
+"""
+from __future__ import annotations
+
+from ._binding import (  # noqa: F401
+    FLAG_BLOCK_OUT_OF_RANGE,
+    FLAG_CONTEXT_NEGATIVE,
+    FLAG_CONTEXT_OVER_HINT,
+    FLAG_CONTEXT_TOO_LONG,
+    FLAG_SLOT_OUT_OF_RANGE,
+    FLAG_TIMEOUT,
+    PkvError,
+    DecodeWorkspace,
+    exported_symbols,
+    library_path,
+    load_library,
+    pkv_decode_attention,
+    pkv_decode_plan,
+    pkv_decode_workspace_size,
+    pkv_status_string,
+    pkv_version,
+    pkv_write,
+)

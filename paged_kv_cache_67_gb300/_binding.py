@@ -1,0 +1,196 @@
+"""ctypes binding of libpkv.so: argument marshalling only.
+
+Each function takes torch tensors, checks the shapes/dtypes/devices needed
+to fill the C arguments, and calls the C entry point of the same name on the
+caller's current CUDA stream (or the given one).  Status codes other than
+PKV_OK raise PkvError.  Memory is the caller's: nothing here allocates on
+the call path (DecodeWorkspace is a one-off helper that allocates the
+workspace buffer with torch, zero-filled).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import threading
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_PKG, "_build", "libpkv.so")
+_HEADER = os.path.join(os.path.dirname(_PKG), "include", "pkv.h")
+
+PKV_F32, PKV_BF16, PKV_F16 = 0, 1, 2
+_DT = {torch.float32: PKV_F32, torch.bfloat16: PKV_BF16, torch.float16: PKV_F16}
+
+FLAG_SLOT_OUT_OF_RANGE = 0x1
+FLAG_BLOCK_OUT_OF_RANGE = 0x2
+FLAG_CONTEXT_TOO_LONG = 0x4
+FLAG_CONTEXT_NEGATIVE = 0x8
+FLAG_CONTEXT_OVER_HINT = 0x10
+FLAG_TIMEOUT = 0x20
+
+_lock = threading.Lock()
+_lib = None
+
+
+class PkvError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: status {status} ({pkv_status_string(status)})")
+        self.status = status
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load_library():
+    """Load libpkv.so (raises if it has not been built: no fallback)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError(
+                f"{_LIB_PATH} is missing: build it with "
+                "`python -m paged_kv_cache_67_gb300.build` (nvcc, sm_103a)")
+        lib = ctypes.CDLL(_LIB_PATH)
+        vp, i64, c_int, c_size = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
+        lib.pkv_write.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, c_int, c_int, c_int,
+                                  c_int, vp, vp]
+        lib.pkv_write.restype = c_int
+        lib.pkv_decode_workspace_size.argtypes = [c_int] * 8
+        lib.pkv_decode_workspace_size.restype = c_size
+        lib.pkv_decode_plan.argtypes = [c_int] * 10 + [ctypes.POINTER(c_int), ctypes.POINTER(c_int)]
+        lib.pkv_decode_plan.restype = c_int
+        lib.pkv_decode_attention.argtypes = [vp, vp, vp, vp, vp, vp, c_int, c_int, c_int, c_int,
+                                             c_int, c_int, i64, ctypes.c_float, c_int, c_int,
+                                             c_int, vp, c_size, vp, vp]
+        lib.pkv_decode_attention.restype = c_int
+        lib.pkv_status_string.argtypes = [c_int]
+        lib.pkv_status_string.restype = ctypes.c_char_p
+        lib.pkv_version.argtypes = []
+        lib.pkv_version.restype = ctypes.c_char_p
+        _lib = lib
+        return lib
+
+
+def exported_symbols() -> list[str]:
+    """Names of the entry points include/pkv.h declares (PKV_API)."""
+    with open(_HEADER) as f:
+        text = f.read()
+    return re.findall(r"PKV_API\s+[\w\s\*]+?\b(pkv_\w+)\s*\(", text)
+
+
+def pkv_status_string(status: int) -> str:
+    return load_library().pkv_status_string(status).decode()
+
+
+def pkv_version() -> str:
+    return load_library().pkv_version().decode()
+
+
+def _stream_handle(stream, device) -> int:
+    if stream is None:
+        return torch.cuda.current_stream(device).cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _check(status: int, what: str):
+    if status != 0:
+        raise PkvError(status, what)
+
+
+def _require(cond: bool, msg: str):
+    if not cond:
+        raise ValueError(msg)
+
+
+def pkv_write(k_cache, v_cache, k, v, slot_mapping, err_flags=None, stream=None) -> None:
+    """write_kv in place: k_cache/v_cache [num_blocks, bs, KVH, D]; k, v
+    [T, KVH, D] (each token's row contiguous; the token stride may be
+    larger); slot_mapping [T] int64 with negative = padding."""
+    lib = load_library()
+    _require(k_cache.dim() == 4 and v_cache.shape == k_cache.shape, "caches must be [nb, bs, KVH, D]")
+    nb, bs, kvh, d = k_cache.shape
+    _require(k_cache.is_contiguous() and v_cache.is_contiguous(), "caches must be contiguous")
+    _require(k.dim() == 3 and v.shape == k.shape and k.shape[1:] == (kvh, d), "k, v must be [T, KVH, D]")
+    _require(k.stride(2) == 1 and k.stride(1) == d and v.stride(2) == 1 and v.stride(1) == d,
+             "each token's [KVH, D] row must be contiguous")
+    _require(k.dtype == v.dtype == k_cache.dtype == v_cache.dtype and k.dtype in _DT, "dtype mismatch")
+    _require(slot_mapping.dtype == torch.int64 and slot_mapping.is_contiguous()
+             and slot_mapping.numel() == k.shape[0], "slot_mapping must be contiguous int64 [T]")
+    dev = k_cache.device
+    _require(dev.type == "cuda" and all(t.device == dev for t in (v_cache, k, v, slot_mapping)),
+             "all tensors must be on the same CUDA device")
+    T = k.shape[0]
+    _check(lib.pkv_write(_ptr(k_cache), _ptr(v_cache), _ptr(k), _ptr(v), _ptr(slot_mapping), T,
+                         k.stride(0) if T > 0 else kvh * d, v.stride(0) if T > 0 else kvh * d, nb,
+                         bs, kvh, d, _DT[k.dtype], _ptr(err_flags), _stream_handle(stream, dev)),
+           "pkv_write")
+
+
+def pkv_decode_workspace_size(B, H, num_kv_heads, head_dim, block_size, max_blocks,
+                              max_context_len=0, partition_size=0) -> int:
+    return int(load_library().pkv_decode_workspace_size(B, H, num_kv_heads, head_dim, block_size,
+                                                        max_blocks, max_context_len, partition_size))
+
+
+def pkv_decode_plan(B, H, num_kv_heads, head_dim, block_size, max_blocks, max_context_len=0,
+                    partition_size=0, dtype=torch.bfloat16, num_sms=152):
+    """(partition_size, max_partitions, kernel) the library would use
+    (kernel 1 = TMA/tensor-core, 0 = CUDA-core); host only."""
+    mp, kern = ctypes.c_int(0), ctypes.c_int(0)
+    P = load_library().pkv_decode_plan(B, H, num_kv_heads, head_dim, block_size, max_blocks,
+                                       max_context_len, partition_size, _DT[dtype], num_sms,
+                                       ctypes.byref(mp), ctypes.byref(kern))
+    return P, mp.value, kern.value
+
+
+class DecodeWorkspace:
+    """A zero-filled device workspace sized for pkv_decode_attention."""
+
+    def __init__(self, B, H, num_kv_heads, head_dim, block_size, max_blocks, max_context_len=0,
+                 partition_size=0, device="cuda"):
+        self.nbytes = pkv_decode_workspace_size(B, H, num_kv_heads, head_dim, block_size,
+                                                max_blocks, max_context_len, partition_size)
+        self.buffer = torch.zeros(max(self.nbytes, 256), dtype=torch.uint8, device=device)
+
+
+def pkv_decode_attention(out, q, k_cache, v_cache, block_tables, context_lens, scale: float,
+                         max_context_len: int = 0, partition_size: int = 0, workspace=None,
+                         err_flags=None, stream=None):
+    """Paged decode attention into ``out`` [B, H, D] (returned)."""
+    lib = load_library()
+    _require(q.dim() == 3 and out.shape == q.shape, "q and out must be [B, H, D]")
+    B, H, D = q.shape
+    _require(k_cache.dim() == 4 and v_cache.shape == k_cache.shape and k_cache.shape[3] == D,
+             "caches must be [nb, bs, KVH, D]")
+    nb, bs, kvh, _ = k_cache.shape
+    for t in (out, q, k_cache, v_cache, block_tables, context_lens):
+        _require(t.is_contiguous(), "tensors must be contiguous")
+    _require(q.dtype == out.dtype == k_cache.dtype == v_cache.dtype and q.dtype in _DT, "dtype mismatch")
+    _require(block_tables.dtype == torch.int32 and block_tables.dim() == 2 and block_tables.shape[0] == B,
+             "block_tables must be int32 [B, max_blocks]")
+    _require(context_lens.dtype == torch.int32 and context_lens.shape == (B,), "context_lens must be int32 [B]")
+    dev = q.device
+    _require(dev.type == "cuda" and all(t.device == dev for t in (out, k_cache, v_cache, block_tables,
+                                                                   context_lens)),
+             "all tensors must be on the same CUDA device")
+    ws_ptr, ws_bytes = None, 0
+    if workspace is not None:
+        buf = workspace.buffer if isinstance(workspace, DecodeWorkspace) else workspace
+        ws_ptr, ws_bytes = _ptr(buf), buf.numel() * buf.element_size()
+    _check(lib.pkv_decode_attention(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+                                    _ptr(block_tables), _ptr(context_lens), B, H, kvh, D, bs,
+                                    block_tables.shape[1], nb, float(scale), _DT[q.dtype],
+                                    int(max_context_len), int(partition_size), ws_ptr, ws_bytes,
+                                    _ptr(err_flags), _stream_handle(stream, dev)),
+           "pkv_decode_attention")
+    return out

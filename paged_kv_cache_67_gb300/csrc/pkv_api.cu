@@ -1,0 +1,240 @@
+// pkv_api.cu -- the C ABI declared in include/pkv.h: host-side argument
+// checks, the decode plan (kernel choice, partition size, workspace
+// layout) and the launches.  Nothing here allocates device memory.
+#include <math.h>
+#include <string.h>
+
+#include "pkv_device.cuh"
+#include "pkv_internal.h"
+
+namespace pkv {
+
+size_t simt_smem_bytes(int D, int GH);
+size_t tc_smem_bytes(int D, int stages);
+
+static int round_up(long long x, int m) { return (int)(((x + m - 1) / m) * m); }
+static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+bool tc_eligible(pkv_dtype dt, int D, int bs) {
+  return (dt == PKV_BF16 || dt == PKV_F16) && (D == 64 || D == 128 || D == 192 || D == 256) &&
+         bs % 16 == 0;
+}
+
+// Context capacity the grid must cover: the host hint, else the table width.
+static long long context_cap(int bs, int max_blocks, int max_context_len) {
+  const long long table = (long long)max_blocks * bs;
+  long long cap = max_context_len > 0 ? (long long)max_context_len : table;
+  if (cap > table) cap = table;
+  return cap < 1 ? 1 : cap;
+}
+
+// Smallest partition the automatic choice uses for this capacity: at least
+// 64 tokens and at most kMaxAutoParts partitions per sequence.
+static int auto_partition_floor(long long cap) {
+  const int p = round_up((cap + kMaxAutoParts - 1) / kMaxAutoParts, 16);
+  return p < 64 ? 64 : p;
+}
+
+static int tc_stages(int D) { return D <= 64 ? 6 : (D <= 128 ? 3 : (D <= 192 ? 2 : 3)); }
+
+bool make_plan(int B, int H, int KVH, int D, int bs, int max_blocks, int max_context_len,
+               int partition_size, pkv_dtype dt, int num_sms, bool aligned16, DecodePlan *plan) {
+  if (B < 0 || H <= 0 || KVH <= 0 || H % KVH != 0 || D <= 0 || D > 512 || bs <= 0 ||
+      max_blocks < 0 || partition_size < 0 || partition_size % 16 != 0 || max_context_len < 0)
+    return false;
+  if (dt != PKV_F32 && dt != PKV_BF16 && dt != PKV_F16) return false;
+  const int G = H / KVH;
+  DecodePlan p;
+  p.kernel = (tc_eligible(dt, D, bs) && aligned16) ? 1 : 0;
+  p.heads_per_cta = p.kernel ? kTcHeads : (D <= 256 ? 4 : 2);
+  p.gchunks = (G + p.heads_per_cta - 1) / p.heads_per_cta;
+  p.threads = 128;
+  const long long cap = context_cap(bs, max_blocks, max_context_len);
+  if (partition_size > 0) {
+    p.P = partition_size;
+  } else {
+    // Enough CTAs for about four per resident slot when contexts average
+    // half the capacity; never below the floor.
+    const long long units = (long long)B * KVH * p.gchunks;
+    const int per_sm = p.kernel ? (D <= 128 ? 2 : 1) : 4;
+    const long long slots = (long long)(num_sms > 0 ? num_sms : 1) * per_sm;
+    long long parts = units > 0 ? (8 * slots + units - 1) / units : 1;
+    if (parts < 1) parts = 1;
+    int P = round_up((cap + parts - 1) / parts, 16);
+    const int floor_p = auto_partition_floor(cap);
+    if (P < floor_p) P = floor_p;
+    if (P < 256 && cap > 256) P = 256;
+    p.P = P;
+  }
+  const long long mp = (cap + p.P - 1) / p.P;
+  if (mp > 0x7fffffffLL) return false;
+  p.max_parts = (int)(mp < 1 ? 1 : mp);
+  p.stages = p.kernel ? tc_stages(D) : 0;
+  p.smem_bytes = p.kernel ? tc_smem_bytes(D, p.stages) : simt_smem_bytes(D, p.heads_per_cta);
+  *plan = p;
+  return true;
+}
+
+size_t workspace_bytes_for(int B, int H, int D, int max_parts) {
+  if (max_parts <= 1) return 0;
+  const size_t rows = (size_t)B * H;
+  return align256(rows * sizeof(int)) + 2 * align256(rows * max_parts * sizeof(float)) +
+         rows * max_parts * (size_t)D * sizeof(float);
+}
+
+static int sm_count_cached() {
+  static int counts[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (dev >= 64) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    return n;
+  }
+  if (counts[dev] == 0) cudaDeviceGetAttribute(&counts[dev], cudaDevAttrMultiProcessorCount, dev);
+  return counts[dev];
+}
+
+static int elem_size(pkv_dtype dt) { return dt == PKV_F32 ? 4 : 2; }
+
+}  // namespace pkv
+
+using namespace pkv;
+
+extern "C" {
+
+PKV_API pkv_status pkv_write(void *k_cache, void *v_cache, const void *k, const void *v,
+                             const int64_t *slot_mapping, int64_t num_tokens,
+                             int64_t k_token_stride, int64_t v_token_stride, int64_t num_blocks,
+                             int block_size, int num_kv_heads, int head_dim, pkv_dtype dt,
+                             int *err_flags, pkv_stream_t stream) {
+  if (num_tokens < 0 || num_blocks < 0 || block_size <= 0 || num_kv_heads <= 0 || head_dim <= 0)
+    return PKV_ERR_INVALID_ARG;
+  if (dt != PKV_F32 && dt != PKV_BF16 && dt != PKV_F16) return PKV_ERR_INVALID_ARG;
+  const int64_t row = (int64_t)num_kv_heads * head_dim;
+  if (k_token_stride < row || v_token_stride < row) return PKV_ERR_INVALID_ARG;
+  if (num_tokens == 0) return PKV_OK;
+  if (!k_cache || !v_cache || !k || !v || !slot_mapping) return PKV_ERR_INVALID_ARG;
+  return launch_write(k_cache, v_cache, k, v, slot_mapping, num_tokens, k_token_stride,
+                      v_token_stride, num_blocks, block_size, num_kv_heads, head_dim,
+                      elem_size(dt), err_flags, reinterpret_cast<cudaStream_t>(stream));
+}
+
+PKV_API size_t pkv_decode_workspace_size(int B, int H, int num_kv_heads, int head_dim,
+                                         int block_size, int max_blocks, int max_context_len,
+                                         int partition_size) {
+  if (B < 0 || H <= 0 || num_kv_heads <= 0 || H % num_kv_heads != 0 || head_dim <= 0 ||
+      head_dim > 512 || block_size <= 0 || max_blocks < 0 || max_context_len < 0 ||
+      partition_size < 0 || partition_size % 16 != 0)
+    return 0;
+  const long long cap = context_cap(block_size, max_blocks, max_context_len);
+  const int P = partition_size > 0 ? partition_size : auto_partition_floor(cap);
+  const long long parts = (cap + P - 1) / P;
+  if (parts > 0x7fffffffLL) return 0;
+  return workspace_bytes_for(B, H, head_dim, (int)parts);
+}
+
+PKV_API int pkv_decode_plan(int B, int H, int num_kv_heads, int head_dim, int block_size,
+                            int max_blocks, int max_context_len, int partition_size, pkv_dtype dt,
+                            int num_sms, int *max_partitions, int *kernel) {
+  DecodePlan p;
+  if (!make_plan(B, H, num_kv_heads, head_dim, block_size, max_blocks, max_context_len,
+                 partition_size, dt, num_sms, true, &p))
+    return 0;
+  if (max_partitions) *max_partitions = p.max_parts;
+  if (kernel) *kernel = p.kernel;
+  return p.P;
+}
+
+PKV_API pkv_status pkv_decode_attention(void *out, const void *q, const void *k_cache,
+                                        const void *v_cache, const int32_t *block_tables,
+                                        const int32_t *context_lens, int B, int H,
+                                        int num_kv_heads, int head_dim, int block_size,
+                                        int max_blocks, int64_t num_blocks, float scale,
+                                        pkv_dtype dt, int max_context_len, int partition_size,
+                                        void *workspace, size_t workspace_bytes, int *err_flags,
+                                        pkv_stream_t stream) {
+  if (B < 0 || B > 65535 || H <= 0 || H > 65535 || num_kv_heads <= 0 || H % num_kv_heads != 0 ||
+      head_dim <= 0 || block_size <= 0 || max_blocks < 0 || num_blocks < 0 ||
+      num_blocks > 0x7fffffffLL || max_context_len < 0 || partition_size < 0 ||
+      partition_size % 16 != 0)
+    return PKV_ERR_INVALID_ARG;
+  if (dt != PKV_F32 && dt != PKV_BF16 && dt != PKV_F16) return PKV_ERR_INVALID_ARG;
+  if (head_dim > 512) return PKV_ERR_UNSUPPORTED;
+  if (B == 0) return PKV_OK;
+  if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens)
+    return PKV_ERR_INVALID_ARG;
+  const uintptr_t el = (uintptr_t)elem_size(dt);
+  const void *ptrs[4] = {out, q, k_cache, v_cache};
+  bool aligned16 = true;
+  for (const void *p : ptrs) {
+    if (reinterpret_cast<uintptr_t>(p) % el) return PKV_ERR_INVALID_ARG;
+    aligned16 = aligned16 && (reinterpret_cast<uintptr_t>(p) % 16 == 0);
+  }
+  if (reinterpret_cast<uintptr_t>(block_tables) % 4 || reinterpret_cast<uintptr_t>(context_lens) % 4)
+    return PKV_ERR_INVALID_ARG;
+
+  const int sms = sm_count_cached();
+  if (sms <= 0) return PKV_ERR_CUDA;
+  DecodePlan plan;
+  if (!make_plan(B, H, num_kv_heads, head_dim, block_size, max_blocks, max_context_len,
+                 partition_size, dt, sms, aligned16, &plan))
+    return PKV_ERR_INVALID_ARG;
+  if ((long long)num_kv_heads * plan.gchunks > 65535) return PKV_ERR_UNSUPPORTED;
+
+  DecodeArgs a;
+  memset(&a, 0, sizeof a);
+  a.out = out;
+  a.q = q;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.tables = block_tables;
+  a.lens = context_lens;
+  a.err = err_flags;
+  a.num_blocks = num_blocks;
+  a.B = B;
+  a.H = H;
+  a.KVH = num_kv_heads;
+  a.D = head_dim;
+  a.G = H / num_kv_heads;
+  a.bs = block_size;
+  a.max_blocks = max_blocks;
+  a.heads_per_cta = plan.heads_per_cta;
+  a.gchunks = plan.gchunks;
+  a.P = plan.P;
+  a.max_parts = plan.max_parts;
+  a.stages = plan.stages;
+  a.scale_log2 = scale * kLog2e;
+
+  const size_t need = workspace_bytes_for(B, H, head_dim, plan.max_parts);
+  if (need > 0) {
+    if (!workspace || workspace_bytes < need || reinterpret_cast<uintptr_t>(workspace) % 256)
+      return PKV_ERR_WORKSPACE;
+    const size_t rows = (size_t)B * H;
+    char *ws = static_cast<char *>(workspace);
+    a.ws_cnt = reinterpret_cast<int *>(ws);
+    ws += align256(rows * sizeof(int));
+    a.ws_m = reinterpret_cast<float *>(ws);
+    ws += align256(rows * plan.max_parts * sizeof(float));
+    a.ws_l = reinterpret_cast<float *>(ws);
+    ws += align256(rows * plan.max_parts * sizeof(float));
+    a.ws_o = reinterpret_cast<float *>(ws);
+  }
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  return plan.kernel ? launch_decode_tc(a, plan, dt, s) : launch_decode_simt(a, plan, dt, s);
+}
+
+PKV_API const char *pkv_status_string(pkv_status status) {
+  switch (status) {
+    case PKV_OK: return "ok";
+    case PKV_ERR_INVALID_ARG: return "invalid argument";
+    case PKV_ERR_UNSUPPORTED: return "unsupported shape or dtype";
+    case PKV_ERR_CUDA: return "CUDA error";
+    case PKV_ERR_WORKSPACE: return "workspace missing or too small";
+  }
+  return "unknown status";
+}
+
+PKV_API const char *pkv_version(void) { return "pkv 0.1 (sm_103a)"; }
+
+}  // extern "C"

@@ -1,0 +1,324 @@
+// pkv_device.cuh -- device-side building blocks shared by the decode kernels:
+// PTX wrappers (mbarrier, TMA, ldmatrix, mma.sync, ex2), bounded waits, the
+// per-launch argument block and the end-of-partition epilogue (direct
+// output, or partial results + log-sum-exp merge by the last CTA).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "pkv.h"
+
+namespace pkv {
+
+constexpr float kLog2e = 1.4426950408889634f;
+// A wait on an asynchronous copy gives up after this long (the copies take
+// microseconds); the kernel then reports PKV_FLAG_TIMEOUT and winds down.
+constexpr unsigned long long kWaitLimitNs = 500ull * 1000ull * 1000ull;
+
+// Everything a decode launch needs, passed by value.
+struct DecodeArgs {
+  void *out;
+  const void *q;
+  const void *k_cache;   // used by the CUDA-core kernel (the TMA kernel uses tensor maps)
+  const void *v_cache;
+  const int32_t *tables;
+  const int32_t *lens;
+  float *ws_m;           // [B][H][max_parts]   running max (log2 units)
+  float *ws_l;           // [B][H][max_parts]   sum of weights
+  float *ws_o;           // [B][H][max_parts][D] weighted sum of V rows (unnormalised)
+  int *ws_cnt;           // [B][heads_chunks]    finished-partition counters
+  int *err;
+  long long num_blocks;
+  int B, H, KVH, D, G, bs, max_blocks;
+  int heads_per_cta;     // query heads one CTA serves (<= its kernel's maximum)
+  int gchunks;           // ceil(G / heads_per_cta)
+  int P;                 // partition size in tokens (multiple of 16)
+  int max_parts;         // partitions the grid covers per sequence (gridDim.x)
+  int stages;            // pipeline depth per warp (TMA kernel)
+  float scale_log2;      // scale * log2(e): scores are kept in log2 units
+};
+
+__device__ __forceinline__ void raise_flag(int *err, int bit) {
+  if (err) atomicOr(err, bit);
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ unsigned long long global_timer_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// 2^x on the SFU (ex2.approx, flush-to-zero); exp2(-inf) = 0.
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// ------------------------------------------------------------ mbarrier + TMA
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+               : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait for the phase with the given parity to complete; false after
+// kWaitLimitNs without completion.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+  }
+  return true;
+}
+
+// Tiled 4-D TMA load global -> shared, completion counted on `bar`.
+__device__ __forceinline__ void tma_load_4d(void *dst, const CUtensorMap *map, uint64_t *bar,
+                                            int c0, int c1, int c2, int c3, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%3, %4, %5, %6}], [%2], %7;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2),
+      "r"(c3), "l"(policy)
+      : "memory");
+}
+
+// L2 policy for data read exactly once (K/V rows): evict first.
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// ------------------------------------------------------ ldmatrix + mma.sync
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
+                                        uint32_t &r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t &r0, uint32_t &r1,
+                                              uint32_t &r2, uint32_t &r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+template <typename T>
+struct MmaOp;
+
+template <>
+struct MmaOp<__nv_bfloat16> {
+  __device__ __forceinline__ static void run(float c[4], const uint32_t a[4], uint32_t b0,
+                                             uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
+        "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+  }
+  // Two fp32 -> one packed pair (lo in the low half), round to nearest even;
+  // also returns the rounded values' sum so weights and their total agree.
+  __device__ __forceinline__ static uint32_t pack(float lo, float hi, float &sum) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    float2 f = __bfloat1622float2(v);
+    sum += f.x + f.y;
+    return *reinterpret_cast<uint32_t *>(&v);
+  }
+};
+
+template <>
+struct MmaOp<__half> {
+  __device__ __forceinline__ static void run(float c[4], const uint32_t a[4], uint32_t b0,
+                                             uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, "
+        "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+  }
+  __device__ __forceinline__ static uint32_t pack(float lo, float hi, float &sum) {
+    __half2 v = __floats2half2_rn(lo, hi);
+    float2 f = __half22float2(v);
+    sum += f.x + f.y;
+    return *reinterpret_cast<uint32_t *>(&v);
+  }
+};
+
+// --------------------------------------------------------- element access
+
+template <typename T>
+__device__ __forceinline__ float to_f32(T x);
+template <>
+__device__ __forceinline__ float to_f32<float>(float x) { return x; }
+template <>
+__device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 x) {
+  return __bfloat162float(x);
+}
+template <>
+__device__ __forceinline__ float to_f32<__half>(__half x) { return __half2float(x); }
+
+template <typename T>
+__device__ __forceinline__ T from_f32(float x);
+template <>
+__device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <>
+__device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
+  return __float2bfloat16_rn(x);
+}
+template <>
+__device__ __forceinline__ __half from_f32<__half>(float x) { return __float2half_rn(x); }
+
+// ------------------------------------------------------ sequence bookkeeping
+
+// Context length of sequence b after the device-side checks: negative -> 0,
+// longer than the table -> clamped.  Flags are raised by partition 0 only.
+__device__ __forceinline__ int checked_len(const DecodeArgs &a, int b, bool report) {
+  int n = __ldg(a.lens + b);
+  if (n < 0) {
+    if (report) raise_flag(a.err, PKV_FLAG_CONTEXT_NEGATIVE);
+    n = 0;
+  }
+  const long long cap = (long long)a.max_blocks * a.bs;
+  if ((long long)n > cap) {
+    if (report) raise_flag(a.err, PKV_FLAG_CONTEXT_TOO_LONG);
+    n = (int)cap;
+  }
+  return n;
+}
+
+// Physical block of logical block lb of sequence b; an entry outside
+// [0, num_blocks) is reported and replaced by block 0 (always in bounds).
+__device__ __forceinline__ int checked_block(const DecodeArgs &a, int b, int lb) {
+  const int phys = __ldg(a.tables + (size_t)b * a.max_blocks + lb);
+  if (phys < 0 || (long long)phys >= a.num_blocks) {
+    raise_flag(a.err, PKV_FLAG_BLOCK_OUT_OF_RANGE);
+    return 0;
+  }
+  return phys;
+}
+
+// ----------------------------------------------------------------- epilogue
+//
+// Called by every thread of the CTA once the partition [part*P, ...) of
+// sequence b has been reduced to, for each of its nh query heads r:
+//   s_m[r]  running max of the log2-unit scores,
+//   s_l[r]  sum of 2^(score - s_m[r]),
+//   s_o[r*ostride + d]  sum of 2^(score - s_m[r]) * V[d].
+// With one partition the output row is s_o / s_l.  Otherwise the partials go
+// to the workspace; the CTA that finishes a (sequence, head group) last
+// merges all partitions:  M = max_p m_p,  L = sum_p l_p 2^(m_p - M),
+// out = sum_p o_p 2^(m_p - M) / L, and resets the counter to zero.
+template <typename T>
+__device__ void finish_partition(const DecodeArgs &a, int b, int head0, int nh, int part,
+                                 int nparts, const float *s_m, const float *s_l,
+                                 const float *s_o, int ostride, int *s_scratch) {
+  const int tid = threadIdx.x, nthr = blockDim.x;
+  const int D = a.D;
+  T *out = reinterpret_cast<T *>(a.out);
+  if (nparts == 1) {
+    for (int i = tid; i < nh * D; i += nthr) {
+      const int r = i / D, d = i - r * D;
+      const float v = s_o[r * ostride + d] / s_l[r];
+      out[((size_t)b * a.H + head0 + r) * D + d] = from_f32<T>(v);
+    }
+    return;
+  }
+  const size_t row0 = (size_t)b * a.H + head0;  // first (b, h) row of this CTA
+  for (int r = tid; r < nh; r += nthr) {
+    a.ws_m[(row0 + r) * a.max_parts + part] = s_m[r];
+    a.ws_l[(row0 + r) * a.max_parts + part] = s_l[r];
+  }
+  for (int i = tid; i < nh * D; i += nthr) {
+    const int r = i / D, d = i - r * D;
+    a.ws_o[((row0 + r) * a.max_parts + part) * D + d] = s_o[r * ostride + d];
+  }
+  __threadfence();
+  __syncthreads();
+  int *counter = a.ws_cnt + (size_t)b * gridDim.y + blockIdx.y;
+  if (tid == 0) {
+    const int prev = atomicAdd(counter, 1);
+    s_scratch[0] = (prev == nparts - 1);
+  }
+  __syncthreads();
+  if (!s_scratch[0]) return;
+  __threadfence();
+  // Last CTA: per-row max and total, then the merged rows.
+  float *s_M = reinterpret_cast<float *>(s_scratch + 1);
+  float *s_invL = s_M + nh;
+  const int warp = tid >> 5, lane = tid & 31, nwarps = nthr >> 5;
+  for (int r = warp; r < nh; r += nwarps) {
+    const float *pm = a.ws_m + (row0 + r) * a.max_parts;
+    const float *pl = a.ws_l + (row0 + r) * a.max_parts;
+    float M = -INFINITY;
+    for (int p = lane; p < nparts; p += 32) M = fmaxf(M, __ldcg(pm + p));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    float L = 0.f;
+    for (int p = lane; p < nparts; p += 32) L += __ldcg(pl + p) * fast_exp2(__ldcg(pm + p) - M);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+    if (lane == 0) {
+      s_M[r] = M;
+      s_invL[r] = 1.f / L;
+    }
+  }
+  __syncthreads();
+  for (int i = tid; i < nh * D; i += nthr) {
+    const int r = i / D, d = i - r * D;
+    const float *pm = a.ws_m + (row0 + r) * a.max_parts;
+    const float *po = a.ws_o + (row0 + r) * a.max_parts * D + d;
+    const float M = s_M[r];
+    float acc = 0.f;
+    for (int p = 0; p < nparts; ++p) acc += __ldcg(po + (size_t)p * D) * fast_exp2(__ldcg(pm + p) - M);
+    out[(row0 + r) * D + d] = from_f32<T>(acc * s_invL[r]);
+  }
+  if (tid == 0) *counter = 0;  // every partition has arrived: ready for the next call
+}
+
+// Zero output rows for an empty context (partition 0 only).
+template <typename T>
+__device__ void zero_rows(const DecodeArgs &a, int b, int head0, int nh) {
+  T *out = reinterpret_cast<T *>(a.out);
+  for (int i = threadIdx.x; i < nh * a.D; i += blockDim.x)
+    out[((size_t)b * a.H + head0) * a.D + i] = from_f32<T>(0.f);
+}
+
+}  // namespace pkv

@@ -1,0 +1,47 @@
+// pkv_internal.h -- host-side declarations shared by the translation units of
+// libpkv (not part of the public C ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "pkv.h"
+
+namespace pkv {
+
+// Which decode kernel runs and how the context is partitioned.
+struct DecodePlan {
+  int kernel;          // 1: TMA + tensor-core kernel, 0: CUDA-core kernel
+  int P;               // partition size in tokens (multiple of 16)
+  int max_parts;       // partitions per sequence the grid covers
+  int heads_per_cta;   // query heads served by one CTA
+  int gchunks;         // CTAs per KV head (ceil(G / heads_per_cta))
+  int stages;          // TMA pipeline depth per warp
+  int threads;         // threads per CTA
+  size_t smem_bytes;   // dynamic shared memory per CTA
+};
+
+// Heads one tensor-core CTA serves (the M = 16 rows of one mma tile).
+constexpr int kTcHeads = 16;
+// Partitions per sequence the automatic partition size never exceeds.
+constexpr int kMaxAutoParts = 64;
+
+bool tc_eligible(pkv_dtype dt, int D, int bs);
+// Fills *plan; returns false for sizes no kernel handles.
+bool make_plan(int B, int H, int KVH, int D, int bs, int max_blocks, int max_context_len,
+               int partition_size, pkv_dtype dt, int num_sms, bool aligned16, DecodePlan *plan);
+size_t workspace_bytes_for(int B, int H, int D, int max_parts);
+
+pkv_status launch_write(void *k_cache, void *v_cache, const void *k, const void *v,
+                        const int64_t *slot_mapping, int64_t T, int64_t k_stride, int64_t v_stride,
+                        int64_t num_blocks, int bs, int KVH, int D, int elem, int *err,
+                        cudaStream_t stream);
+
+struct DecodeArgs;
+pkv_status launch_decode_simt(const DecodeArgs &a, const DecodePlan &plan, pkv_dtype dt,
+                              cudaStream_t stream);
+pkv_status launch_decode_tc(const DecodeArgs &a, const DecodePlan &plan, pkv_dtype dt,
+                            cudaStream_t stream);
+
+}  // namespace pkv

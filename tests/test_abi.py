@@ -1,0 +1,110 @@
+"""The C ABI on the CPU: the library builds and loads, exports every entry
+point include/pkv.h declares, and its host-only logic (argument checks,
+workspace sizes, the decode plan) behaves.  No compute call needs a GPU."""
+import ctypes
+import subprocess
+
+import pytest
+
+from paged_kv_cache_67_gb300 import build as libbuild
+
+
+@pytest.fixture(scope="module")
+def pkv():
+    libbuild.build()
+    import paged_kv_cache_67_gb300 as m
+    m.load_library()
+    return m
+
+
+def test_every_declared_symbol_is_exported(pkv):
+    names = pkv.exported_symbols()
+    assert set(names) >= {"pkv_write", "pkv_decode_attention", "pkv_decode_workspace_size",
+                          "pkv_decode_plan", "pkv_status_string", "pkv_version"}
+    lib = pkv.load_library()
+    for n in names:
+        assert hasattr(lib, n), n
+    dyn = subprocess.run(["nm", "-D", "--defined-only", pkv.library_path()], capture_output=True,
+                         text=True, check=True).stdout
+    exported = {line.split()[-1] for line in dyn.splitlines() if " T " in line}
+    assert set(names) <= exported
+    # only the C ABI is visible
+    assert all(s.startswith("pkv_") for s in exported), sorted(exported)
+
+
+def test_status_strings_and_version(pkv):
+    assert pkv.pkv_status_string(0) == "ok"
+    assert "workspace" in pkv.pkv_status_string(4)
+    assert pkv.pkv_status_string(99) == "unknown status"
+    assert "sm_103a" in pkv.pkv_version()
+
+
+def test_workspace_size(pkv):
+    # one partition covers everything -> no workspace
+    assert pkv.pkv_decode_workspace_size(4, 8, 2, 64, 16, 4, 0, 64) == 0
+    # rows * parts * (D + 2) floats + counters, each region 256-aligned
+    B, H, D, P, cap = 3, 8, 64, 64, 1000
+    parts = -(-cap // P)
+    rows = B * H
+    al = lambda x: (x + 255) // 256 * 256
+    want = al(rows * 4) + 2 * al(rows * parts * 4) + rows * parts * D * 4
+    assert pkv.pkv_decode_workspace_size(B, H, 2, D, 16, 100, cap, P) == want
+    # invalid sizes -> 0
+    assert pkv.pkv_decode_workspace_size(4, 6, 4, 64, 16, 8, 0, 0) == 0   # H % KVH
+    assert pkv.pkv_decode_workspace_size(4, 8, 2, 64, 16, 8, 0, 24) == 0  # P % 16
+    # auto mode: never more than 64 partitions per sequence
+    auto = pkv.pkv_decode_workspace_size(8, 32, 8, 128, 16, 2048, 0, 0)
+    assert auto == pkv.pkv_decode_workspace_size(8, 32, 8, 128, 16, 2048, 0, 512)
+
+
+def test_plan(pkv):
+    import torch
+    P, mp, kern = pkv.pkv_decode_plan(64, 32, 8, 128, 16, 256, 4096, 0, torch.bfloat16, 152)
+    assert kern == 1 and P % 16 == 0 and P >= 256 and mp == -(-4096 // P)
+    # the workspace sized in auto mode always fits the automatic plan
+    for B, H, KVH, D, bs, mb, cap in ((64, 32, 8, 128, 16, 256, 4096), (8, 32, 8, 128, 16, 2048, 32768),
+                                      (128, 16, 1, 256, 32, 256, 8192), (1, 4, 4, 64, 16, 100, 0)):
+        P, mp, _ = pkv.pkv_decode_plan(B, H, KVH, D, bs, mb, cap, 0, torch.bfloat16, 152)
+        assert mp <= 64
+        ws = pkv.pkv_decode_workspace_size(B, H, KVH, D, bs, mb, cap, 0)
+        rows = B * H
+        al = lambda x: (x + 255) // 256 * 256
+        need = 0 if mp <= 1 else al(rows * 4) + 2 * al(rows * mp * 4) + rows * mp * D * 4
+        assert ws >= need
+    # fp32, odd head_dim or block size not a multiple of 16 -> CUDA-core kernel
+    assert pkv.pkv_decode_plan(4, 4, 2, 64, 16, 8, 0, 0, torch.float32)[2] == 0
+    assert pkv.pkv_decode_plan(4, 4, 2, 96, 16, 8, 0, 0, torch.bfloat16)[2] == 0
+    assert pkv.pkv_decode_plan(4, 4, 2, 128, 8, 8, 0, 0, torch.bfloat16)[2] == 0
+    assert pkv.pkv_decode_plan(4, 4, 2, 128, 32, 8, 0, 0, torch.float16)[2] == 1
+    # explicit partition size is honoured
+    assert pkv.pkv_decode_plan(4, 4, 2, 128, 16, 64, 0, 48, torch.bfloat16)[:2] == (48, -(-1024 // 48))
+    # invalid -> 0
+    assert pkv.pkv_decode_plan(4, 6, 4, 128, 16, 8, 0, 0, torch.bfloat16)[0] == 0
+
+
+def test_host_side_argument_errors(pkv):
+    """Argument errors come back as a status before any CUDA call (so they
+    are checkable without a GPU)."""
+    lib = pkv.load_library()
+    null = None
+    # pkv_write: negative token count, bad sizes, stride shorter than a row
+    assert lib.pkv_write(null, null, null, null, null, -1, 8, 8, 4, 16, 1, 8, 1, null, null) == 1
+    assert lib.pkv_write(null, null, null, null, null, 4, 8, 8, 4, 0, 1, 8, 1, null, null) == 1
+    assert lib.pkv_write(null, null, null, null, null, 4, 7, 8, 4, 16, 1, 8, 1, null, null) == 1
+    assert lib.pkv_write(null, null, null, null, null, 4, 8, 8, 4, 16, 1, 8, 7, null, null) == 1
+    # zero tokens: nothing to do
+    assert lib.pkv_write(null, null, null, null, null, 0, 8, 8, 4, 16, 1, 8, 1, null, null) == 0
+    # NULL pointers with work to do
+    assert lib.pkv_write(null, null, null, null, null, 3, 8, 8, 4, 16, 1, 8, 1, null, null) == 1
+    dec = lambda **kw: lib.pkv_decode_attention(
+        kw.get("out"), kw.get("q"), kw.get("k"), kw.get("v"), kw.get("t"), kw.get("l"),
+        kw.get("B", 2), kw.get("H", 4), kw.get("KVH", 2), kw.get("D", 64), kw.get("bs", 16),
+        kw.get("mb", 4), kw.get("nb", 8), ctypes.c_float(0.125), kw.get("dt", 1), 0,
+        kw.get("P", 0), None, 0, None, None)
+    assert dec(H=6, KVH=4) == 1          # H % KVH
+    assert dec(bs=0) == 1
+    assert dec(P=24) == 1                # partition not a multiple of 16
+    assert dec(dt=9) == 1
+    assert dec(D=1024) == 2              # head_dim above 512
+    assert dec(B=0) == 0                 # empty batch: nothing to do
+    assert dec() == 1                    # NULL pointers
