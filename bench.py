@@ -45,6 +45,19 @@ FALLBACK_HBM_GBS = 6800.0
 
 # ------------------------------------------------------------------ helpers
 
+def config_block(dec_bytes=None, wr_bytes=None, world=1):
+    c = {"workload": (f"{WORKLOAD}: B=64 H=32 KVH=8 D=128 block_size=16, context_lens "
+                      "U[512,4096], shuffled blocks from a 1.25x pool, garbage table tails, "
+                      "q/k/v~N(0,1) bf16; step = pkv_write of 64 new tokens + "
+                      "pkv_decode_attention"),
+         "parallelism": f"{world} independent replica batch(es), no collective"}
+    if dec_bytes is not None:
+        c["l2"] = f"inputs larger than L2 ({dec_bytes / 1e6:.0f} MB of K/V per step, no flush)"
+        c["decode_bytes_per_step"] = dec_bytes
+        c["write_bytes_per_step"] = wr_bytes
+    return c
+
+
 def hbm_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -237,8 +250,7 @@ def run_reference(args, world, rank):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(dt / max(args.steps, 1) * 1e3, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": f"{WORKLOAD}: B=64 H=32 KVH=8 D=128 bs=16 n~U[512,4096] bf16 inputs",
-                   "sample": f"{threads} (sequence, KV head) units per step"},
+        "config": dict(config_block(), sample=f"{threads} (sequence, KV head) units per step"),
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads,
                          "kind": "oracle",
                          "sample": f"{threads} (sequence, KV head) units per step, rotating"},
@@ -274,6 +286,7 @@ def run_gpu(args, world, rank, local):
     dec_bytes = wl.decode_bytes(inp.context_lens, cfg.B, cfg.H, cfg.KVH, cfg.D, cfg.bs, elem)
     wr_bytes = wl.write_bytes(wb.slot_mapping, cfg.KVH, cfg.D, elem)
     step_bytes = dec_bytes + wr_bytes
+    peak, peak_kind = hbm_peak()
 
     def write():
         pkv.pkv_write(inp.k_cache, inp.v_cache, wb.k, wb.v, wb.slot_mapping, err_flags=err,
@@ -284,41 +297,47 @@ def run_gpu(args, world, rank, local):
                                  max_context_len=max_ctx, workspace=ws, err_flags=err,
                                  stream=stream)
 
-    # write_kv on a bulk fill (every context token, ~147k tokens): GB/s
-    bulk = wl.make_bulk_fill(inp, seed=99 + rank, device=dev)
-    bulk_bytes = wl.write_bytes(bulk.slot_mapping, cfg.KVH, cfg.D, elem)
+    extra = {}
+    if not args.only_decode:
+        # write_kv on a bulk fill (every context token, ~147k tokens): GB/s
+        bulk = wl.make_bulk_fill(inp, seed=99 + rank, device=dev)
+        bulk_bytes = wl.write_bytes(bulk.slot_mapping, cfg.KVH, cfg.D, elem)
 
-    def bulk_write():
-        pkv.pkv_write(inp.k_cache, inp.v_cache, bulk.k, bulk.v, bulk.slot_mapping, err_flags=err,
-                      stream=stream)
+        def bulk_write():
+            pkv.pkv_write(inp.k_cache, inp.v_cache, bulk.k, bulk.v, bulk.slot_mapping,
+                          err_flags=err, stream=stream)
 
-    for _ in range(3):
-        bulk_write()
-    torch.cuda.synchronize()
-    reps = 20
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
-    for a, b in evs:
-        a.record(stream)
-        bulk_write()
-        b.record(stream)
-    torch.cuda.synchronize()
-    bulk_ms = statistics.median(a.elapsed_time(b) for a, b in evs)
-    del bulk
-    # the bulk fill rewrote the pool with new values; the decode reads those
+        for _ in range(3):
+            bulk_write()
+        torch.cuda.synchronize()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(20)]
+        for a, b in evs:
+            a.record(stream)
+            bulk_write()
+            b.record(stream)
+        torch.cuda.synchronize()
+        bulk_ms = statistics.median(a.elapsed_time(b) for a, b in evs)
+        bulk_gbs = bulk_bytes / (bulk_ms * 1e-3) / 1e9
+        extra["write_kv"] = {"value": round(bulk_gbs, 1), "unit": "GB/s",
+                             "frac": round(bulk_gbs / peak, 4), "tokens": int(bulk.slot_mapping.numel()),
+                             "bytes": bulk_bytes, "us": round(bulk_ms * 1e3, 2),
+                             "what": "bulk fill: every context token of the workload, random order"}
+        del bulk  # the pool now holds the bulk-fill values; the decode reads those
 
-    # in-run copy bandwidth of a 1 GiB buffer (context for the peak)
-    src = torch.empty(1 << 29, dtype=torch.bfloat16, device=dev)
-    dst = torch.empty_like(src)
-    for _ in range(3):
-        dst.copy_(src)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(10):
-        dst.copy_(src)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    copy_gbs = 10 * 2 * src.numel() * 2 / (e0.elapsed_time(e1) * 1e-3) / 1e9
-    del src, dst
+        # in-run copy bandwidth of a 1 GiB buffer (context for the measured peak)
+        src = torch.empty(1 << 29, dtype=torch.bfloat16, device=dev)
+        dst = torch.empty_like(src)
+        for _ in range(3):
+            dst.copy_(src)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(10):
+            dst.copy_(src)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        extra["hbm_copy_gbs_in_run"] = round(10 * 2 * src.numel() * 2 / (e0.elapsed_time(e1) * 1e-3) / 1e9, 1)
+        del src, dst
 
     # warm-up
     for _ in range(args.warmup):
@@ -328,12 +347,13 @@ def run_gpu(args, world, rank, local):
     if int(err.item()) != 0:
         raise RuntimeError(f"device error flags {int(err.item()):#x} during warm-up")
 
-    # timed region: K steps, decode launches bracketed by events on the stream
+    # timed region: K steps; each decode launch bracketed by events on its stream
     dec_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
               for _ in range(args.steps)]
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
     torch.cuda.synchronize()
+    torch.cuda.nvtx.range_push("timed")
     with ClockSampler(local) as clocks:
         t_start.record(stream)
         for i in range(args.steps):
@@ -343,6 +363,7 @@ def run_gpu(args, world, rank, local):
             dec_ev[i][1].record(stream)
         t_end.record(stream)
         torch.cuda.synchronize()
+    torch.cuda.nvtx.range_pop()
     barrier(world)
     elapsed = t_start.elapsed_time(t_end) * 1e-3
     dec_ms = statistics.mean(a.elapsed_time(b) for a, b in dec_ev)
@@ -351,81 +372,73 @@ def run_gpu(args, world, rank, local):
         raise RuntimeError(f"device error flags {int(err.item()):#x} in the timed region")
     value, tmax, _ = aggregate(elapsed, step_bytes * args.steps / 1e9, world, dev)
 
-    # end to end through the public API: pinned host inputs in, result out
-    h_q = q.cpu().pin_memory()
-    h_k, h_v = wb.k.cpu().pin_memory(), wb.v.cpu().pin_memory()
-    h_slots = wb.slot_mapping.cpu().pin_memory()
-    h_tables, h_lens = inp.block_tables.cpu().pin_memory(), inp.context_lens.cpu().pin_memory()
-    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    d_q, d_k, d_v = torch.empty_like(q), torch.empty_like(wb.k), torch.empty_like(wb.v)
-    d_slots, d_tables, d_lens = (torch.empty_like(wb.slot_mapping), torch.empty_like(tables),
-                                 torch.empty_like(lens))
-    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v, h_slots, h_tables, h_lens))
-    d2h = h_out.numel() * h_out.element_size()
+    e2e = None
+    if not args.only_decode:
+        # end to end through the public API: pinned host inputs in, result out
+        h_q = q.cpu().pin_memory()
+        h_k, h_v = wb.k.cpu().pin_memory(), wb.v.cpu().pin_memory()
+        h_slots = wb.slot_mapping.cpu().pin_memory()
+        h_tables, h_lens = inp.block_tables.cpu().pin_memory(), inp.context_lens.cpu().pin_memory()
+        h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        d_q, d_k, d_v = torch.empty_like(q), torch.empty_like(wb.k), torch.empty_like(wb.v)
+        d_slots, d_tables, d_lens = (torch.empty_like(wb.slot_mapping), torch.empty_like(tables),
+                                     torch.empty_like(lens))
+        h2d = sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v, h_slots, h_tables, h_lens))
+        d2h = h_out.numel() * h_out.element_size()
 
-    def e2e_step():
-        d_q.copy_(h_q, non_blocking=True)
-        d_k.copy_(h_k, non_blocking=True)
-        d_v.copy_(h_v, non_blocking=True)
-        d_slots.copy_(h_slots, non_blocking=True)
-        d_tables.copy_(h_tables, non_blocking=True)
-        d_lens.copy_(h_lens, non_blocking=True)
-        pkv.pkv_write(inp.k_cache, inp.v_cache, d_k, d_v, d_slots, err_flags=err, stream=stream)
-        pkv.pkv_decode_attention(out, d_q, inp.k_cache, inp.v_cache, d_tables, d_lens, inp.scale,
-                                 max_context_len=max_ctx, workspace=ws, err_flags=err, stream=stream)
-        h_out.copy_(out, non_blocking=True)
-        stream.synchronize()  # the caller reads the result every step
+        def e2e_step():
+            d_q.copy_(h_q, non_blocking=True)
+            d_k.copy_(h_k, non_blocking=True)
+            d_v.copy_(h_v, non_blocking=True)
+            d_slots.copy_(h_slots, non_blocking=True)
+            d_tables.copy_(h_tables, non_blocking=True)
+            d_lens.copy_(h_lens, non_blocking=True)
+            pkv.pkv_write(inp.k_cache, inp.v_cache, d_k, d_v, d_slots, err_flags=err, stream=stream)
+            pkv.pkv_decode_attention(out, d_q, inp.k_cache, inp.v_cache, d_tables, d_lens, inp.scale,
+                                     max_context_len=max_ctx, workspace=ws, err_flags=err,
+                                     stream=stream)
+            h_out.copy_(out, non_blocking=True)
+            stream.synchronize()  # the caller reads the result every step
 
-    for _ in range(max(3, args.warmup)):
-        e2e_step()
-    e2e_steps = args.steps
-    barrier(world)
-    torch.cuda.synchronize()
-    t0 = time.perf_counter()
-    for _ in range(e2e_steps):
-        e2e_step()
-    torch.cuda.synchronize()
-    e2e_elapsed = time.perf_counter() - t0
-    barrier(world)
-    e2e_value, _, _ = aggregate(e2e_elapsed, step_bytes * e2e_steps / 1e9, world, dev)
+        for _ in range(max(3, args.warmup)):
+            e2e_step()
+        barrier(world)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            e2e_step()
+        torch.cuda.synchronize()
+        e2e_elapsed = time.perf_counter() - t0
+        barrier(world)
+        e2e_value, _, _ = aggregate(e2e_elapsed, step_bytes * args.steps / 1e9, world, dev)
+        e2e = {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h}
 
-    peak, peak_kind = hbm_peak()
     achieved = dec_bytes / (dec_ms * 1e-3) / 1e9
-    line = None
-    if rank == 0:
-        cpu = cpu_baseline(inp, elem) if world == 1 and not args.no_cpu_baseline else None
-        line = {
-            "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": round(tmax / args.steps * 1e3, 4), "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {
-                "workload": (f"{WORKLOAD}: B=64 H=32 KVH=8 D=128 block_size=16, context_lens "
-                             "U[512,4096], shuffled blocks from a 1.25x pool, garbage table tails, "
-                             "q/k/v~N(0,1) bf16; step = pkv_write of 64 new tokens + "
-                             "pkv_decode_attention"),
-                "l2": f"inputs larger than L2 ({dec_bytes / 1e6:.0f} MB of K/V per step, no flush)",
-                "decode_bytes_per_step": dec_bytes, "write_bytes_per_step": wr_bytes,
-                "parallelism": f"{world} independent replica batch(es), no collective",
-            },
-            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
-                         "unit": "GB/s", "frac": round(achieved / peak, 4),
-                         "traffic": None, "kernel": "pkv_decode_tc_kernel<128, bf16>",
-                         "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
-                         if peak_kind == "measured" else "fallback 6.8 TB/s",
-                         "decode_us": round(dec_ms * 1e3, 2)},
-            "write_kv": {"value": round(bulk_bytes / (bulk_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
-                         "frac": round(bulk_bytes / (bulk_ms * 1e-3) / 1e9 / peak, 4),
-                         "tokens": int(len(inp.owned) and sum(int(n) for n in inp.context_lens)),
-                         "us": round(bulk_ms * 1e3, 2)},
-            "hbm_copy_gbs_in_run": round(copy_gbs, 1),
-            "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h},
-            "gpu_launches": launches,
-            "clocks": clocks.summary(),
-            "cpu_baseline": cpu,
-        }
-        print(json.dumps(line), flush=True)
+    if rank != 0:
+        return None
+    cpu = None
+    if world == 1 and not args.only_decode and not args.no_cpu_baseline:
+        cpu = cpu_baseline(inp, elem)
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(tmax / args.steps * 1e3, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": config_block(dec_bytes, wr_bytes, world),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": None,
+                     "kernel": "pkv_decode_tc_kernel<128, bf16>",
+                     "peak_source": ("measured (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
+                                     else "fallback 6.8 TB/s"),
+                     "decode_us": round(dec_ms * 1e3, 2)},
+        **extra,
+        "e2e": e2e,
+        "gpu_launches": launches,
+        "clocks": clocks.summary(),
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
     return line
 
 
@@ -436,6 +449,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="lib", choices=["lib", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only-decode", action="store_true",
+                    help="warm-up + timed steps only (no bulk fill, e2e or CPU baseline): for profiling")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
