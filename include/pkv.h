@@ -180,6 +180,40 @@ PKV_API pkv_status pkv_decode_attention(void *out, const void *q, const void *k_
                                         pkv_stream_t stream);
 
 /*
+ * pkv_decode_attention_static -- pkv_decode_attention without a workspace
+ * argument, for callers that may not allocate device memory: for example an
+ * engine plugin whose execute step is forbidden to call cudaMalloc, code that
+ * enqueues work while some other component owns the device allocator, or a
+ * deployment whose device memory is fixed when the process starts.  The
+ * pages have no counterpart: this is a convenience of this library.
+ *
+ * Arguments, results and errors are those of pkv_decode_attention, minus
+ * workspace / workspace_bytes.  The split-KV scratch comes instead from a
+ * fixed array of PKV_STATIC_SCRATCH_BYTES bytes inside the library, which
+ * every GPU the library runs on keeps until the process exits.
+ *   - Sizes whose split-KV scratch would exceed PKV_STATIC_SCRATCH_BYTES are
+ *     rejected with PKV_ERR_WORKSPACE before anything is enqueued (pass a
+ *     larger partition_size, or use pkv_decode_attention with a workspace).
+ *   - No cudaMalloc, cudaFree or other allocating call is made.  The first
+ *     call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - Each call clears the array's merge counters on `stream` before the
+ *     kernel runs.  All calls share the one array: calls whose work overlaps
+ *     on the GPU (different streams, or concurrent host threads) race and
+ *     give wrong results; serialise them.
+ */
+#define PKV_STATIC_SCRATCH_BYTES (16u * 1024u * 1024u)
+PKV_API pkv_status pkv_decode_attention_static(void *out, const void *q, const void *k_cache,
+                                               const void *v_cache, const int32_t *block_tables,
+                                               const int32_t *context_lens, int B, int H,
+                                               int num_kv_heads, int head_dim, int block_size,
+                                               int max_blocks, int64_t num_blocks, float scale,
+                                               pkv_dtype dt, int max_context_len,
+                                               int partition_size, int *err_flags,
+                                               pkv_stream_t stream);
+
+/*
  * pkv_decode_plan -- the partition size and the partitions per sequence that
  * pkv_decode_attention would use for these arguments on a GPU with
  * num_sms SMs (host only, no CUDA call; for tests and tuning).  Returns the
