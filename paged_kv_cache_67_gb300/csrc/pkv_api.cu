@@ -12,6 +12,7 @@ namespace pkv {
 size_t simt_smem_bytes(int D, int GH);
 size_t tc_smem_bytes(int D, int stages);
 
+
 static int round_up(long long x, int m) { return (int)(((x + m - 1) / m) * m); }
 static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
@@ -35,16 +36,27 @@ static int auto_partition_floor(long long cap) {
   return p < 64 ? 64 : p;
 }
 
+// Partial-result slots per (sequence, head) the workspace holds: ceil(cap / P)
+// for an explicit partition size P; for the automatic choice the partition
+// is never below the floor, so ceil(cap / floor) <= kMaxAutoParts.
+static int workspace_parts(long long cap, int partition_size) {
+  const long long P = partition_size > 0 ? partition_size : auto_partition_floor(cap);
+  const long long parts = (cap + P - 1) / P;
+  return parts > 0x7fffffffLL ? 0x7fffffff : (int)parts;
+}
+
 static int tc_stages(int D) { return D <= 64 ? 6 : (D <= 128 ? 3 : (D <= 192 ? 2 : 3)); }
 
 bool make_plan(int B, int H, int KVH, int D, int bs, int max_blocks, int max_context_len,
-               int partition_size, pkv_dtype dt, int num_sms, bool aligned16, DecodePlan *plan) {
+               int partition_size, pkv_dtype dt, int num_sms, size_t smem_optin, bool aligned16,
+               DecodePlan *plan) {
   if (B < 0 || H <= 0 || KVH <= 0 || H % KVH != 0 || D <= 0 || D > 512 || bs <= 0 ||
       max_blocks < 0 || partition_size < 0 || partition_size % 16 != 0 || max_context_len < 0)
     return false;
   if (dt != PKV_F32 && dt != PKV_BF16 && dt != PKV_F16) return false;
   const int G = H / KVH;
   DecodePlan p;
+  memset(&p, 0, sizeof p);
   p.kernel = (tc_eligible(dt, D, bs) && aligned16) ? 1 : 0;
   p.heads_per_cta = p.kernel ? kTcHeads : (D <= 256 ? 4 : 2);
   p.gchunks = (G + p.heads_per_cta - 1) / p.heads_per_cta;
@@ -53,17 +65,21 @@ bool make_plan(int B, int H, int KVH, int D, int bs, int max_blocks, int max_con
   if (partition_size > 0) {
     p.P = partition_size;
   } else {
-    // Enough CTAs for about four per resident slot when contexts average
-    // half the capacity; never below the floor.
+    // About four CTAs per resident CTA slot: split each (sequence, head
+    // group) unit into enough partitions of the capacity, but never below
+    // 1024 tokens (each CTA pays a fixed start-up and merge cost) nor below
+    // the floor that bounds the partitions per sequence.  With enough units
+    // to fill the GPU nothing is split.
     const long long units = (long long)B * KVH * p.gchunks;
     const int per_sm = p.kernel ? (D <= 128 ? 2 : 1) : 4;
     const long long slots = (long long)(num_sms > 0 ? num_sms : 1) * per_sm;
-    long long parts = units > 0 ? (8 * slots + units - 1) / units : 1;
+    long long parts = units > 0 ? (4 * slots + units - 1) / units : 1;
     if (parts < 1) parts = 1;
     int P = round_up((cap + parts - 1) / parts, 16);
     const int floor_p = auto_partition_floor(cap);
     if (P < floor_p) P = floor_p;
-    if (P < 256 && cap > 256) P = 256;
+    const int min_p = cap < 1024 ? round_up(cap, 16) : 1024;
+    if (P < min_p) P = min_p;
     p.P = P;
   }
   const long long mp = (cap + p.P - 1) / p.P;
@@ -75,24 +91,36 @@ bool make_plan(int B, int H, int KVH, int D, int bs, int max_blocks, int max_con
   return true;
 }
 
+size_t workspace_counter_bytes(int B, int H) { return align256((size_t)B * H * sizeof(int)); }
+
 size_t workspace_bytes_for(int B, int H, int D, int max_parts) {
-  if (max_parts <= 1) return 0;
   const size_t rows = (size_t)B * H;
-  return align256(rows * sizeof(int)) + 2 * align256(rows * max_parts * sizeof(float)) +
-         rows * max_parts * (size_t)D * sizeof(float);
+  size_t bytes = workspace_counter_bytes(B, H);
+  if (max_parts > 1)
+    bytes += 2 * align256(rows * max_parts * sizeof(float)) +
+             rows * max_parts * (size_t)D * sizeof(float);
+  return bytes;
 }
 
-static int sm_count_cached() {
+// SM count and opt-in shared memory per block of the current device (cached).
+static bool device_caps(int *sms, size_t *smem_optin) {
   static int counts[64] = {0};
+  static int optin[64] = {0};
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-  if (dev >= 64) {
-    int n = 0;
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    return n;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return false;
+  int n = dev < 64 ? counts[dev] : 0, o = dev < 64 ? optin[dev] : 0;
+  if (n == 0) {
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&o, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+      return false;
+    if (dev < 64) {
+      counts[dev] = n;
+      optin[dev] = o;
+    }
   }
-  if (counts[dev] == 0) cudaDeviceGetAttribute(&counts[dev], cudaDevAttrMultiProcessorCount, dev);
-  return counts[dev];
+  *sms = n;
+  *smem_optin = (size_t)o;
+  return n > 0;
 }
 
 static int elem_size(pkv_dtype dt) { return dt == PKV_F32 ? 4 : 2; }
@@ -128,10 +156,9 @@ PKV_API size_t pkv_decode_workspace_size(int B, int H, int num_kv_heads, int hea
       partition_size < 0 || partition_size % 16 != 0)
     return 0;
   const long long cap = context_cap(block_size, max_blocks, max_context_len);
-  const int P = partition_size > 0 ? partition_size : auto_partition_floor(cap);
-  const long long parts = (cap + P - 1) / P;
-  if (parts > 0x7fffffffLL) return 0;
-  return workspace_bytes_for(B, H, head_dim, (int)parts);
+  const int parts = workspace_parts(cap, partition_size);
+  if ((long long)B * H * parts > 0x7fffffffLL) return 0;
+  return workspace_bytes_for(B, H, head_dim, parts);
 }
 
 PKV_API int pkv_decode_plan(int B, int H, int num_kv_heads, int head_dim, int block_size,
@@ -139,7 +166,7 @@ PKV_API int pkv_decode_plan(int B, int H, int num_kv_heads, int head_dim, int bl
                             int num_sms, int *max_partitions, int *kernel) {
   DecodePlan p;
   if (!make_plan(B, H, num_kv_heads, head_dim, block_size, max_blocks, max_context_len,
-                 partition_size, dt, num_sms, true, &p))
+                 partition_size, dt, num_sms, kDefaultSmemOptin, true, &p))
     return 0;
   if (max_partitions) *max_partitions = p.max_parts;
   if (kernel) *kernel = p.kernel;
@@ -174,11 +201,12 @@ PKV_API pkv_status pkv_decode_attention(void *out, const void *q, const void *k_
   if (reinterpret_cast<uintptr_t>(block_tables) % 4 || reinterpret_cast<uintptr_t>(context_lens) % 4)
     return PKV_ERR_INVALID_ARG;
 
-  const int sms = sm_count_cached();
-  if (sms <= 0) return PKV_ERR_CUDA;
+  int sms = 0;
+  size_t smem_optin = 0;
+  if (!device_caps(&sms, &smem_optin)) return PKV_ERR_CUDA;
   DecodePlan plan;
   if (!make_plan(B, H, num_kv_heads, head_dim, block_size, max_blocks, max_context_len,
-                 partition_size, dt, sms, aligned16, &plan))
+                 partition_size, dt, sms, smem_optin, aligned16, &plan))
     return PKV_ERR_INVALID_ARG;
   if ((long long)num_kv_heads * plan.gchunks > 65535) return PKV_ERR_UNSUPPORTED;
 
@@ -207,18 +235,20 @@ PKV_API pkv_status pkv_decode_attention(void *out, const void *q, const void *k_
   a.scale_log2 = scale * kLog2e;
 
   const size_t need = workspace_bytes_for(B, H, head_dim, plan.max_parts);
-  if (need > 0) {
-    if (!workspace || workspace_bytes < need || reinterpret_cast<uintptr_t>(workspace) % 256)
-      return PKV_ERR_WORKSPACE;
+  if (!workspace || workspace_bytes < need || reinterpret_cast<uintptr_t>(workspace) % 256)
+    return PKV_ERR_WORKSPACE;
+  {
     const size_t rows = (size_t)B * H;
     char *ws = static_cast<char *>(workspace);
     a.ws_cnt = reinterpret_cast<int *>(ws);
     ws += align256(rows * sizeof(int));
-    a.ws_m = reinterpret_cast<float *>(ws);
-    ws += align256(rows * plan.max_parts * sizeof(float));
-    a.ws_l = reinterpret_cast<float *>(ws);
-    ws += align256(rows * plan.max_parts * sizeof(float));
-    a.ws_o = reinterpret_cast<float *>(ws);
+    if (plan.max_parts > 1) {
+      a.ws_m = reinterpret_cast<float *>(ws);
+      ws += align256(rows * plan.max_parts * sizeof(float));
+      a.ws_l = reinterpret_cast<float *>(ws);
+      ws += align256(rows * plan.max_parts * sizeof(float));
+      a.ws_o = reinterpret_cast<float *>(ws);
+    }
   }
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   return plan.kernel ? launch_decode_tc(a, plan, dt, s) : launch_decode_simt(a, plan, dt, s);

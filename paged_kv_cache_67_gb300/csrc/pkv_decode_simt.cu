@@ -151,7 +151,9 @@ __global__ void __launch_bounds__(32 * kSimtWarps) pkv_decode_simt_kernel(const 
     s_o[r * D + d] = o;
   }
   __syncthreads();
-  finish_partition<T>(a, b, head0, nh, part, nparts, s_m, s_l, s_o, D, s_scratch);
+  finish_partition<T>(a, b, head0, nh, part, nparts, s_m, s_l, s_o, D, s_scratch,
+                      a.ws_cnt + (size_t)b * gridDim.y + blockIdx.y, tid, blockDim.x, CtaSync(),
+                      false);
 }
 
 template <typename T, int EPL, int GH>

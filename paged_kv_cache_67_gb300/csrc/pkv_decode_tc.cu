@@ -10,34 +10,38 @@
 // instead of copying K": one CTA serves the whole group; fp32 scores scaled
 // before an fp32 softmax; weighted V sum cast to the output dtype.  The
 // block-wise online softmax is the one of the interview note
-// "PagedAttention kernel: paged KV cache 与 block table", section 代码.
+// "PagedAttention kernel: paged KV cache 与 block table", section 代码; its
+// partitioned (v2) variant, section 深入原理, is the split into work items.
 //
 // Work decomposition.  CTA = (partition of the context, KV head x chunk of
-// <= 16 query heads, sequence); 4 warps.  A partition is split into
-// 16-token chunks (block_size is a multiple of 16, so a chunk never spans
-// two physical blocks); warp w takes chunks w, w+4, w+8, ...  Each warp has
-// its own ring of `stages` shared-memory slots; lane 0 fetches the chunk's
-// K and V rows of this KV head with tiled 4-D TMA loads (box 64 elements x
-// 16 rows, 128-byte swizzle) that complete on the slot's mbarrier; the table
-// entries come from one coalesced load per 32 chunks, broadcast by shuffle.
+// <= 16 query heads, sequence); 4 warps.  A partition is split into 16-token
+// chunks (block_size is a multiple of 16, so a chunk never spans two
+// physical blocks); warp w takes chunks w, w+4, w+8, ...  Each warp has its
+// own ring of `stages` shared-memory slots; lanes 0..2*D/64-1 fetch a chunk's
+// K and V rows of this KV head with one tiled 4-D TMA load each (box 64
+// elements x 1 head x 16 rows x 1 block, 128-byte swizzle, L2 evict-first)
+// completing on the slot's mbarrier; the table entries come from one
+// coalesced load per 32 chunks, broadcast by shuffle.
 //
-// Per chunk, per warp (G padded to 16 rows):
+// Per chunk, per warp (the query group padded to the 16 rows of one tile):
 //   S[16 x 16]  = Qgroup[16 x D] . K^T        D/16 mma, K via ldmatrix
-//   online softmax on S in fp32 (log2 units), masked past n
+//   online softmax on S in fp32 (log2 units), masked past the end
 //   O[16 x D]  += P[16 x 16] . V              D/16 mma, V via ldmatrix.trans
 // The P fragment is the S accumulator re-packed to bf16/fp16 in registers.
 // At the end the 4 warp states are merged in shared memory and the
 // partition is finished by finish_partition (direct output, or partials +
 // log-sum-exp merge by the last CTA of the sequence).
+#include <string.h>
+
 #include "pkv_device.cuh"
 #include "pkv_internal.h"
 
 namespace pkv {
 
-constexpr int kTcWarps = 4;
 constexpr int kChunk = 16;          // tokens per pipeline slot
 constexpr int kBoxElems = 64;       // elements per TMA box row (128 bytes)
 constexpr int kBoxBytes = kChunk * 128;
+constexpr int kTcWarps = 4;         // grid kernel: warps per CTA
 
 template <int D>
 struct TcShape {
@@ -45,10 +49,107 @@ struct TcShape {
   static constexpr int kNTiles = D / 8;         // 8-wide output tiles
   static constexpr int kBoxes = D / kBoxElems;  // TMA boxes per row
   static constexpr int kStageBytes = 2 * kBoxes * kBoxBytes;  // K + V of one chunk
-  static constexpr int kQStride = D + 8;        // padded Q row in shared memory (elements)
+  static constexpr int kQBytes = kBoxes * kBoxBytes;          // 16 query rows (TMA, swizzled)
+  static constexpr int kQStride = D + 8;        // grid kernel: padded Q row (elements)
   static constexpr int kOStride = D + 8;        // padded fp32 row for the warp merge
   static constexpr bool kQInRegs = D <= 128;
 };
+
+// --------------------------------------------------- one chunk of one warp
+//
+// kb / vb: shared addresses of the chunk's K and V tiles (kBoxes boxes of 16
+// rows x 128 bytes, 128-byte swizzle: 16-byte column c of row r sits at
+// r * 128 + ((c ^ (r & 7)) << 4)).  qfrag(kk, af) yields the A fragment of
+// the 16 x 16 query tile for k-step kk.  o/m/l: the warp's running state for
+// rows lane/4 (m0, l0, o[.][0..1]) and lane/4 + 8 (m1, l1, o[.][2..3]).
+template <int D, typename T, typename QFrag>
+__device__ __forceinline__ void tc_chunk(uint32_t kb, uint32_t vb, int valid, const QFrag &qfrag,
+                                         float (&o)[D / 8][4], float &m0, float &m1, float &l0,
+                                         float &l1, float scale_log2, int lane) {
+  using Sh = TcShape<D>;
+  using Mma = MmaOp<T>;
+  const int k_row = (lane & 7) + ((lane >> 4) << 3);        // token row of the K fragment
+  const int k_col = (lane >> 3) & 1;                        // +1 column for b1 / b3
+  const int v_row = (lane & 7) + (((lane >> 3) & 1) << 3);  // token row of the V fragment
+  const int v_col = lane >> 4;                              // +1 column for the 2nd n-tile
+  const int sw = lane & 7;                                  // swizzle term (row & 7)
+
+  // ---- S = Q . K^T  (rows: query heads, cols: the chunk's 16 tokens); even
+  // and odd k-steps accumulate separately (two shorter dependency chains)
+  float sacc[2][2][4] = {};
+#pragma unroll
+  for (int kk = 0; kk < Sh::kSteps; ++kk) {
+    const int col = ((kk & 3) << 1) + k_col;
+    const uint32_t addr = kb + (kk >> 2) * kBoxBytes + k_row * 128 + ((col ^ sw) << 4);
+    uint32_t b0, b1, b2, b3;
+    ldsm_x4(addr, b0, b1, b2, b3);
+    uint32_t af[4];
+    qfrag(kk, af);
+    Mma::run(sacc[kk & 1][0], af, b0, b1);
+    Mma::run(sacc[kk & 1][1], af, b2, b3);
+  }
+
+  // ---- online softmax in log2 units; tokens past the end are -inf
+  float x[2][4];
+  if (valid == kChunk) {
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) x[nt][e] = (sacc[0][nt][e] + sacc[1][nt][e]) * scale_log2;
+  } else {
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int tok = nt * 8 + (lane & 3) * 2 + (e & 1);
+        x[nt][e] = tok < valid ? (sacc[0][nt][e] + sacc[1][nt][e]) * scale_log2 : -INFINITY;
+      }
+  }
+  float mx0 = fmaxf(fmaxf(x[0][0], x[0][1]), fmaxf(x[1][0], x[1][1]));
+  float mx1 = fmaxf(fmaxf(x[0][2], x[0][3]), fmaxf(x[1][2], x[1][3]));
+  mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+  mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+  mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+  mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+  const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+  if (__any_sync(0xffffffffu, (mn0 > m0) || (mn1 > m1))) {
+    const float c0 = fast_exp2(m0 - mn0), c1 = fast_exp2(m1 - mn1);
+    l0 *= c0;
+    l1 *= c1;
+#pragma unroll
+    for (int nt = 0; nt < Sh::kNTiles; ++nt) {
+      o[nt][0] *= c0; o[nt][1] *= c0;
+      o[nt][2] *= c1; o[nt][3] *= c1;
+    }
+    m0 = mn0;
+    m1 = mn1;
+  }
+  uint32_t pa[4];
+  pa[0] = Mma::pack(fast_exp2(x[0][0] - m0), fast_exp2(x[0][1] - m0), l0);
+  pa[1] = Mma::pack(fast_exp2(x[0][2] - m1), fast_exp2(x[0][3] - m1), l1);
+  pa[2] = Mma::pack(fast_exp2(x[1][0] - m0), fast_exp2(x[1][1] - m0), l0);
+  pa[3] = Mma::pack(fast_exp2(x[1][2] - m1), fast_exp2(x[1][3] - m1), l1);
+
+  // ---- O += P . V ; V rows past the end are zeroed (they may hold NaN/Inf)
+  uint32_t vm0 = 0xffffffffu, vm1 = 0xffffffffu;
+  if (valid < kChunk) {
+    const int tk = (lane & 3) * 2;
+    vm0 = (tk < valid ? 0x0000ffffu : 0u) | (tk + 1 < valid ? 0xffff0000u : 0u);
+    vm1 = (tk + 8 < valid ? 0x0000ffffu : 0u) | (tk + 9 < valid ? 0xffff0000u : 0u);
+  }
+#pragma unroll
+  for (int dp = 0; dp < Sh::kSteps; ++dp) {
+    const int col = ((dp & 3) << 1) + v_col;
+    const uint32_t addr = vb + (dp >> 2) * kBoxBytes + v_row * 128 + ((col ^ sw) << 4);
+    uint32_t b0, b1, b2, b3;
+    ldsm_x4_trans(addr, b0, b1, b2, b3);
+    b0 &= vm0; b1 &= vm1; b2 &= vm0; b3 &= vm1;
+    Mma::run(o[2 * dp], pa, b0, b1);
+    Mma::run(o[2 * dp + 1], pa, b2, b3);
+  }
+}
+
+// ======================================================= grid kernel (4 warps)
 
 size_t tc_smem_bytes(int D, int stages) {
   const size_t stage_bytes = 2 * (size_t)(D / kBoxElems) * kBoxBytes;
@@ -60,12 +161,15 @@ size_t tc_smem_bytes(int D, int stages) {
          + sizeof(int) * (4 + 2 * kTcHeads);              // epilogue scratch
 }
 
+// CTA = (partition, KV head x chunk of <= 16 query heads, sequence); warp w
+// takes chunks w, w+4, ... of the partition through its own ring of
+// `stages` slots; lane 0 issues the TMA loads; table entries are fetched 32
+// at a time by one coalesced load and broadcast by shuffle.
 template <int D, typename T>
 __global__ void __launch_bounds__(32 * kTcWarps, 1)
     pkv_decode_tc_kernel(const __grid_constant__ CUtensorMap tmK,
                          const __grid_constant__ CUtensorMap tmV, const DecodeArgs a) {
   using Sh = TcShape<D>;
-  using Mma = MmaOp<T>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -105,10 +209,48 @@ __global__ void __launch_bounds__(32 * kTcWarps, 1)
     for (int s = 0; s < S; ++s) mbar_init(&bars[w * S + s], 1);
     fence_mbar_init();
   }
+  __syncwarp();
   if (tid == 0) {
     prefetch_tensormap(&tmK);
     prefetch_tensormap(&tmV);
   }
+  const uint64_t policy = l2_evict_first_policy();
+  int tbl_batch = -1, my_phys = 0;
+  auto phys_of = [&](int i) -> int {  // physical block of this warp's i-th chunk (warp-collective)
+    const int batch = i >> 5;
+    if (batch != tbl_batch) {
+      tbl_batch = batch;
+      const int ii = batch * 32 + lane;
+      my_phys = 0;
+      if (ii < nch_w) my_phys = checked_block(a, b, (t0 + kChunk * (w + kTcWarps * ii)) / a.bs);
+    }
+    return __shfl_sync(0xffffffffu, my_phys, i & 31);
+  };
+  // Fetch chunk i of this warp into `slot` (warp-collective).  Lane 0 posts
+  // the byte count; lanes 0 .. 2*kBoxes-1 issue one box each (one thread
+  // issues TMA operations one after another, so they are spread over lanes).
+  const int bs_mask = (a.bs & (a.bs - 1)) == 0 ? a.bs - 1 : -1;
+  auto issue = [&](int i, int slot) {
+    const int phys = phys_of(i);
+    const int tok = t0 + kChunk * (w + kTcWarps * i);
+    const int row0 = bs_mask >= 0 ? (tok & bs_mask) : tok % a.bs;
+    uint8_t *st = ring + (size_t)(w * S + slot) * Sh::kStageBytes;
+    uint64_t *bar = &bars[w * S + slot];
+    if (lane == 0) mbar_arrive_expect_tx(bar, Sh::kStageBytes);
+    __syncwarp();
+    if (lane < 2 * Sh::kBoxes) {
+      if (lane < Sh::kBoxes)
+        tma_load_4d(st + lane * kBoxBytes, &tmK, bar, lane * kBoxElems, kvh, row0, phys, policy);
+      else
+        tma_load_4d(st + lane * kBoxBytes, &tmV, bar, (lane - Sh::kBoxes) * kBoxElems, kvh, row0,
+                    phys, policy);
+    }
+  };
+  // Start the warp's first fetches before staging Q: the copies are in
+  // flight while the query tile is loaded.
+  const int npro = min(S, nch_w);
+  for (int i = 0; i < npro; ++i) issue(i, i);
+
   // Q rows of the group (rows >= nh are zero) into padded shared rows.
   {
     const T *qg = reinterpret_cast<const T *>(a.q) + ((size_t)b * a.H + head0) * D;
@@ -122,7 +264,6 @@ __global__ void __launch_bounds__(32 * kTcWarps, 1)
   }
   __syncthreads();
 
-  // ldmatrix address of the Q A-fragment for k-step kk (lane-dependent row / column).
   const uint32_t q_lane_addr =
       smem_u32(sQ) + (((lane & 7) + ((lane >> 3) & 1) * 8) * Sh::kQStride + (lane >> 4) * 8) * 2;
   uint32_t qf[Sh::kQInRegs ? Sh::kSteps : 1][4];
@@ -131,53 +272,18 @@ __global__ void __launch_bounds__(32 * kTcWarps, 1)
     for (int kk = 0; kk < Sh::kSteps; ++kk)
       ldsm_x4(q_lane_addr + kk * 32, qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3]);
   }
-
-  const uint64_t policy = l2_evict_first_policy();
-  int tbl_batch = -1, my_phys = 0;
-  // Physical block of this warp's i-th chunk (warp-collective).
-  auto phys_of = [&](int i) -> int {
-    const int batch = i >> 5;
-    if (batch != tbl_batch) {
-      tbl_batch = batch;
-      const int ii = batch * 32 + lane;
-      my_phys = 0;
-      if (ii < nch_w) my_phys = checked_block(a, b, (t0 + kChunk * (w + kTcWarps * ii)) / a.bs);
-    }
-    return __shfl_sync(0xffffffffu, my_phys, i & 31);
-  };
-  // Fetch chunk i of this warp into ring slot `slot` (warp-collective).
-  auto issue = [&](int i, int slot) {
-    const int phys = phys_of(i);
-    if (lane == 0) {
-      const int row0 = (t0 + kChunk * (w + kTcWarps * i)) % a.bs;
-      uint8_t *st = ring + (size_t)(w * S + slot) * Sh::kStageBytes;
-      uint64_t *bar = &bars[w * S + slot];
-      mbar_arrive_expect_tx(bar, Sh::kStageBytes);
-#pragma unroll
-      for (int h = 0; h < Sh::kBoxes; ++h) {
-        tma_load_4d(st + h * kBoxBytes, &tmK, bar, h * kBoxElems, kvh, row0, phys, policy);
-        tma_load_4d(st + (Sh::kBoxes + h) * kBoxBytes, &tmV, bar, h * kBoxElems, kvh, row0, phys,
-                    policy);
-      }
+  auto qfrag = [&](int kk, uint32_t(&af)[4]) {
+    if constexpr (Sh::kQInRegs) {
+      af[0] = qf[kk][0]; af[1] = qf[kk][1]; af[2] = qf[kk][2]; af[3] = qf[kk][3];
+    } else {
+      ldsm_x4(q_lane_addr + kk * 32, af[0], af[1], af[2], af[3]);
     }
   };
 
   float o[Sh::kNTiles][4];
 #pragma unroll
   for (int nt = 0; nt < Sh::kNTiles; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
-  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;  // rows lane/4 and lane/4 + 8
-
-  const int npro = min(S, nch_w);
-  for (int i = 0; i < npro; ++i) issue(i, i);
-
-  // Lane-dependent parts of the swizzled ldmatrix addresses.  In a slot each
-  // box is 16 rows of 128 bytes; the 16-byte chunk c of row r sits at
-  // r * 128 + ((c ^ (r & 7)) << 4) (TMA 128-byte swizzle); r & 7 == lane & 7.
-  const int k_row = (lane & 7) + ((lane >> 4) << 3);       // token row for the K (B) fragment
-  const int k_col = (lane >> 3) & 1;                       // +1 chunk for b1 / b3
-  const int v_row = (lane & 7) + (((lane >> 3) & 1) << 3); // token row for the V fragment
-  const int v_col = lane >> 4;                              // +1 chunk for the 2nd n-tile
-  const int sw = lane & 7;
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
 
   int slot = 0;
   uint32_t parity = 0;
@@ -190,78 +296,8 @@ __global__ void __launch_bounds__(32 * kTcWarps, 1)
     }
     const int valid = min(kChunk, t1 - (t0 + kChunk * (w + kTcWarps * i)));
     const uint32_t kb = smem_u32(ring + (size_t)(w * S + slot) * Sh::kStageBytes);
-    const uint32_t vb = kb + Sh::kBoxes * kBoxBytes;
-
-    // ---- S = Q . K^T  (rows: query heads, cols: the chunk's 16 tokens)
-    float sacc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-#pragma unroll
-    for (int kk = 0; kk < Sh::kSteps; ++kk) {
-      const int chunk = ((kk & 3) << 1) + k_col;
-      const uint32_t addr = kb + (kk >> 2) * kBoxBytes + k_row * 128 + ((chunk ^ sw) << 4);
-      uint32_t b0, b1, b2, b3;
-      ldsm_x4(addr, b0, b1, b2, b3);
-      uint32_t af[4];
-      if constexpr (Sh::kQInRegs) {
-        af[0] = qf[kk][0]; af[1] = qf[kk][1]; af[2] = qf[kk][2]; af[3] = qf[kk][3];
-      } else {
-        ldsm_x4(q_lane_addr + kk * 32, af[0], af[1], af[2], af[3]);
-      }
-      Mma::run(sacc[0], af, b0, b1);
-      Mma::run(sacc[1], af, b2, b3);
-    }
-
-    // ---- online softmax in log2 units; tokens past the partition end are -inf
-    float x[2][4];
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int tok = nt * 8 + (lane & 3) * 2 + (e & 1);
-        x[nt][e] = tok < valid ? sacc[nt][e] * a.scale_log2 : -INFINITY;
-      }
-    float mx0 = fmaxf(fmaxf(x[0][0], x[0][1]), fmaxf(x[1][0], x[1][1]));
-    float mx1 = fmaxf(fmaxf(x[0][2], x[0][3]), fmaxf(x[1][2], x[1][3]));
-    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-    if (__any_sync(0xffffffffu, (mn0 > m0) || (mn1 > m1))) {
-      const float c0 = fast_exp2(m0 - mn0), c1 = fast_exp2(m1 - mn1);
-      l0 *= c0;
-      l1 *= c1;
-#pragma unroll
-      for (int nt = 0; nt < Sh::kNTiles; ++nt) {
-        o[nt][0] *= c0; o[nt][1] *= c0;
-        o[nt][2] *= c1; o[nt][3] *= c1;
-      }
-      m0 = mn0;
-      m1 = mn1;
-    }
-    uint32_t pa[4];
-    pa[0] = Mma::pack(fast_exp2(x[0][0] - m0), fast_exp2(x[0][1] - m0), l0);
-    pa[1] = Mma::pack(fast_exp2(x[0][2] - m1), fast_exp2(x[0][3] - m1), l1);
-    pa[2] = Mma::pack(fast_exp2(x[1][0] - m0), fast_exp2(x[1][1] - m0), l0);
-    pa[3] = Mma::pack(fast_exp2(x[1][2] - m1), fast_exp2(x[1][3] - m1), l1);
-
-    // ---- O += P . V ; V rows past the end are zeroed (they may hold NaN/Inf)
-    uint32_t vm0 = 0xffffffffu, vm1 = 0xffffffffu;
-    if (valid < kChunk) {
-      const int tk = (lane & 3) * 2;
-      vm0 = (tk < valid ? 0x0000ffffu : 0u) | (tk + 1 < valid ? 0xffff0000u : 0u);
-      vm1 = (tk + 8 < valid ? 0x0000ffffu : 0u) | (tk + 9 < valid ? 0xffff0000u : 0u);
-    }
-#pragma unroll
-    for (int dp = 0; dp < Sh::kSteps; ++dp) {
-      const int chunk = ((dp & 3) << 1) + v_col;
-      const uint32_t addr = vb + (dp >> 2) * kBoxBytes + v_row * 128 + ((chunk ^ sw) << 4);
-      uint32_t b0, b1, b2, b3;
-      ldsm_x4_trans(addr, b0, b1, b2, b3);
-      b0 &= vm0; b1 &= vm1; b2 &= vm0; b3 &= vm1;
-      Mma::run(o[2 * dp], pa, b0, b1);
-      Mma::run(o[2 * dp + 1], pa, b2, b3);
-    }
-
+    tc_chunk<D, T>(kb, kb + Sh::kBoxes * kBoxBytes, valid, qfrag, o, m0, m1, l0, l1, a.scale_log2,
+                   lane);
     __syncwarp();
     if (i + S < nch_w) issue(i + S, slot);
     if (++slot == S) {
@@ -281,7 +317,6 @@ __global__ void __launch_bounds__(32 * kTcWarps, 1)
     }
   }
 
-  // Row sums over the 4 lanes holding a row's columns.
   l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
   l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
   l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
@@ -304,13 +339,17 @@ __global__ void __launch_bounds__(32 * kTcWarps, 1)
   }
   const float f0 = fast_exp2(m0 - M0), f1 = fast_exp2(m1 - M1);  // 0 for a warp without chunks
   float *sO = reinterpret_cast<float *>(ring);                   // [W][16][kOStride]
+  if (r0 < nh) {  // rows past the group are padding: never merged
 #pragma unroll
-  for (int nt = 0; nt < Sh::kNTiles; ++nt) {
-    const int d = nt * 8 + (lane & 3) * 2;
-    *reinterpret_cast<float2 *>(sO + (w * kTcHeads + r0) * Sh::kOStride + d) =
-        make_float2(o[nt][0] * f0, o[nt][1] * f0);
-    *reinterpret_cast<float2 *>(sO + (w * kTcHeads + r1) * Sh::kOStride + d) =
-        make_float2(o[nt][2] * f1, o[nt][3] * f1);
+    for (int nt = 0; nt < Sh::kNTiles; ++nt)
+      *reinterpret_cast<float2 *>(sO + (w * kTcHeads + r0) * Sh::kOStride + nt * 8 + (lane & 3) * 2) =
+          make_float2(o[nt][0] * f0, o[nt][1] * f0);
+  }
+  if (r1 < nh) {
+#pragma unroll
+    for (int nt = 0; nt < Sh::kNTiles; ++nt)
+      *reinterpret_cast<float2 *>(sO + (w * kTcHeads + r1) * Sh::kOStride + nt * 8 + (lane & 3) * 2) =
+          make_float2(o[nt][2] * f1, o[nt][3] * f1);
   }
   if (tid < kTcHeads) {
     float M = -INFINITY;
@@ -330,7 +369,9 @@ __global__ void __launch_bounds__(32 * kTcWarps, 1)
     sO[r * Sh::kOStride + d] = acc;  // row r of warp 0's slot: read above only by this thread
   }
   __syncthreads();
-  finish_partition<T>(a, b, head0, nh, part, nparts, s_m, s_l, sO, Sh::kOStride, s_scratch);
+  finish_partition<T>(a, b, head0, nh, part, nparts, s_m, s_l, sO, Sh::kOStride, s_scratch,
+                      a.ws_cnt + (size_t)b * gridDim.y + blockIdx.y, tid, blockDim.x, CtaSync(),
+                      false);
 }
 
 // ---------------------------------------------------------------- host side
@@ -355,6 +396,10 @@ static EncodeTiledFn encode_fn() {
   return fn;
 }
 
+static CUtensorMapDataType map_type(pkv_dtype dt) {
+  return dt == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+}
+
 // Tensor map of a [num_blocks, bs, KVH, D] cache: dims innermost first, box of
 // 64 elements x 1 head x 16 rows x 1 block, 128-byte swizzle.
 static bool encode_cache_map(CUtensorMap *map, const void *cache, pkv_dtype dt, long long num_blocks,
@@ -366,27 +411,30 @@ static bool encode_cache_map(CUtensorMap *map, const void *cache, pkv_dtype dt, 
   cuuint64_t strides[3] = {D * el, (cuuint64_t)KVH * D * el, (cuuint64_t)bs * KVH * D * el};
   cuuint32_t box[4] = {kBoxElems, 1, kChunk, 1};
   cuuint32_t estr[4] = {1, 1, 1, 1};
-  CUtensorMapDataType t =
-      dt == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-  CUresult r = fn(map, t, 4, const_cast<void *>(cache), dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
+  return fn(map, map_type(dt), 4, const_cast<void *>(cache), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// One-time opt-in to the kernel's dynamic shared memory, per device.
+template <typename K>
+static bool allow_smem(K kern, size_t bytes, int *configured) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  if (dev < 64 && configured[dev] >= (int)bytes) return true;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) !=
+      cudaSuccess)
+    return false;
+  if (dev < 64) configured[dev] = (int)bytes;
+  return true;
 }
 
 template <int D, typename T>
 static pkv_status launch_tc_t(const DecodeArgs &a, const DecodePlan &plan, const CUtensorMap &mk,
                               const CUtensorMap &mv, cudaStream_t stream) {
   auto kern = pkv_decode_tc_kernel<D, T>;
-  static int configured_bytes[64] = {0};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
-  if (dev < 64 && configured_bytes[dev] < (int)plan.smem_bytes) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)plan.smem_bytes) != cudaSuccess)
-      return PKV_ERR_CUDA;
-    configured_bytes[dev] = (int)plan.smem_bytes;
-  }
+  static int configured[64] = {0};
+  if (!allow_smem(kern, plan.smem_bytes, configured)) return PKV_ERR_CUDA;
   dim3 grid(plan.max_parts, a.KVH * plan.gchunks, a.B);
   kern<<<grid, 32 * kTcWarps, plan.smem_bytes, stream>>>(mk, mv, a);
   return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;

@@ -37,7 +37,7 @@ struct DecodeArgs {
   int heads_per_cta;     // query heads one CTA serves (<= its kernel's maximum)
   int gchunks;           // ceil(G / heads_per_cta)
   int P;                 // partition size in tokens (multiple of 16)
-  int max_parts;         // partitions the grid covers per sequence (gridDim.x)
+  int max_parts;         // partitions the grid covers per sequence (gridDim.x); workspace stride
   int stages;            // pipeline depth per warp (TMA kernel)
   float scale_log2;      // scale * log2(e): scores are kept in log2 units
 };
@@ -92,6 +92,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
   return ok != 0;
 }
 
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
 // Wait for the phase with the given parity to complete; false after
 // kWaitLimitNs without completion.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity) {
@@ -111,6 +115,16 @@ __device__ __forceinline__ void tma_load_4d(void *dst, const CUtensorMap *map, u
       ".L2::cache_hint [%0], [%1, {%3, %4, %5, %6}], [%2], %7;" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2),
       "r"(c3), "l"(policy)
+      : "memory");
+}
+
+// Tiled 2-D TMA load global -> shared (no cache hint).
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, uint64_t *bar,
+                                            int c0, int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1)
       : "memory");
 }
 
@@ -236,32 +250,51 @@ __device__ __forceinline__ int checked_block(const DecodeArgs &a, int b, int lb)
 }
 
 // ----------------------------------------------------------------- epilogue
+
+// Named barrier over the first `nthreads` threads of the CTA (id 1..15).
+__device__ __forceinline__ void named_barrier(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+struct CtaSync {
+  __device__ __forceinline__ void operator()() const { __syncthreads(); }
+};
+
+struct NamedSync {
+  int id, nthreads;
+  __device__ __forceinline__ void operator()() const { named_barrier(id, nthreads); }
+};
+
 //
-// Called by every thread of the CTA once the partition [part*P, ...) of
-// sequence b has been reduced to, for each of its nh query heads r:
+// Called by `nthr` threads (thread index `tid`, synchronised by `sync`) once
+// the partition [part*P, ...) of sequence b has been reduced to, for each of
+// its nh query heads r:
 //   s_m[r]  running max of the log2-unit scores,
 //   s_l[r]  sum of 2^(score - s_m[r]),
 //   s_o[r*ostride + d]  sum of 2^(score - s_m[r]) * V[d].
 // With one partition the output row is s_o / s_l.  Otherwise the partials go
-// to the workspace; the CTA that finishes a (sequence, head group) last
-// merges all partitions:  M = max_p m_p,  L = sum_p l_p 2^(m_p - M),
-// out = sum_p o_p 2^(m_p - M) / L, and resets the counter to zero.
-template <typename T>
+// to the workspace; the group that finishes a (sequence, head group) last --
+// counted by `counter` -- merges all partitions:  M = max_p m_p,
+// L = sum_p l_p 2^(m_p - M),  out = sum_p o_p 2^(m_p - M) / L, and resets the
+// counter to zero.  With `clear_o`, each s_o element is zeroed right after
+// the thread that reads it has read it.
+template <typename T, typename Sync>
 __device__ void finish_partition(const DecodeArgs &a, int b, int head0, int nh, int part,
-                                 int nparts, const float *s_m, const float *s_l,
-                                 const float *s_o, int ostride, int *s_scratch) {
-  const int tid = threadIdx.x, nthr = blockDim.x;
+                                 int nparts, const float *s_m, const float *s_l, float *s_o,
+                                 int ostride, int *s_scratch, int *counter, int tid, int nthr,
+                                 Sync sync, bool clear_o) {
   const int D = a.D;
   T *out = reinterpret_cast<T *>(a.out);
   if (nparts == 1) {
     for (int i = tid; i < nh * D; i += nthr) {
       const int r = i / D, d = i - r * D;
       const float v = s_o[r * ostride + d] / s_l[r];
+      if (clear_o) s_o[r * ostride + d] = 0.f;
       out[((size_t)b * a.H + head0 + r) * D + d] = from_f32<T>(v);
     }
     return;
   }
-  const size_t row0 = (size_t)b * a.H + head0;  // first (b, h) row of this CTA
+  const size_t row0 = (size_t)b * a.H + head0;  // first (b, h) row of this group
   for (int r = tid; r < nh; r += nthr) {
     a.ws_m[(row0 + r) * a.max_parts + part] = s_m[r];
     a.ws_l[(row0 + r) * a.max_parts + part] = s_l[r];
@@ -269,18 +302,22 @@ __device__ void finish_partition(const DecodeArgs &a, int b, int head0, int nh, 
   for (int i = tid; i < nh * D; i += nthr) {
     const int r = i / D, d = i - r * D;
     a.ws_o[((row0 + r) * a.max_parts + part) * D + d] = s_o[r * ostride + d];
+    if (clear_o) s_o[r * ostride + d] = 0.f;
   }
-  __threadfence();
-  __syncthreads();
-  int *counter = a.ws_cnt + (size_t)b * gridDim.y + blockIdx.y;
+  // One thread publishes the group's partials: the barrier orders the
+  // group's writes before its fence (release is cumulative), the atomic
+  // counts the partition, and the finisher's fence orders the reads after it.
+  sync();
   if (tid == 0) {
+    __threadfence();
     const int prev = atomicAdd(counter, 1);
-    s_scratch[0] = (prev == nparts - 1);
+    const int last = prev == nparts - 1;
+    if (last) __threadfence();
+    s_scratch[0] = last;
   }
-  __syncthreads();
+  sync();
   if (!s_scratch[0]) return;
-  __threadfence();
-  // Last CTA: per-row max and total, then the merged rows.
+  // Last group: per-row max and total, then the merged rows.
   float *s_M = reinterpret_cast<float *>(s_scratch + 1);
   float *s_invL = s_M + nh;
   const int warp = tid >> 5, lane = tid & 31, nwarps = nthr >> 5;
@@ -300,15 +337,22 @@ __device__ void finish_partition(const DecodeArgs &a, int b, int head0, int nh, 
       s_invL[r] = 1.f / L;
     }
   }
-  __syncthreads();
+  sync();
   for (int i = tid; i < nh * D; i += nthr) {
     const int r = i / D, d = i - r * D;
     const float *pm = a.ws_m + (row0 + r) * a.max_parts;
     const float *po = a.ws_o + (row0 + r) * a.max_parts * D + d;
     const float M = s_M[r];
-    float acc = 0.f;
-    for (int p = 0; p < nparts; ++p) acc += __ldcg(po + (size_t)p * D) * fast_exp2(__ldcg(pm + p) - M);
-    out[(row0 + r) * D + d] = from_f32<T>(acc * s_invL[r]);
+    float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;  // four independent load chains
+    int p = 0;
+    for (; p + 3 < nparts; p += 4) {
+      acc0 += __ldcg(po + (size_t)p * D) * fast_exp2(__ldcg(pm + p) - M);
+      acc1 += __ldcg(po + (size_t)(p + 1) * D) * fast_exp2(__ldcg(pm + p + 1) - M);
+      acc2 += __ldcg(po + (size_t)(p + 2) * D) * fast_exp2(__ldcg(pm + p + 2) - M);
+      acc3 += __ldcg(po + (size_t)(p + 3) * D) * fast_exp2(__ldcg(pm + p + 3) - M);
+    }
+    for (; p < nparts; ++p) acc0 += __ldcg(po + (size_t)p * D) * fast_exp2(__ldcg(pm + p) - M);
+    out[(row0 + r) * D + d] = from_f32<T>(((acc0 + acc1) + (acc2 + acc3)) * s_invL[r]);
   }
   if (tid == 0) *counter = 0;  // every partition has arrived: ready for the next call
 }

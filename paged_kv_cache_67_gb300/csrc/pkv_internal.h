@@ -26,12 +26,19 @@ struct DecodePlan {
 constexpr int kTcHeads = 16;
 // Partitions per sequence the automatic partition size never exceeds.
 constexpr int kMaxAutoParts = 64;
+// Shared memory a block may opt in to on sm_100-class GPUs (used when no
+// device is queried).
+constexpr size_t kDefaultSmemOptin = 232448;
 
 bool tc_eligible(pkv_dtype dt, int D, int bs);
 // Fills *plan; returns false for sizes no kernel handles.
 bool make_plan(int B, int H, int KVH, int D, int bs, int max_blocks, int max_context_len,
-               int partition_size, pkv_dtype dt, int num_sms, bool aligned16, DecodePlan *plan);
+               int partition_size, pkv_dtype dt, int num_sms, size_t smem_optin, bool aligned16,
+               DecodePlan *plan);
 size_t workspace_bytes_for(int B, int H, int D, int max_parts);
+// Bytes at the start of the workspace that must be zero before a call (the
+// work queue and the per-(sequence, head group) counters).
+size_t workspace_counter_bytes(int B, int H);
 
 pkv_status launch_write(void *k_cache, void *v_cache, const void *k, const void *v,
                         const int64_t *slot_mapping, int64_t T, int64_t k_stride, int64_t v_stride,

@@ -39,8 +39,6 @@ pkv_status scratch_address(void **addr) {
   return PKV_OK;
 }
 
-size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
-
 }  // namespace
 
 extern "C" PKV_API pkv_status pkv_decode_attention_static(
@@ -56,9 +54,10 @@ extern "C" PKV_API pkv_status pkv_decode_attention_static(
   void *scratch = nullptr;
   pkv_status st = scratch_address(&scratch);
   if (st != PKV_OK) return st;
-  int dev = 0, sms = 0;
+  int dev = 0, sms = 0, optin = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
     return PKV_ERR_CUDA;
   // The same plan pkv_decode_attention will make: how much scratch it needs.
   const void *ptrs[4] = {out, q, k_cache, v_cache};
@@ -66,19 +65,17 @@ extern "C" PKV_API pkv_status pkv_decode_attention_static(
   for (const void *p : ptrs) aligned16 = aligned16 && (reinterpret_cast<uintptr_t>(p) % 16 == 0);
   pkv::DecodePlan plan;
   if (!pkv::make_plan(B, H, num_kv_heads, head_dim, block_size, max_blocks, max_context_len,
-                      partition_size, dt, sms, aligned16, &plan))
+                      partition_size, dt, sms, (size_t)optin, aligned16, &plan))
     return PKV_ERR_INVALID_ARG;
   const size_t need = pkv::workspace_bytes_for(B, H, head_dim, plan.max_parts);
   if (need > kStaticScratchBytes) return PKV_ERR_WORKSPACE;  // beyond the fixed maximum
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (need > 0) {
-    // The merge counters must start at zero; the array keeps whatever the
-    // previous call left, so clear them on this call's stream.
-    if (cudaMemsetAsync(scratch, 0, align256((size_t)B * H * sizeof(int)), s) != cudaSuccess)
-      return PKV_ERR_CUDA;
-  }
+  // The merge counters must start at zero; the array keeps whatever the
+  // previous call left, so clear them on this call's stream.
+  if (cudaMemsetAsync(scratch, 0, pkv::workspace_counter_bytes(B, H), s) != cudaSuccess)
+    return PKV_ERR_CUDA;
   return pkv_decode_attention(out, q, k_cache, v_cache, block_tables, context_lens, B, H,
                               num_kv_heads, head_dim, block_size, max_blocks, num_blocks, scale, dt,
-                              max_context_len, partition_size, need > 0 ? scratch : nullptr,
-                              need > 0 ? kStaticScratchBytes : 0, err_flags, stream);
+                              max_context_len, partition_size, scratch, kStaticScratchBytes,
+                              err_flags, stream);
 }

@@ -39,45 +39,69 @@ def test_status_strings_and_version(pkv):
     assert "sm_103a" in pkv.pkv_version()
 
 
-def test_workspace_size(pkv):
-    # one partition covers everything -> no workspace
-    assert pkv.pkv_decode_workspace_size(4, 8, 2, 64, 16, 4, 0, 64) == 0
-    # rows * parts * (D + 2) floats + counters, each region 256-aligned
-    B, H, D, P, cap = 3, 8, 64, 64, 1000
-    parts = -(-cap // P)
-    rows = B * H
+def _ws_bytes(B, H, D, parts):
+    """Workspace layout: one int counter per (sequence, head), then with more
+    than one partition per sequence the partial (m, l) and weighted-V rows;
+    every region 256-byte aligned."""
     al = lambda x: (x + 255) // 256 * 256
-    want = al(rows * 4) + 2 * al(rows * parts * 4) + rows * parts * D * 4
-    assert pkv.pkv_decode_workspace_size(B, H, 2, D, 16, 100, cap, P) == want
+    rows = B * H
+    head = al(rows * 4)
+    return head if parts <= 1 else head + 2 * al(rows * parts * 4) + rows * parts * D * 4
+
+
+def _ws_parts(cap, P):
+    """Partitions per sequence the workspace holds: ceil(cap / P) for an
+    explicit P; automatic: the partition is never below max(64, cap / 64)
+    rounded up to 16, so at most 64."""
+    if not P:
+        P = max(64, -(-(-(-cap // 64)) // 16) * 16)
+    return -(-cap // P)
+
+
+def test_workspace_size(pkv):
+    # one partition covers everything -> only the counters
+    assert pkv.pkv_decode_workspace_size(4, 8, 2, 64, 16, 4, 0, 64) == _ws_bytes(4, 8, 64, 1)
+    B, H, D, P, cap = 3, 8, 64, 64, 1000
+    assert pkv.pkv_decode_workspace_size(B, H, 2, D, 16, 100, cap, P) == \
+        _ws_bytes(B, H, D, _ws_parts(cap, P))
+    for cap in (16, 100, 1000, 4096, 32768):
+        assert pkv.pkv_decode_workspace_size(B, H, 2, D, 16, 4096, cap, 0) == \
+            _ws_bytes(B, H, D, _ws_parts(cap, 0))
     # invalid sizes -> 0
     assert pkv.pkv_decode_workspace_size(4, 6, 4, 64, 16, 8, 0, 0) == 0   # H % KVH
     assert pkv.pkv_decode_workspace_size(4, 8, 2, 64, 16, 8, 0, 24) == 0  # P % 16
     # auto mode: never more than 64 partitions per sequence
     auto = pkv.pkv_decode_workspace_size(8, 32, 8, 128, 16, 2048, 0, 0)
-    assert auto == pkv.pkv_decode_workspace_size(8, 32, 8, 128, 16, 2048, 0, 512)
+    assert auto == _ws_bytes(8, 32, 128, 64)
 
 
 def test_plan(pkv):
     import torch
+    # tensor-core kernel (1): about four CTAs per resident slot, >= 1024 tokens
     P, mp, kern = pkv.pkv_decode_plan(64, 32, 8, 128, 16, 256, 4096, 0, torch.bfloat16, 152)
-    assert kern == 1 and P % 16 == 0 and P >= 256 and mp == -(-4096 // P)
+    assert kern == 1 and P % 16 == 0 and P >= 1024 and mp == -(-4096 // P)
+    # enough (sequence, head) units to fill the GPU: no split
+    P, mp, kern = pkv.pkv_decode_plan(256, 64, 8, 128, 16, 132, 2080, 0, torch.bfloat16, 152)
+    assert kern == 1 and mp == 1
+    # long contexts, few units: split
+    P, mp, kern = pkv.pkv_decode_plan(8, 32, 8, 128, 16, 2048, 32768, 0, torch.bfloat16, 152)
+    assert kern == 1 and 1024 <= P <= 4096 and mp > 1
+    P, mp, kern = pkv.pkv_decode_plan(64, 32, 8, 128, 16, 256, 4096, 48, torch.bfloat16, 152)
+    assert kern == 1 and (P, mp) == (48, -(-4096 // 48))
     # the workspace sized in auto mode always fits the automatic plan
     for B, H, KVH, D, bs, mb, cap in ((64, 32, 8, 128, 16, 256, 4096), (8, 32, 8, 128, 16, 2048, 32768),
                                       (128, 16, 1, 256, 32, 256, 8192), (1, 4, 4, 64, 16, 100, 0)):
         P, mp, _ = pkv.pkv_decode_plan(B, H, KVH, D, bs, mb, cap, 0, torch.bfloat16, 152)
         assert mp <= 64
         ws = pkv.pkv_decode_workspace_size(B, H, KVH, D, bs, mb, cap, 0)
-        rows = B * H
-        al = lambda x: (x + 255) // 256 * 256
-        need = 0 if mp <= 1 else al(rows * 4) + 2 * al(rows * mp * 4) + rows * mp * D * 4
-        assert ws >= need
+        assert ws >= _ws_bytes(B, H, D, mp)
     # fp32, odd head_dim or block size not a multiple of 16 -> CUDA-core kernel
     assert pkv.pkv_decode_plan(4, 4, 2, 64, 16, 8, 0, 0, torch.float32)[2] == 0
     assert pkv.pkv_decode_plan(4, 4, 2, 96, 16, 8, 0, 0, torch.bfloat16)[2] == 0
     assert pkv.pkv_decode_plan(4, 4, 2, 128, 8, 8, 0, 0, torch.bfloat16)[2] == 0
     assert pkv.pkv_decode_plan(4, 4, 2, 128, 32, 8, 0, 0, torch.float16)[2] == 1
-    # explicit partition size is honoured
-    assert pkv.pkv_decode_plan(4, 4, 2, 128, 16, 64, 0, 48, torch.bfloat16)[:2] == (48, -(-1024 // 48))
+    # explicit partition size is honoured (CUDA-core kernel: one slot per partition)
+    assert pkv.pkv_decode_plan(4, 4, 2, 96, 16, 64, 0, 48, torch.bfloat16)[:2] == (48, -(-1024 // 48))
     # invalid -> 0
     assert pkv.pkv_decode_plan(4, 6, 4, 128, 16, 8, 0, 0, torch.bfloat16)[0] == 0
 

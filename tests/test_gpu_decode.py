@@ -69,7 +69,7 @@ def test_tensor_core_shapes(dtype, D, H, KVH):
     case = random_paged_case(D + H * 7 + KVH, lens, H=H, KVH=KVH, D=D, bs=bs, dtype=dtype)
     P, _, kern = pkv.pkv_decode_plan(len(lens), H, KVH, D, bs, case["block_tables"].shape[1],
                                      dtype=dtype)
-    assert kern == 1
+    assert kern == 1  # TMA + tensor-core kernel
     args = (case["q"], case["k_cache"], case["v_cache"], case["block_tables"], case["context_lens"],
             1.0 / math.sqrt(D))
     for ps in (0, 32):
@@ -202,7 +202,7 @@ def test_workspace_reused_across_calls():
     assert int(ws.buffer[: 4 * 8 * 4].view(torch.int32).abs().sum()) == 0
 
 
-def test_missing_workspace_is_an_error():
+def test_missing_or_short_workspace_is_an_error():
     case = random_paged_case(1, [300], H=4, KVH=2, D=128, bs=16, dtype=torch.bfloat16)
     args = [t.to(DEV) for t in (case["q"], case["k_cache"], case["v_cache"], case["block_tables"],
                                 case["context_lens"])]
@@ -210,6 +210,50 @@ def test_missing_workspace_is_an_error():
     with pytest.raises(pkv.PkvError) as e:
         pkv.pkv_decode_attention(out, *args, 0.1, partition_size=64)
     assert e.value.status == 4
+    short = torch.zeros(256, dtype=torch.uint8, device=DEV)
+    with pytest.raises(pkv.PkvError) as e:
+        pkv.pkv_decode_attention(out, *args, 0.1, partition_size=64, workspace=short)
+    assert e.value.status == 4
+
+
+@pytest.mark.parametrize("lens", [
+    [1] * 300,                                   # many one-chunk sequences
+    [5000],                                      # one sequence split into many partitions
+    [3],                                         # a single tiny sequence
+    [0, 0, 0],                                   # no work at all: only zero rows
+    [1, 2, 3, 16, 17, 4096, 33, 1000, 0, 15] * 3,
+])
+@pytest.mark.parametrize("partition_size", [0, 16, 160])
+def test_work_distribution(lens, partition_size):
+    """Ragged, tiny, single and empty workloads; automatic and explicit
+    partition sizes (16 tokens: every chunk its own partition, most
+    sequences merged from many partials); two calls on one workspace."""
+    B = len(lens)
+    case = random_paged_case(len(lens) + sum(lens) % 97, lens, H=8, KVH=2, D=128, bs=16,
+                             dtype=torch.bfloat16, extra_blocks=1)
+    assert pkv.pkv_decode_plan(B, 8, 2, 128, 16, case["block_tables"].shape[1])[2] == 1
+    args = (case["q"], case["k_cache"], case["v_cache"], case["block_tables"], case["context_lens"], 0.1)
+    ws = pkv.DecodeWorkspace(B, 8, 2, 128, 16, case["block_tables"].shape[1], 0, partition_size,
+                             device=DEV)
+    want = oracle_decode(*args)
+    for call in range(2):  # the merge counters reset themselves between calls
+        out, err = gpu_decode(*args, partition_size=partition_size, workspace=ws)
+        assert err == 0
+        assert_close(out, want, torch.bfloat16, f"call {call}")
+    assert int(ws.buffer[: B * 8 * 4].view(torch.int32).abs().sum()) == 0
+
+
+def test_large_batch():
+    """2100 short sequences in one call."""
+    lens = [1 + (i * 37) % 200 for i in range(2100)]
+    case = random_paged_case(9, lens, H=4, KVH=1, D=64, bs=16, dtype=torch.bfloat16, extra_blocks=1)
+    assert pkv.pkv_decode_plan(len(lens), 4, 1, 64, 16, case["block_tables"].shape[1])[2] == 1
+    args = (case["q"], case["k_cache"], case["v_cache"], case["block_tables"], case["context_lens"], 0.125)
+    want = oracle_decode(*args)
+    for ps in (0, 48):
+        out, err = gpu_decode(*args, partition_size=ps)
+        assert err == 0
+        assert_close(out, want, torch.bfloat16, f"P={ps}")
 
 
 def test_step_loop_in_cuda_graph():
