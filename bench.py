@@ -58,6 +58,22 @@ def config_block(dec_bytes=None, wr_bytes=None, world=1):
     return c
 
 
+def decode_traffic():
+    """DRAM bytes per decode launch from the committed ncu capture, or None
+    when the decode kernel's sources have changed since it was taken."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "decode_traffic.txt")
+    try:
+        rec = dict(line.split() for line in open(path) if line.strip() and not line.startswith("#"))
+        h = hashlib.sha256()
+        for f in ("pkv_decode_tc.cu", "pkv_device.cuh", "pkv_api.cu"):
+            with open(os.path.join(ROOT, "paged_kv_cache_67_gb300", "csrc", f), "rb") as fh:
+                h.update(fh.read())
+        return int(rec["bytes_per_launch"]) if h.hexdigest() == rec["sources_sha256"] else None
+    except Exception:
+        return None
+
+
 def hbm_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -427,7 +443,7 @@ def run_gpu(args, world, rank, local):
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": config_block(dec_bytes, wr_bytes, world),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "traffic": None,
+                     "frac": round(achieved / peak, 4), "traffic": decode_traffic(),
                      "kernel": "pkv_decode_tc_kernel<128, bf16>",
                      "peak_source": ("measured (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
                                      else "fallback 6.8 TB/s"),
