@@ -157,9 +157,9 @@ PKV_API size_t pkv_decode_workspace_size(int B, int H, int num_kv_heads, int hea
  *                 CTAs whose (max, sum, weighted-V) partials are merged in the
  *                 workspace with a log-sum-exp rescale.
  *   workspace, workspace_bytes  device scratch of at least
- *                 pkv_decode_workspace_size(...) bytes, zero-filled before
- *                 first use (may be NULL/0 when no context is longer than one
- *                 partition)
+ *                 pkv_decode_workspace_size(...) bytes, 256-byte aligned,
+ *                 zero-filled before first use; always required (it holds the
+ *                 merge counters even when nothing is split)
  *   err_flags     device int or NULL (PKV_FLAG_BLOCK_OUT_OF_RANGE,
  *                 PKV_FLAG_CONTEXT_*, PKV_FLAG_TIMEOUT)
  * Supported: H % num_kv_heads == 0; head_dim a multiple of 8 in [8, 512] (fp32:
