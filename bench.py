@@ -1,22 +1,28 @@
 """Benchmark: paged KV-cache write + paged decode attention on one GB300.
 
-One step = pkv_write of the batch's new tokens (one per sequence, the last
-token of its context) followed by pkv_decode_attention over the whole paged
-context, on the Llama-3-8B-shaped decode workload (B=64, H=32, KVH=8,
-D=128, block 16, context lengths uniform in [512, 4096], shuffled physical
-blocks, garbage table tails, bf16), synthetic and seeded.
+One step = the batch's new tokens (one per sequence, the last token of its
+context) written into the paged cache, then decode attention over the whole
+paged context, on the Llama-3-8B-shaped decode workload (B=64, H=32,
+KVH=8, D=128, block 16, context lengths uniform in [512, 4096], shuffled
+physical blocks, garbage table tails, bf16), synthetic and seeded.  By
+default a step is one pkv_write_decode_attention launch (`--mode
+two-launch`: pkv_write, then pkv_decode_attention).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+                    [--workload NAME] [--mode fused|two-launch] [--graph]
 
 Prints one JSON line.  `value` is the step's algorithmic bytes (K/V rows
 used, q, out, table prefix, lengths, plus the write's rows and slots) per
 second of device time over the K timed steps, all ranks together.  The
-`roofline` block is for the decode kernel alone: its algorithmic bytes over
-its mean launch time from CUDA events on its stream, against the measured
-HBM copy bandwidth.  `--impl reference` times the oracle (plain fp64 C on
-the host cores) on bounded samples of the same workload instead.
-Under torchrun (N > 1) every rank runs its own independent batch (weak
-scaling, no collective on the data path); time is the max over ranks.
+`roofline` block is for the attention kernel (with the write, when fused):
+its algorithmic bytes over its mean launch time from CUDA events on its
+stream, against the measured HBM copy bandwidth.  `--impl reference` times
+the oracle (plain fp64 C on the host cores) on bounded samples of the same
+workload instead.  Under torchrun (N > 1) every rank runs its own
+independent batch (weak scaling, no collective on the data path); time is
+the max over ranks.  `--workload` picks another of the five workloads (the
+per-step one cycles through its 32 steps); `--graph` replays the timed
+steps from one CUDA graph.
 """
 from __future__ import annotations
 
@@ -45,12 +51,28 @@ FALLBACK_HBM_GBS = 6800.0
 
 # ------------------------------------------------------------------ helpers
 
-def config_block(dec_bytes=None, wr_bytes=None, world=1):
-    c = {"workload": (f"{WORKLOAD}: B=64 H=32 KVH=8 D=128 block_size=16, context_lens "
-                      "U[512,4096], shuffled blocks from a 1.25x pool, garbage table tails, "
-                      "q/k/v~N(0,1) bf16; step = pkv_write of 64 new tokens + "
-                      "pkv_decode_attention"),
+WORKLOAD_TEXT = {
+    "llama8b_bf16": ("B=64 H=32 KVH=8 D=128 block_size=16, context_lens U[512,4096], shuffled "
+                     "blocks from a 1.25x pool, garbage table tails, q/k/v~N(0,1) bf16"),
+    "long_bf16": ("B=8 H=32 KVH=8 D=128 block_size=16, context_lens U[16384,32768], shuffled "
+                  "blocks, garbage table tails, bf16"),
+    "mqa_bf16": ("B=128 H=16 KVH=1 D=256 block_size=32, context_lens log-uniform [1,8192], "
+                 "shuffled blocks, garbage table tails, bf16"),
+    "step_bf16": ("256 sequences (200 live, 56 padded: slot -1, length 0) H=64 KVH=8 D=128 "
+                  "block_size=16, context_lens U[1,2048], 32 decode steps cycled, bf16"),
+    "tiny_fp32": "B=4 H=4 KVH=2 D=64 block_size=16, context_lens U[1,100], fp32",
+}
+
+
+def config_block(workload=WORKLOAD, mode="fused", dec_bytes=None, wr_bytes=None, world=1,
+                 graph=False):
+    step = ("pkv_write_decode_attention (new token of every sequence written, then attention "
+            "over the context that counts it, one launch)" if mode == "fused" else
+            "pkv_write of the new tokens, then pkv_decode_attention")
+    c = {"workload": f"{workload}: {WORKLOAD_TEXT[workload]}; step = {step}",
          "parallelism": f"{world} independent replica batch(es), no collective"}
+    if graph:
+        c["launch"] = "the timed steps replayed from one CUDA graph"
     if dec_bytes is not None:
         c["l2"] = f"inputs larger than L2 ({dec_bytes / 1e6:.0f} MB of K/V per step, no flush)"
         c["decode_bytes_per_step"] = dec_bytes
@@ -58,20 +80,33 @@ def config_block(dec_bytes=None, wr_bytes=None, world=1):
     return c
 
 
-def decode_traffic():
-    """DRAM bytes per decode launch from the committed ncu capture, or None
-    when the decode kernel's sources have changed since it was taken."""
-    import hashlib
+def decode_traffic(kernel, workload):
+    """DRAM bytes per launch of `kernel` on `workload` from the committed ncu
+    capture, or None when there is none for them or the kernel's sources
+    have changed since it was taken."""
     path = os.path.join(ROOT, "profiles", "decode_traffic.txt")
     try:
-        rec = dict(line.split() for line in open(path) if line.strip() and not line.startswith("#"))
-        h = hashlib.sha256()
-        for f in ("pkv_decode_tc.cu", "pkv_device.cuh", "pkv_api.cu"):
-            with open(os.path.join(ROOT, "paged_kv_cache_67_gb300", "csrc", f), "rb") as fh:
-                h.update(fh.read())
-        return int(rec["bytes_per_launch"]) if h.hexdigest() == rec["sources_sha256"] else None
+        rec = {}
+        for line in open(path):
+            if line.strip() and not line.startswith("#"):
+                key, val = line.split(None, 1)
+                rec[key] = val.strip()
+        if (sources_sha256() != rec["sources_sha256"] or rec["kernel"] != kernel
+                or rec["workload"] != workload):
+            return None
+        return int(rec["bytes_per_launch"])
     except Exception:
         return None
+
+
+def sources_sha256():
+    """Digest of the sources the decode kernels are built from."""
+    import hashlib
+    h = hashlib.sha256()
+    for f in ("pkv_decode_tc.cu", "pkv_device.cuh", "pkv_api.cu"):
+        with open(os.path.join(ROOT, "paged_kv_cache_67_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
 
 
 def hbm_peak():
@@ -226,7 +261,7 @@ def cpu_baseline(inp, elem, seconds=10.0):
             break
     dt = time.perf_counter() - t0
     return {"value": done_bytes / dt / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
-            "sample": (f"{done_units} (sequence, KV head) units of the {WORKLOAD} workload "
+            "sample": (f"{done_units} (sequence, KV head) units of the {inp.cfg.name} workload "
                        f"({done_units / len(units):.2f} decode passes over its {len(units)} units), "
                        f"fp64 C oracle, {dt:.1f} s on {threads} threads")}
 
@@ -236,8 +271,8 @@ def run_reference(args, world, rank):
         return
     import oracle
     oracle.build()
-    cfg = wl.CONFIGS[WORKLOAD]
-    elem = 2
+    cfg = wl.CONFIGS[args.workload]
+    elem = torch.empty((), dtype=cfg.dtype).element_size()
     inp = wl.make_decode_inputs(cfg, seed=1234, device="cpu")
     cpu = cpu_copy(inp)
     threads = max(1, min(os.cpu_count() or 1, 64))
@@ -266,7 +301,8 @@ def run_reference(args, world, rank):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(dt / max(args.steps, 1) * 1e3, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": dict(config_block(), sample=f"{threads} (sequence, KV head) units per step"),
+        "config": dict(config_block(args.workload, args.mode),
+                       sample=f"{threads} (sequence, KV head) units per step"),
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads,
                          "kind": "oracle",
                          "sample": f"{threads} (sequence, KV head) units per step, rotating"},
@@ -278,6 +314,39 @@ def run_reference(args, world, rank):
 
 # -------------------------------------------------------------- GPU (lib)
 
+def make_step_inputs(cfg, inp, rank, dev, elem):
+    """Device inputs of each distinct step (one for a single-step workload:
+    the new token is the last of every context; the per-step workload's 32
+    appends otherwise) with their algorithmic bytes."""
+    steps = []
+    if cfg.steps > 1:
+        st = wl.make_steps(inp, seed=4321 + rank, device=dev)
+        lens_c, slots_c = st.lens.cpu(), st.slots.cpu()
+        for s in range(cfg.steps):
+            steps.append(dict(q=st.q[s], k=st.k[s], v=st.v[s], slots=st.slots[s],
+                              tables=st.tables[s], lens=st.lens[s],
+                              dec=wl.decode_bytes(lens_c[s], cfg.B, cfg.H, cfg.KVH, cfg.D, cfg.bs, elem),
+                              wr=wl.write_bytes(slots_c[s], cfg.KVH, cfg.D, elem)))
+    else:
+        positions = [int(n) - 1 if int(n) > 0 else None for n in inp.context_lens]
+        wb = wl.make_write_batch(inp, positions, seed=4321 + rank, device=dev)
+        steps.append(dict(q=inp.q, k=wb.k, v=wb.v, slots=wb.slot_mapping,
+                          tables=inp.block_tables.to(dev), lens=inp.context_lens.to(dev),
+                          dec=wl.decode_bytes(inp.context_lens, cfg.B, cfg.H, cfg.KVH, cfg.D,
+                                              cfg.bs, elem),
+                          wr=wl.write_bytes(wb.slot_mapping.cpu(), cfg.KVH, cfg.D, elem)))
+    return steps
+
+
+def kernel_name(cfg, mode):
+    import paged_kv_cache_67_gb300 as pkv
+    P, _, kern = pkv.pkv_decode_plan(cfg.B, cfg.H, cfg.KVH, cfg.D, cfg.bs, cfg.table_width,
+                                     dtype=cfg.dtype)
+    t = {torch.bfloat16: "bf16", torch.float16: "fp16", torch.float32: "fp32"}[cfg.dtype]
+    base = f"pkv_decode_tc_kernel<{cfg.D}, {t}" if kern == 1 else f"pkv_decode_simt_kernel<{t}"
+    return base + (", append>" if mode == "fused" else ">")
+
+
 def run_gpu(args, world, rank, local):
     from paged_kv_cache_67_gb300 import build as libbuild
     import paged_kv_cache_67_gb300 as pkv
@@ -285,37 +354,48 @@ def run_gpu(args, world, rank, local):
     libbuild.build()
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    cfg = wl.CONFIGS[WORKLOAD]
-    elem = 2
+    cfg = wl.CONFIGS[args.workload]
+    elem = torch.empty((), dtype=cfg.dtype).element_size()
     inp = wl.make_decode_inputs(cfg, seed=1234 + rank, device=dev)
-    positions = [int(n) - 1 for n in inp.context_lens]
-    wb = wl.make_write_batch(inp, positions, seed=4321 + rank, device=dev)
-    tables = inp.block_tables.to(dev)
-    lens = inp.context_lens.to(dev)
-    q = inp.q
-    out = torch.empty_like(q)
+    steps = make_step_inputs(cfg, inp, rank, dev, elem)
+    S = len(steps)
+    out = torch.empty_like(inp.q)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
-    max_ctx = cfg.len_hi
+    max_ctx = cfg.len_hi + (cfg.steps if cfg.steps > 1 else 0)
     ws = pkv.DecodeWorkspace(cfg.B, cfg.H, cfg.KVH, cfg.D, cfg.bs, cfg.table_width, max_ctx, 0,
                              device=dev)
     stream = torch.cuda.current_stream(dev)
-    dec_bytes = wl.decode_bytes(inp.context_lens, cfg.B, cfg.H, cfg.KVH, cfg.D, cfg.bs, elem)
-    wr_bytes = wl.write_bytes(wb.slot_mapping, cfg.KVH, cfg.D, elem)
-    step_bytes = dec_bytes + wr_bytes
+    fused = args.mode == "fused"
     peak, peak_kind = hbm_peak()
 
-    def write():
-        pkv.pkv_write(inp.k_cache, inp.v_cache, wb.k, wb.v, wb.slot_mapping, err_flags=err,
+    def write(st):
+        pkv.pkv_write(inp.k_cache, inp.v_cache, st["k"], st["v"], st["slots"], err_flags=err,
                       stream=stream)
 
-    def decode():
-        pkv.pkv_decode_attention(out, q, inp.k_cache, inp.v_cache, tables, lens, inp.scale,
-                                 max_context_len=max_ctx, workspace=ws, err_flags=err,
-                                 stream=stream)
+    def decode(st):
+        if fused:
+            pkv.pkv_write_decode_attention(out, st["q"], st["k"], st["v"], st["slots"],
+                                           inp.k_cache, inp.v_cache, st["tables"], st["lens"],
+                                           inp.scale, max_context_len=max_ctx, workspace=ws,
+                                           err_flags=err, stream=stream)
+        else:
+            pkv.pkv_decode_attention(out, st["q"], inp.k_cache, inp.v_cache, st["tables"],
+                                     st["lens"], inp.scale, max_context_len=max_ctx,
+                                     workspace=ws, err_flags=err, stream=stream)
+
+    def step(i, ev=None):
+        st = steps[i % S]
+        if not fused:
+            write(st)
+        if ev is not None:
+            ev[0].record(stream)
+        decode(st)
+        if ev is not None:
+            ev[1].record(stream)
 
     extra = {}
     if not args.only_decode:
-        # write_kv on a bulk fill (every context token, ~147k tokens): GB/s
+        # write_kv on a bulk fill (every context token of the batch): GB/s
         bulk = wl.make_bulk_fill(inp, seed=99 + rank, device=dev)
         bulk_bytes = wl.write_bytes(bulk.slot_mapping, cfg.KVH, cfg.D, elem)
 
@@ -355,13 +435,27 @@ def run_gpu(args, world, rank, local):
         extra["hbm_copy_gbs_in_run"] = round(10 * 2 * src.numel() * 2 / (e0.elapsed_time(e1) * 1e-3) / 1e9, 1)
         del src, dst
 
-    # warm-up
-    for _ in range(args.warmup):
-        write()
-        decode()
+    # warm-up (every distinct step at least once)
+    for i in range(max(args.warmup, S)):
+        step(i)
     torch.cuda.synchronize()
     if int(err.item()) != 0:
         raise RuntimeError(f"device error flags {int(err.item()):#x} during warm-up")
+
+    graph = None
+    if args.graph:
+        # the K timed steps as one CUDA graph (captured on a side stream)
+        cap = torch.cuda.Stream(dev)
+        cap.wait_stream(stream)
+        graph = torch.cuda.CUDAGraph()
+        outer = stream
+        with torch.cuda.stream(cap):
+            stream = cap
+            with torch.cuda.graph(graph, stream=cap):
+                for i in range(args.steps):
+                    step(i)
+            stream = outer
+        torch.cuda.synchronize()
 
     # timed region: K steps; each decode launch bracketed by events on its stream
     dec_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
@@ -372,82 +466,58 @@ def run_gpu(args, world, rank, local):
     torch.cuda.nvtx.range_push("timed")
     with ClockSampler(local) as clocks:
         t_start.record(stream)
-        for i in range(args.steps):
-            write()
-            dec_ev[i][0].record(stream)
-            decode()
-            dec_ev[i][1].record(stream)
+        if graph is not None:
+            graph.replay()
+        else:
+            for i in range(args.steps):
+                step(i, dec_ev[i])
         t_end.record(stream)
         torch.cuda.synchronize()
     torch.cuda.nvtx.range_pop()
     barrier(world)
     elapsed = t_start.elapsed_time(t_end) * 1e-3
-    dec_ms = statistics.mean(a.elapsed_time(b) for a, b in dec_ev)
-    launches = 2 * args.steps
+    if graph is None:
+        dec_ms = statistics.mean(a.elapsed_time(b) for a, b in dec_ev)
+    else:
+        dec_ms = elapsed * 1e3 / args.steps  # back-to-back graph nodes: the per-step time
+    launches = args.steps * (1 if fused else 2)
     if int(err.item()) != 0:
         raise RuntimeError(f"device error flags {int(err.item()):#x} in the timed region")
-    value, tmax, _ = aggregate(elapsed, step_bytes * args.steps / 1e9, world, dev)
+    step_bytes = [steps[i % S]["dec"] + steps[i % S]["wr"] for i in range(args.steps)]
+    value, tmax, _ = aggregate(elapsed, sum(step_bytes) / 1e9, world, dev)
+    # the timed kernel's algorithmic bytes: the fused launch does the write too
+    kern_bytes = statistics.mean(steps[i % S]["dec"] + (steps[i % S]["wr"] if fused else 0)
+                                 for i in range(args.steps))
+    dec_bytes = statistics.mean(st["dec"] for st in steps)
+    wr_bytes = statistics.mean(st["wr"] for st in steps)
 
     e2e = None
     if not args.only_decode:
-        # end to end through the public API: pinned host inputs in, result out
-        h_q = q.cpu().pin_memory()
-        h_k, h_v = wb.k.cpu().pin_memory(), wb.v.cpu().pin_memory()
-        h_slots = wb.slot_mapping.cpu().pin_memory()
-        h_tables, h_lens = inp.block_tables.cpu().pin_memory(), inp.context_lens.cpu().pin_memory()
-        h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-        d_q, d_k, d_v = torch.empty_like(q), torch.empty_like(wb.k), torch.empty_like(wb.v)
-        d_slots, d_tables, d_lens = (torch.empty_like(wb.slot_mapping), torch.empty_like(tables),
-                                     torch.empty_like(lens))
-        h2d = sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v, h_slots, h_tables, h_lens))
-        d2h = h_out.numel() * h_out.element_size()
+        e2e = run_e2e(args, world, dev, pkv, inp, steps, out, ws, err, stream, max_ctx, fused,
+                      sum(step_bytes))
 
-        def e2e_step():
-            d_q.copy_(h_q, non_blocking=True)
-            d_k.copy_(h_k, non_blocking=True)
-            d_v.copy_(h_v, non_blocking=True)
-            d_slots.copy_(h_slots, non_blocking=True)
-            d_tables.copy_(h_tables, non_blocking=True)
-            d_lens.copy_(h_lens, non_blocking=True)
-            pkv.pkv_write(inp.k_cache, inp.v_cache, d_k, d_v, d_slots, err_flags=err, stream=stream)
-            pkv.pkv_decode_attention(out, d_q, inp.k_cache, inp.v_cache, d_tables, d_lens, inp.scale,
-                                     max_context_len=max_ctx, workspace=ws, err_flags=err,
-                                     stream=stream)
-            h_out.copy_(out, non_blocking=True)
-            stream.synchronize()  # the caller reads the result every step
-
-        for _ in range(max(3, args.warmup)):
-            e2e_step()
-        barrier(world)
-        torch.cuda.synchronize()
-        t0 = time.perf_counter()
-        for _ in range(args.steps):
-            e2e_step()
-        torch.cuda.synchronize()
-        e2e_elapsed = time.perf_counter() - t0
-        barrier(world)
-        e2e_value, _, _ = aggregate(e2e_elapsed, step_bytes * args.steps / 1e9, world, dev)
-        e2e = {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": d2h}
-
-    achieved = dec_bytes / (dec_ms * 1e-3) / 1e9
+    achieved = kern_bytes / (dec_ms * 1e-3) / 1e9
     if rank != 0:
         return None
     cpu = None
     if world == 1 and not args.only_decode and not args.no_cpu_baseline:
         cpu = cpu_baseline(inp, elem)
+    kname = kernel_name(cfg, args.mode)
+    dt = {torch.bfloat16: "bf16", torch.float16: "fp16", torch.float32: "fp32"}[cfg.dtype]
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(tmax / args.steps * 1e3, 4), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": config_block(dec_bytes, wr_bytes, world),
+        "scaling": "weak", "vs_baseline": None, "dtype": dt, "data": "synthetic",
+        "config": config_block(args.workload, args.mode, round(dec_bytes), round(wr_bytes), world,
+                               args.graph),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "traffic": decode_traffic(),
-                     "kernel": "pkv_decode_tc_kernel<128, bf16>",
+                     "frac": round(achieved / peak, 4),
+                     "traffic": decode_traffic(kname, args.workload),
+                     "kernel": kname, "bytes_per_launch": round(kern_bytes),
                      "peak_source": ("measured (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
                                      else "fallback 6.8 TB/s"),
-                     "decode_us": round(dec_ms * 1e3, 2)},
+                     "kernel_us": round(dec_ms * 1e3, 2)},
         **extra,
         "e2e": e2e,
         "gpu_launches": launches,
@@ -456,6 +526,49 @@ def run_gpu(args, world, rank, local):
     }
     print(json.dumps(line), flush=True)
     return line
+
+
+def run_e2e(args, world, dev, pkv, inp, steps, out, ws, err, stream, max_ctx, fused, total_bytes):
+    """The same steps end to end through the public API: each step's inputs
+    copied in from pinned host memory, the output read back and waited for."""
+    S = len(steps)
+    host = [{k: steps[s][k].cpu().pin_memory() for k in ("q", "k", "v", "slots", "tables", "lens")}
+            for s in range(S)]
+    dbuf = {k: torch.empty_like(steps[0][k]) for k in ("q", "k", "v", "slots", "tables", "lens")}
+    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host[0].values())
+    d2h = h_out.numel() * h_out.element_size()
+
+    def e2e_step(i):
+        for k, t in host[i % S].items():
+            dbuf[k].copy_(t, non_blocking=True)
+        if fused:
+            pkv.pkv_write_decode_attention(out, dbuf["q"], dbuf["k"], dbuf["v"], dbuf["slots"],
+                                           inp.k_cache, inp.v_cache, dbuf["tables"], dbuf["lens"],
+                                           inp.scale, max_context_len=max_ctx, workspace=ws,
+                                           err_flags=err, stream=stream)
+        else:
+            pkv.pkv_write(inp.k_cache, inp.v_cache, dbuf["k"], dbuf["v"], dbuf["slots"],
+                          err_flags=err, stream=stream)
+            pkv.pkv_decode_attention(out, dbuf["q"], inp.k_cache, inp.v_cache, dbuf["tables"],
+                                     dbuf["lens"], inp.scale, max_context_len=max_ctx,
+                                     workspace=ws, err_flags=err, stream=stream)
+        h_out.copy_(out, non_blocking=True)
+        stream.synchronize()  # the caller reads the result every step
+
+    for i in range(max(3, args.warmup, S)):
+        e2e_step(i)
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    e2e_elapsed = time.perf_counter() - t0
+    barrier(world)
+    e2e_value, _, _ = aggregate(e2e_elapsed, total_bytes / 1e9, world, dev)
+    return {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h}
 
 
 def main():
@@ -467,6 +580,13 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only-decode", action="store_true",
                     help="warm-up + timed steps only (no bulk fill, e2e or CPU baseline): for profiling")
+    ap.add_argument("--workload", default=WORKLOAD, choices=sorted(wl.CONFIGS),
+                    help="the batch the steps run on (default: the Llama-3-8B-shaped decode)")
+    ap.add_argument("--mode", default="fused", choices=["fused", "two-launch"],
+                    help="fused: one pkv_write_decode_attention launch per step; two-launch: "
+                         "pkv_write then pkv_decode_attention")
+    ap.add_argument("--graph", action="store_true",
+                    help="replay the timed steps from one CUDA graph")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

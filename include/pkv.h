@@ -85,6 +85,11 @@ typedef enum pkv_dtype {
                                             sequence unspecified */
 #define PKV_FLAG_TIMEOUT 0x20            /* a bounded wait for an asynchronous copy ran out
                                             (should never happen); outputs unspecified */
+#define PKV_FLAG_APPEND_MISMATCH 0x40    /* pkv_write_decode_attention: a kept slot is not the
+                                            slot of position context_lens[b] - 1 through
+                                            block_tables (or context_lens[b] == 0); the token
+                                            is still written, that sequence's output is
+                                            unspecified */
 
 /*
  * pkv_write -- write_kv / reshape_and_cache.
@@ -212,6 +217,45 @@ PKV_API pkv_status pkv_decode_attention_static(void *out, const void *q, const v
                                                pkv_dtype dt, int max_context_len,
                                                int partition_size, int *err_flags,
                                                pkv_stream_t stream);
+
+/*
+ * pkv_write_decode_attention -- one decode step in one launch: pkv_write of
+ * each sequence's new token followed by pkv_decode_attention over contexts
+ * that already count it.
+ * Definition: course page "P09 · Paged KV 写入 + decode attention（参考实现）",
+ * section 题面速览 -- a decode step first writes the new token's K/V to
+ * cache[slot // bs, slot % bs] and then reads the paged context; the result
+ * is that of the two calls above made one after the other.
+ *
+ *   k, v          [B, num_kv_heads, head_dim]: the new token of sequence b
+ *                 starts at element b * k_token_stride (resp. v_token_stride)
+ *   slot_mapping  [B] int64: slot of sequence b's new token; negative = no
+ *                 new token (padding), nothing written for b
+ *   everything else as in pkv_decode_attention (k_cache, v_cache are
+ *   written in place at the kept slots).
+ * Precondition (the decode append): a kept slot_mapping[b] is the slot of
+ * logical position context_lens[b] - 1 of sequence b,
+ *   block_tables[b, (n-1) / bs] * bs + (n-1) % bs,   n = context_lens[b],
+ * and no other sequence's context reads that slot.  The kernel checks the
+ * first part and raises PKV_FLAG_APPEND_MISMATCH when it does not hold.
+ * The launch that reads position n-1 takes the new token's K/V from k/v
+ * directly, so it does not wait for its own cache write; one CTA per
+ * (sequence, KV head) writes the cache row.  The cache ends bit-identical
+ * to pkv_write's; the output is bit-identical to pkv_write +
+ * pkv_decode_attention with the same partition size.
+ * Additional requirements: k, v, k_cache, v_cache 16-byte aligned;
+ * head_dim * element size a multiple of 16 bytes; k_token_stride and
+ * v_token_stride >= num_kv_heads * head_dim and multiples of 16 bytes.
+ * Errors: those of pkv_decode_attention; PKV_ERR_INVALID_ARG for a NULL
+ * k, v or slot_mapping or a misaligned row.
+ */
+PKV_API pkv_status pkv_write_decode_attention(
+    void *out, const void *q, const void *k, const void *v, int64_t k_token_stride,
+    int64_t v_token_stride, const int64_t *slot_mapping, void *k_cache, void *v_cache,
+    const int32_t *block_tables, const int32_t *context_lens, int B, int H, int num_kv_heads,
+    int head_dim, int block_size, int max_blocks, int64_t num_blocks, float scale, pkv_dtype dt,
+    int max_context_len, int partition_size, void *workspace, size_t workspace_bytes,
+    int *err_flags, pkv_stream_t stream);
 
 /*
  * pkv_decode_plan -- the partition size and the partitions per sequence that

@@ -9,6 +9,7 @@ fallback; if the library is missing or a call fails, an exception is raised.
 from __future__ import annotations
 
 from ._binding import (  # noqa: F401
+    FLAG_APPEND_MISMATCH,
     FLAG_BLOCK_OUT_OF_RANGE,
     FLAG_CONTEXT_NEGATIVE,
     FLAG_CONTEXT_OVER_HINT,
@@ -26,4 +27,5 @@ from ._binding import (  # noqa: F401
     pkv_status_string,
     pkv_version,
     pkv_write,
+    pkv_write_decode_attention,
 )

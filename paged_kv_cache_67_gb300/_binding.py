@@ -29,6 +29,7 @@ FLAG_CONTEXT_TOO_LONG = 0x4
 FLAG_CONTEXT_NEGATIVE = 0x8
 FLAG_CONTEXT_OVER_HINT = 0x10
 FLAG_TIMEOUT = 0x20
+FLAG_APPEND_MISMATCH = 0x40
 
 _lock = threading.Lock()
 _lib = None
@@ -67,6 +68,11 @@ def load_library():
                                              c_int, c_int, i64, ctypes.c_float, c_int, c_int,
                                              c_int, vp, c_size, vp, vp]
         lib.pkv_decode_attention.restype = c_int
+        lib.pkv_write_decode_attention.argtypes = [vp, vp, vp, vp, i64, i64, vp, vp, vp, vp, vp,
+                                                   c_int, c_int, c_int, c_int, c_int, c_int, i64,
+                                                   ctypes.c_float, c_int, c_int, c_int, vp, c_size,
+                                                   vp, vp]
+        lib.pkv_write_decode_attention.restype = c_int
         lib.pkv_status_string.argtypes = [c_int]
         lib.pkv_status_string.restype = ctypes.c_char_p
         lib.pkv_version.argtypes = []
@@ -161,6 +167,61 @@ class DecodeWorkspace:
         self.nbytes = pkv_decode_workspace_size(B, H, num_kv_heads, head_dim, block_size,
                                                 max_blocks, max_context_len, partition_size)
         self.buffer = torch.zeros(max(self.nbytes, 256), dtype=torch.uint8, device=device)
+
+
+def _decode_checks(out, q, k_cache, v_cache, block_tables, context_lens):
+    _require(q.dim() == 3 and out.shape == q.shape, "q and out must be [B, H, D]")
+    B, H, D = q.shape
+    _require(k_cache.dim() == 4 and v_cache.shape == k_cache.shape and k_cache.shape[3] == D,
+             "caches must be [nb, bs, KVH, D]")
+    for t in (out, q, k_cache, v_cache, block_tables, context_lens):
+        _require(t.is_contiguous(), "tensors must be contiguous")
+    _require(q.dtype == out.dtype == k_cache.dtype == v_cache.dtype and q.dtype in _DT, "dtype mismatch")
+    _require(block_tables.dtype == torch.int32 and block_tables.dim() == 2 and block_tables.shape[0] == B,
+             "block_tables must be int32 [B, max_blocks]")
+    _require(context_lens.dtype == torch.int32 and context_lens.shape == (B,), "context_lens must be int32 [B]")
+    dev = q.device
+    _require(dev.type == "cuda" and all(t.device == dev for t in (out, k_cache, v_cache, block_tables,
+                                                                   context_lens)),
+             "all tensors must be on the same CUDA device")
+    return dev
+
+
+def _workspace_arg(workspace):
+    if workspace is None:
+        return None, 0
+    buf = workspace.buffer if isinstance(workspace, DecodeWorkspace) else workspace
+    return _ptr(buf), buf.numel() * buf.element_size()
+
+
+def pkv_write_decode_attention(out, q, k, v, slot_mapping, k_cache, v_cache, block_tables,
+                               context_lens, scale: float, max_context_len: int = 0,
+                               partition_size: int = 0, workspace=None, err_flags=None,
+                               stream=None):
+    """One decode step in one launch: write each sequence's new token k[b], v[b]
+    ([B, KVH, D]) at slot_mapping[b] (int64 [B], negative = none), then paged
+    decode attention into ``out`` [B, H, D] (returned) over contexts that
+    already count the new token (slot_mapping[b] must be the slot of position
+    context_lens[b] - 1)."""
+    lib = load_library()
+    dev = _decode_checks(out, q, k_cache, v_cache, block_tables, context_lens)
+    B, H, D = q.shape
+    nb, bs, kvh, _ = k_cache.shape
+    _require(k.dim() == 3 and v.shape == k.shape and k.shape == (B, kvh, D), "k, v must be [B, KVH, D]")
+    _require(k.stride(2) == 1 and k.stride(1) == D and v.stride(2) == 1 and v.stride(1) == D,
+             "each token's [KVH, D] row must be contiguous")
+    _require(k.dtype == v.dtype == q.dtype, "dtype mismatch")
+    _require(slot_mapping.dtype == torch.int64 and slot_mapping.is_contiguous()
+             and slot_mapping.shape == (B,), "slot_mapping must be contiguous int64 [B]")
+    _require(all(t.device == dev for t in (k, v, slot_mapping)), "all tensors must be on the same CUDA device")
+    ws_ptr, ws_bytes = _workspace_arg(workspace)
+    _check(lib.pkv_write_decode_attention(
+        _ptr(out), _ptr(q), _ptr(k), _ptr(v), k.stride(0) if B > 0 else kvh * D,
+        v.stride(0) if B > 0 else kvh * D, _ptr(slot_mapping), _ptr(k_cache), _ptr(v_cache),
+        _ptr(block_tables), _ptr(context_lens), B, H, kvh, D, bs, block_tables.shape[1], nb,
+        float(scale), _DT[q.dtype], int(max_context_len), int(partition_size), ws_ptr, ws_bytes,
+        _ptr(err_flags), _stream_handle(stream, dev)), "pkv_write_decode_attention")
+    return out
 
 
 def pkv_decode_attention(out, q, k_cache, v_cache, block_tables, context_lens, scale: float,

@@ -173,14 +173,26 @@ PKV_API int pkv_decode_plan(int B, int H, int num_kv_heads, int head_dim, int bl
   return p.P;
 }
 
-PKV_API pkv_status pkv_decode_attention(void *out, const void *q, const void *k_cache,
-                                        const void *v_cache, const int32_t *block_tables,
-                                        const int32_t *context_lens, int B, int H,
-                                        int num_kv_heads, int head_dim, int block_size,
-                                        int max_blocks, int64_t num_blocks, float scale,
-                                        pkv_dtype dt, int max_context_len, int partition_size,
-                                        void *workspace, size_t workspace_bytes, int *err_flags,
-                                        pkv_stream_t stream) {
+}  // extern "C"
+
+namespace pkv {
+
+// New tokens of a fused write + decode launch (see pkv_write_decode_attention).
+struct AppendIn {
+  const void *k, *v;
+  int64_t k_stride, v_stride;
+  const int64_t *slots;
+};
+
+// pkv_decode_attention, and with `app` the fused append of one new token per
+// sequence.
+static pkv_status decode_entry(void *out, const void *q, const void *k_cache, const void *v_cache,
+                               const int32_t *block_tables, const int32_t *context_lens, int B,
+                               int H, int num_kv_heads, int head_dim, int block_size,
+                               int max_blocks, int64_t num_blocks, float scale, pkv_dtype dt,
+                               int max_context_len, int partition_size, void *workspace,
+                               size_t workspace_bytes, int *err_flags, pkv_stream_t stream,
+                               const AppendIn *app) {
   if (B < 0 || B > 65535 || H <= 0 || H > 65535 || num_kv_heads <= 0 || H % num_kv_heads != 0 ||
       head_dim <= 0 || block_size <= 0 || max_blocks < 0 || num_blocks < 0 ||
       num_blocks > 0x7fffffffLL || max_context_len < 0 || partition_size < 0 ||
@@ -233,6 +245,13 @@ PKV_API pkv_status pkv_decode_attention(void *out, const void *q, const void *k_
   a.max_parts = plan.max_parts;
   a.stages = plan.stages;
   a.scale_log2 = scale * kLog2e;
+  if (app) {
+    a.new_slots = app->slots;
+    a.new_k = app->k;
+    a.new_v = app->v;
+    a.new_k_stride = app->k_stride;
+    a.new_v_stride = app->v_stride;
+  }
 
   const size_t need = workspace_bytes_for(B, H, head_dim, plan.max_parts);
   if (!workspace || workspace_bytes < need || reinterpret_cast<uintptr_t>(workspace) % 256)
@@ -252,6 +271,47 @@ PKV_API pkv_status pkv_decode_attention(void *out, const void *q, const void *k_
   }
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   return plan.kernel ? launch_decode_tc(a, plan, dt, s) : launch_decode_simt(a, plan, dt, s);
+}
+
+}  // namespace pkv
+
+extern "C" {
+
+PKV_API pkv_status pkv_decode_attention(void *out, const void *q, const void *k_cache,
+                                        const void *v_cache, const int32_t *block_tables,
+                                        const int32_t *context_lens, int B, int H,
+                                        int num_kv_heads, int head_dim, int block_size,
+                                        int max_blocks, int64_t num_blocks, float scale,
+                                        pkv_dtype dt, int max_context_len, int partition_size,
+                                        void *workspace, size_t workspace_bytes, int *err_flags,
+                                        pkv_stream_t stream) {
+  return decode_entry(out, q, k_cache, v_cache, block_tables, context_lens, B, H, num_kv_heads,
+                      head_dim, block_size, max_blocks, num_blocks, scale, dt, max_context_len,
+                      partition_size, workspace, workspace_bytes, err_flags, stream, nullptr);
+}
+
+PKV_API pkv_status pkv_write_decode_attention(
+    void *out, const void *q, const void *k, const void *v, int64_t k_token_stride,
+    int64_t v_token_stride, const int64_t *slot_mapping, void *k_cache, void *v_cache,
+    const int32_t *block_tables, const int32_t *context_lens, int B, int H, int num_kv_heads,
+    int head_dim, int block_size, int max_blocks, int64_t num_blocks, float scale, pkv_dtype dt,
+    int max_context_len, int partition_size, void *workspace, size_t workspace_bytes,
+    int *err_flags, pkv_stream_t stream) {
+  if (dt != PKV_F32 && dt != PKV_BF16 && dt != PKV_F16) return PKV_ERR_INVALID_ARG;
+  const int64_t row = (int64_t)num_kv_heads * head_dim;
+  const int64_t el = elem_size(dt);
+  if (num_kv_heads <= 0 || head_dim <= 0 || k_token_stride < row || v_token_stride < row ||
+      (k_token_stride * el) % 16 || (v_token_stride * el) % 16 || (head_dim * el) % 16)
+    return PKV_ERR_INVALID_ARG;
+  // the new rows are copied as 16-byte vectors: inputs and cache rows aligned
+  if (B > 0 && (!k || !v || !slot_mapping || reinterpret_cast<uintptr_t>(k) % 16 ||
+                reinterpret_cast<uintptr_t>(v) % 16 || reinterpret_cast<uintptr_t>(slot_mapping) % 8 ||
+                reinterpret_cast<uintptr_t>(k_cache) % 16 || reinterpret_cast<uintptr_t>(v_cache) % 16))
+    return PKV_ERR_INVALID_ARG;
+  const AppendIn app{k, v, k_token_stride, v_token_stride, slot_mapping};
+  return decode_entry(out, q, k_cache, v_cache, block_tables, context_lens, B, H, num_kv_heads,
+                      head_dim, block_size, max_blocks, num_blocks, scale, dt, max_context_len,
+                      partition_size, workspace, workspace_bytes, err_flags, stream, &app);
 }
 
 PKV_API const char *pkv_status_string(pkv_status status) {

@@ -26,7 +26,7 @@ namespace pkv {
 constexpr int kSimtWarps = 4;
 constexpr int kTableWindow = 256;  // table entries staged per window
 
-template <typename T, int EPL, int GH>
+template <typename T, int EPL, int GH, bool kAppend>
 __global__ void __launch_bounds__(32 * kSimtWarps) pkv_decode_simt_kernel(const DecodeArgs a) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   const int D = a.D;
@@ -51,14 +51,25 @@ __global__ void __launch_bounds__(32 * kSimtWarps) pkv_decode_simt_kernel(const 
     if (part == (int)gridDim.x - 1 && hc == 0 && tid == 0) raise_flag(a.err, PKV_FLAG_CONTEXT_OVER_HINT);
     nparts = gridDim.x;
   }
+  // fused append (kAppend): the new token's slot, or -1
+  const long long s_new = kAppend ? append_slot(a, b) : -1LL;
   if (n == 0) {
-    if (part == 0) zero_rows<T>(a, b, head0, nh);
+    if (part == 0) {
+      zero_rows<T>(a, b, head0, nh);
+      if (s_new >= 0 && gc == 0 && w == 0) append_write_row<T>(a, b, kvh, s_new, n, lane);
+    }
     return;
   }
   if (part >= nparts) return;
   const int t0 = part * a.P;
   const int t1 = min(n, t0 + a.P);
   const int bs = a.bs;
+  // Fused append: one CTA per (sequence, KV head) writes the cache row;
+  // every CTA reads position n-1 from the new token's input row instead of
+  // the cache, so no read waits for (or races with) that write.
+  if (s_new >= 0 && gc == 0 && part == nparts - 1 && w == 0)
+    append_write_row<T>(a, b, kvh, s_new, n, lane);
+  const int t_new = s_new >= 0 ? n - 1 : -1;
 
   // Queries of this CTA's heads, scaled into log2 units: s2 = q.k * scale * log2(e).
   const T *qg = reinterpret_cast<const T *>(a.q) + ((size_t)b * a.H + head0) * D;
@@ -95,12 +106,17 @@ __global__ void __launch_bounds__(32 * kSimtWarps) pkv_decode_simt_kernel(const 
       const int lb = t / bs;
       const int phys = s_tbl[lb - lbA];
       const size_t row = ((size_t)phys * bs + (t - lb * bs)) * tok_stride + (size_t)kvh * D;
+      const T *kp = kc + row, *vp = vc + row;
+      if (t == t_new) {
+        kp = reinterpret_cast<const T *>(append_src<T>(a, false, b, kvh));
+        vp = reinterpret_cast<const T *>(append_src<T>(a, true, b, kvh));
+      }
       float kx[EPL], vx[EPL];
 #pragma unroll
       for (int e = 0; e < EPL; ++e) {
         const int d = lane + 32 * e;
-        kx[e] = d < D ? to_f32<T>(kc[row + d]) : 0.f;
-        vx[e] = d < D ? to_f32<T>(vc[row + d]) : 0.f;
+        kx[e] = d < D ? to_f32<T>(kp[d]) : 0.f;
+        vx[e] = d < D ? to_f32<T>(vp[d]) : 0.f;
       }
 #pragma unroll
       for (int r = 0; r < GH; ++r) {
@@ -159,7 +175,10 @@ __global__ void __launch_bounds__(32 * kSimtWarps) pkv_decode_simt_kernel(const 
 template <typename T, int EPL, int GH>
 static pkv_status launch_simt_t(const DecodeArgs &a, const DecodePlan &plan, cudaStream_t stream) {
   dim3 grid(plan.max_parts, a.KVH * plan.gchunks, a.B);
-  pkv_decode_simt_kernel<T, EPL, GH><<<grid, 32 * kSimtWarps, plan.smem_bytes, stream>>>(a);
+  if (a.new_slots)
+    pkv_decode_simt_kernel<T, EPL, GH, true><<<grid, 32 * kSimtWarps, plan.smem_bytes, stream>>>(a);
+  else
+    pkv_decode_simt_kernel<T, EPL, GH, false><<<grid, 32 * kSimtWarps, plan.smem_bytes, stream>>>(a);
   return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 

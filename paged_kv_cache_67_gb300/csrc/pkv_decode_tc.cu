@@ -156,6 +156,7 @@ size_t tc_smem_bytes(int D, int stages) {
   return 1024                                             // alignment slack
          + (size_t)kTcWarps * stages * stage_bytes        // K/V rings
          + (size_t)kTcHeads * (D + 8) * 2                 // Q
+         + (size_t)2 * D * 2                              // fused append: new K and V rows
          + (size_t)kTcWarps * stages * 8                  // mbarriers
          + sizeof(float) * (2 * kTcWarps * kTcHeads + 2 * kTcHeads)  // warp m/l, final m/l
          + sizeof(int) * (4 + 2 * kTcHeads);              // epilogue scratch
@@ -165,7 +166,7 @@ size_t tc_smem_bytes(int D, int stages) {
 // takes chunks w, w+4, ... of the partition through its own ring of
 // `stages` slots; lane 0 issues the TMA loads; table entries are fetched 32
 // at a time by one coalesced load and broadcast by shuffle.
-template <int D, typename T>
+template <int D, typename T, bool kAppend>
 __global__ void __launch_bounds__(32 * kTcWarps, 1)
     pkv_decode_tc_kernel(const __grid_constant__ CUtensorMap tmK,
                          const __grid_constant__ CUtensorMap tmV, const DecodeArgs a) {
@@ -176,7 +177,8 @@ __global__ void __launch_bounds__(32 * kTcWarps, 1)
   const int S = a.stages;
   uint8_t *ring = smem;                                              // [W][S][stage]
   T *sQ = reinterpret_cast<T *>(ring + (size_t)kTcWarps * S * Sh::kStageBytes);
-  uint64_t *bars = reinterpret_cast<uint64_t *>(sQ + kTcHeads * Sh::kQStride);
+  T *sNew = sQ + kTcHeads * Sh::kQStride;                            // [2][D] new K, V rows
+  uint64_t *bars = reinterpret_cast<uint64_t *>(sNew + 2 * D);
   float *s_wm = reinterpret_cast<float *>(bars + kTcWarps * S);     // [W][16]
   float *s_wl = s_wm + kTcWarps * kTcHeads;                         // [W][16]
   float *s_m = s_wl + kTcWarps * kTcHeads;                          // [16]
@@ -189,6 +191,9 @@ __global__ void __launch_bounds__(32 * kTcWarps, 1)
   const int head0 = kvh * a.G + gc * kTcHeads;
   const int nh = min(kTcHeads, a.G - gc * kTcHeads);
 
+  // fused append (kAppend): the new token's slot, or -1 -- loaded first, so
+  // that its latency overlaps the length's
+  const long long s_new = kAppend ? append_slot(a, b) : -1LL;
   const int n = checked_len(a, b, part == 0 && hc == 0 && tid == 0);
   int nparts = (n + a.P - 1) / a.P;
   if (nparts > (int)gridDim.x) {
@@ -196,7 +201,10 @@ __global__ void __launch_bounds__(32 * kTcWarps, 1)
     nparts = gridDim.x;
   }
   if (n == 0) {
-    if (part == 0) zero_rows<T>(a, b, head0, nh);
+    if (part == 0) {
+      zero_rows<T>(a, b, head0, nh);
+      if (s_new >= 0 && gc == 0 && w == 0) append_write_row<T>(a, b, kvh, s_new, n, lane);
+    }
     return;
   }
   if (part >= nparts) return;
@@ -204,6 +212,17 @@ __global__ void __launch_bounds__(32 * kTcWarps, 1)
   const int t1 = min(n, t0 + a.P);
   const int nchunks = (t1 - t0 + kChunk - 1) / kChunk;
   const int nch_w = nchunks > w ? (nchunks - w + kTcWarps - 1) / kTcWarps : 0;
+  // Fused append: the warp whose chunk holds position n-1 overwrites that
+  // row of its shared-memory tile with the new token (so nothing waits for
+  // the cache write); in the one CTA per (sequence, KV head) that writes the
+  // cache row, the same warp stores it.
+  const bool cache_writer = s_new >= 0 && gc == 0 && part == nparts - 1;
+  const bool covers_new = s_new >= 0 && n - 1 >= t0 && n - 1 < t1;
+  int patch_i = -1, patch_row = 0;
+  if (covers_new && ((n - 1 - t0) / kChunk) % kTcWarps == w) {
+    patch_i = (n - 1 - t0) / kChunk / kTcWarps;
+    patch_row = (n - 1 - t0) % kChunk;
+  }
 
   if (lane == 0) {
     for (int s = 0; s < S; ++s) mbar_init(&bars[w * S + s], 1);
@@ -246,6 +265,18 @@ __global__ void __launch_bounds__(32 * kTcWarps, 1)
                     phys, policy);
     }
   };
+  // The patching warp loads the new rows (and checks the slot) before
+  // anything else, so that these loads overlap the first fetches and the
+  // query loads ...
+  uint4 new_kv = make_uint4(0, 0, 0, 0), new_vv = new_kv;
+  int new_ok = 0;
+  if (patch_i >= 0) {
+    if (lane < D / 8) {
+      new_kv = __ldg(append_src<T>(a, false, b, kvh) + lane);
+      new_vv = __ldg(append_src<T>(a, true, b, kvh) + lane);
+    }
+    if (cache_writer && lane == 0) new_ok = append_check(a, b, kvh, s_new, n);
+  }
   // Start the warp's first fetches before staging Q: the copies are in
   // flight while the query tile is loaded.
   const int npro = min(S, nch_w);
@@ -280,6 +311,19 @@ __global__ void __launch_bounds__(32 * kTcWarps, 1)
     }
   };
 
+  // ... and stages the new rows in shared memory and, in the writing CTA,
+  // stores them to the cache row: no registers are held through the main
+  // loop, no other warp waits, and whatever a TMA load reads of that row
+  // before or after the store is overwritten by the patch.
+  if (patch_i >= 0) {
+    const int ok = __shfl_sync(0xffffffffu, new_ok, 0);
+    if (lane < D / 8) {
+      reinterpret_cast<uint4 *>(sNew)[lane] = new_kv;
+      reinterpret_cast<uint4 *>(sNew)[D / 8 + lane] = new_vv;
+      if (ok) append_store<T>(a, kvh, s_new, lane, new_kv, new_vv);
+    }
+  }
+
   float o[Sh::kNTiles][4];
 #pragma unroll
   for (int nt = 0; nt < Sh::kNTiles; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
@@ -296,6 +340,17 @@ __global__ void __launch_bounds__(32 * kTcWarps, 1)
     }
     const int valid = min(kChunk, t1 - (t0 + kChunk * (w + kTcWarps * i)));
     const uint32_t kb = smem_u32(ring + (size_t)(w * S + slot) * Sh::kStageBytes);
+    if (i == patch_i) {  // overwrite row patch_row of the tiles with the new token
+      if (lane < D / 8) {  // 16-byte column lane&7 of box lane>>3, swizzled
+        const uint32_t off = (lane >> 3) * kBoxBytes + patch_row * 128 +
+                             (((lane & 7) ^ (patch_row & 7)) << 4);
+        st_shared_v4(kb + off, reinterpret_cast<const uint4 *>(sNew)[lane]);
+        st_shared_v4(kb + Sh::kBoxes * kBoxBytes + off,
+                     reinterpret_cast<const uint4 *>(sNew)[D / 8 + lane]);
+      }
+      fence_proxy_async_shared();  // the slot is refilled by TMA later
+      __syncwarp();
+    }
     tc_chunk<D, T>(kb, kb + Sh::kBoxes * kBoxBytes, valid, qfrag, o, m0, m1, l0, l1, a.scale_log2,
                    lane);
     __syncwarp();
@@ -316,6 +371,10 @@ __global__ void __launch_bounds__(32 * kTcWarps, 1)
       }
     }
   }
+
+  // The context was cut short (PKV_FLAG_CONTEXT_OVER_HINT): position n-1 was
+  // not read here, but the cache row is still written.
+  if (cache_writer && !covers_new && w == 0) append_write_row<T>(a, b, kvh, s_new, n, lane);
 
   l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
   l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
@@ -429,15 +488,22 @@ static bool allow_smem(K kern, size_t bytes, int *configured) {
   return true;
 }
 
-template <int D, typename T>
-static pkv_status launch_tc_t(const DecodeArgs &a, const DecodePlan &plan, const CUtensorMap &mk,
+template <int D, typename T, bool kAppend>
+static pkv_status launch_tc_k(const DecodeArgs &a, const DecodePlan &plan, const CUtensorMap &mk,
                               const CUtensorMap &mv, cudaStream_t stream) {
-  auto kern = pkv_decode_tc_kernel<D, T>;
+  auto kern = pkv_decode_tc_kernel<D, T, kAppend>;
   static int configured[64] = {0};
   if (!allow_smem(kern, plan.smem_bytes, configured)) return PKV_ERR_CUDA;
   dim3 grid(plan.max_parts, a.KVH * plan.gchunks, a.B);
   kern<<<grid, 32 * kTcWarps, plan.smem_bytes, stream>>>(mk, mv, a);
   return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+template <int D, typename T>
+static pkv_status launch_tc_t(const DecodeArgs &a, const DecodePlan &plan, const CUtensorMap &mk,
+                              const CUtensorMap &mv, cudaStream_t stream) {
+  return a.new_slots ? launch_tc_k<D, T, true>(a, plan, mk, mv, stream)
+                     : launch_tc_k<D, T, false>(a, plan, mk, mv, stream);
 }
 
 template <typename T>

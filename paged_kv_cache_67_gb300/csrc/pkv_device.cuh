@@ -40,6 +40,11 @@ struct DecodeArgs {
   int max_parts;         // partitions the grid covers per sequence (gridDim.x); workspace stride
   int stages;            // pipeline depth per warp (TMA kernel)
   float scale_log2;      // scale * log2(e): scores are kept in log2 units
+  // Fused append (pkv_write_decode_attention); new_slots == nullptr otherwise.
+  const int64_t *new_slots;   // [B] slot of sequence b's new token, negative: none
+  const void *new_k;          // new token of b at element b * new_k_stride
+  const void *new_v;
+  long long new_k_stride, new_v_stride;
 };
 
 __device__ __forceinline__ void raise_flag(int *err, int bit) {
@@ -133,6 +138,18 @@ __device__ __forceinline__ uint64_t l2_evict_first_policy() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
   return p;
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y),
+               "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
+// Orders this thread's generic-proxy shared-memory accesses before later
+// asynchronous-proxy (TMA) accesses of the same locations.
+__device__ __forceinline__ void fence_proxy_async_shared() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {
@@ -355,6 +372,67 @@ __device__ void finish_partition(const DecodeArgs &a, int b, int head0, int nh, 
     out[(row0 + r) * D + d] = from_f32<T>(((acc0 + acc1) + (acc2 + acc3)) * s_invL[r]);
   }
   if (tid == 0) *counter = 0;  // every partition has arrived: ready for the next call
+}
+
+// ------------------------------------------------------------ fused append
+
+// Slot of sequence b's new token, or -1 (no append in this launch, or padding).
+__device__ __forceinline__ long long append_slot(const DecodeArgs &a, int b) {
+  if (!a.new_slots) return -1;
+  const long long s = __ldg(a.new_slots + b);
+  return s < 0 ? -1 : s;
+}
+
+// Row of KV head kvh of sequence b's new token in the k (or v) input.
+template <typename T>
+__device__ __forceinline__ const uint4 *append_src(const DecodeArgs &a, bool is_v, int b,
+                                                   int kvh) {
+  const T *base = reinterpret_cast<const T *>(is_v ? a.new_v : a.new_k);
+  const long long stride = is_v ? a.new_v_stride : a.new_k_stride;
+  return reinterpret_cast<const uint4 *>(base + (size_t)b * stride + (size_t)kvh * a.D);
+}
+
+// Checks of the cache half of the append (one thread of the writing CTA of
+// (sequence b, KV head kvh)): `slot` must be where the context's position
+// n-1 lives -- the physical block the table gives for it, row (n-1) % bs --
+// and inside the pool.  Flags are raised for KV head 0 only.  Returns
+// whether the row may be written.
+__device__ __forceinline__ bool append_check(const DecodeArgs &a, int b, int kvh, long long slot,
+                                             int n) {
+  bool match = false;
+  if (n > 0) {
+    const int lb = (n - 1) / a.bs;
+    const int phys = __ldg(a.tables + (size_t)b * a.max_blocks + lb);
+    match = (long long)phys * a.bs + (n - 1 - lb * a.bs) == slot;
+  }
+  if (!match && kvh == 0) raise_flag(a.err, PKV_FLAG_APPEND_MISMATCH);
+  const bool in_pool = slot < a.num_blocks * (long long)a.bs;
+  if (!in_pool && kvh == 0) raise_flag(a.err, PKV_FLAG_SLOT_OUT_OF_RANGE);
+  return in_pool;
+}
+
+// 16-byte vector j of the K and V rows of KV head kvh at cache row `slot`.
+template <typename T>
+__device__ __forceinline__ void append_store(const DecodeArgs &a, int kvh, long long slot, int j,
+                                             uint4 kv, uint4 vv) {
+  const size_t row = ((size_t)slot * a.KVH + kvh) * a.D;
+  T *kc = const_cast<T *>(reinterpret_cast<const T *>(a.k_cache)) + row;
+  T *vc = const_cast<T *>(reinterpret_cast<const T *>(a.v_cache)) + row;
+  reinterpret_cast<uint4 *>(kc)[j] = kv;
+  reinterpret_cast<uint4 *>(vc)[j] = vv;
+}
+
+// The cache half of the append by one warp: check, then copy the new
+// token's K and V rows of KV head kvh to cache row `slot`.
+template <typename T>
+__device__ void append_write_row(const DecodeArgs &a, int b, int kvh, long long slot, int n,
+                                 int lane) {
+  int ok = 0;
+  if (lane == 0) ok = append_check(a, b, kvh, slot, n);
+  if (!__shfl_sync(0xffffffffu, ok, 0)) return;
+  const int vecs = a.D * (int)sizeof(T) / 16;  // per row of one head
+  const uint4 *ks = append_src<T>(a, false, b, kvh), *vs = append_src<T>(a, true, b, kvh);
+  for (int j = lane; j < vecs; j += 32) append_store<T>(a, kvh, slot, j, __ldg(ks + j), __ldg(vs + j));
 }
 
 // Zero output rows for an empty context (partition 0 only).

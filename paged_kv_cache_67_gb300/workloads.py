@@ -154,7 +154,8 @@ def make_decode_inputs(cfg: DecodeConfig, seed: int, device="cpu",
     last block) with NaN, so that any read of them shows in the output."""
     g = torch.Generator().manual_seed(seed)
     lens = _lengths(cfg, g)
-    total_len = lens + (cfg.steps - 1)               # room to grow for per-step runs
+    # room to grow for per-step runs: step s appends the token at position n + s
+    total_len = lens + (cfg.steps if cfg.steps > 1 else 0)
     total_len[cfg.B - cfg.pad_seqs:] = 0
     need = [-(-int(x) // cfg.bs) for x in total_len]
     total_blocks = sum(need)

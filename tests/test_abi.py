@@ -20,7 +20,8 @@ def pkv():
 def test_every_declared_symbol_is_exported(pkv):
     names = pkv.exported_symbols()
     assert set(names) >= {"pkv_write", "pkv_decode_attention", "pkv_decode_workspace_size",
-                          "pkv_decode_plan", "pkv_status_string", "pkv_version"}
+                          "pkv_decode_plan", "pkv_status_string", "pkv_version",
+                          "pkv_write_decode_attention", "pkv_decode_attention_static"}
     lib = pkv.load_library()
     for n in names:
         assert hasattr(lib, n), n
@@ -132,3 +133,18 @@ def test_host_side_argument_errors(pkv):
     assert dec(D=1024) == 2              # head_dim above 512
     assert dec(B=0) == 0                 # empty batch: nothing to do
     assert dec() == 1                    # NULL pointers
+
+    # the fused step: the decode checks plus its new-token rows
+    fake = 1 << 20  # a 16-byte-aligned address that is never dereferenced
+    fz = lambda **kw: lib.pkv_write_decode_attention(
+        kw.get("out"), kw.get("q"), kw.get("k", fake), kw.get("v", fake), kw.get("ks", 128),
+        kw.get("vs", 128), kw.get("slots", fake), kw.get("kc"), kw.get("vc"), kw.get("t"),
+        kw.get("l"), kw.get("B", 2), 4, 2, 64, 16, 4, 8, ctypes.c_float(0.125), kw.get("dt", 1),
+        0, 0, None, 0, None, None)
+    assert fz(B=0) == 0                  # empty batch
+    assert fz() == 1                     # NULL q / out / caches
+    assert fz(slots=None) == 1
+    assert fz(k=fake + 8) == 1           # new-token row not 16-byte aligned
+    assert fz(ks=100) == 1               # stride shorter than a row
+    assert fz(ks=132) == 1               # stride not a multiple of 16 bytes
+    assert fz(dt=9) == 1
