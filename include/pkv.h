@@ -223,9 +223,10 @@ PKV_API pkv_status pkv_decode_attention_static(void *out, const void *q, const v
  * each sequence's new token followed by pkv_decode_attention over contexts
  * that already count it.
  * Definition: course page "P09 · Paged KV 写入 + decode attention（参考实现）",
- * section 题面速览 -- a decode step first writes the new token's K/V to
- * cache[slot // bs, slot % bs] and then reads the paged context; the result
- * is that of the two calls above made one after the other.
+ * section 在系统中的位置 -- each model-runner step first writes the new
+ * tokens' K/V into the cache by slot_mapping, then attention reads the
+ * history through block_tables; the result is that of the two calls above
+ * made one after the other.
  *
  *   k, v          [B, num_kv_heads, head_dim]: the new token of sequence b
  *                 starts at element b * k_token_stride (resp. v_token_stride)
