@@ -63,7 +63,8 @@ typedef enum pkv_status {
   PKV_ERR_INVALID_ARG = 1,   /* a size, pointer, alignment or count is not valid */
   PKV_ERR_UNSUPPORTED = 2,   /* valid, but a shape/dtype this build does not handle */
   PKV_ERR_CUDA = 3,          /* a CUDA runtime call or a kernel launch failed */
-  PKV_ERR_WORKSPACE = 4      /* the workspace is missing or smaller than needed */
+  PKV_ERR_WORKSPACE = 4,     /* the workspace is missing or smaller than needed */
+  PKV_ERR_OUT_OF_BLOCKS = 5  /* block manager (pkv_block_manager.h): not enough free blocks */
 } pkv_status;
 
 typedef enum pkv_dtype {

@@ -16,6 +16,8 @@ from ._binding import (  # noqa: F401
     FLAG_CONTEXT_TOO_LONG,
     FLAG_SLOT_OUT_OF_RANGE,
     FLAG_TIMEOUT,
+    PKV_ERR_OUT_OF_BLOCKS,
+    BlockManager,
     PkvError,
     DecodeWorkspace,
     exported_symbols,

@@ -18,7 +18,7 @@ import torch
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_PKG, "_build", "libpkv.so")
-_HEADER = os.path.join(os.path.dirname(_PKG), "include", "pkv.h")
+_INCLUDE = os.path.join(os.path.dirname(_PKG), "include")
 
 PKV_F32, PKV_BF16, PKV_F16 = 0, 1, 2
 _DT = {torch.float32: PKV_F32, torch.bfloat16: PKV_BF16, torch.float16: PKV_F16}
@@ -73,6 +73,25 @@ def load_library():
                                                    ctypes.c_float, c_int, c_int, c_int, vp, c_size,
                                                    vp, vp]
         lib.pkv_write_decode_attention.restype = c_int
+        P = ctypes.POINTER
+        lib.pkv_bm_create.argtypes = [i64, c_int, c_int, P(vp)]
+        lib.pkv_bm_create.restype = c_int
+        lib.pkv_bm_destroy.argtypes = [vp]
+        lib.pkv_bm_destroy.restype = None
+        lib.pkv_bm_add_sequence.argtypes = [vp, i64, vp, i64, vp, P(i64)]
+        lib.pkv_bm_add_sequence.restype = c_int
+        lib.pkv_bm_append_tokens.argtypes = [vp, vp, vp, c_int, vp]
+        lib.pkv_bm_append_tokens.restype = c_int
+        lib.pkv_bm_free_sequence.argtypes = [vp, i64]
+        lib.pkv_bm_free_sequence.restype = c_int
+        lib.pkv_bm_build_batch.argtypes = [vp, vp, c_int, c_int, ctypes.c_int32, vp, vp]
+        lib.pkv_bm_build_batch.restype = c_int
+        lib.pkv_bm_sequence_info.argtypes = [vp, i64, P(i64), P(c_int), vp, c_int]
+        lib.pkv_bm_sequence_info.restype = c_int
+        lib.pkv_bm_stats.argtypes = [vp, P(i64), P(i64), P(i64)]
+        lib.pkv_bm_stats.restype = None
+        lib.pkv_bm_block_refcount.argtypes = [vp, i64]
+        lib.pkv_bm_block_refcount.restype = c_int
         lib.pkv_status_string.argtypes = [c_int]
         lib.pkv_status_string.restype = ctypes.c_char_p
         lib.pkv_version.argtypes = []
@@ -82,10 +101,13 @@ def load_library():
 
 
 def exported_symbols() -> list[str]:
-    """Names of the entry points include/pkv.h declares (PKV_API)."""
-    with open(_HEADER) as f:
-        text = f.read()
-    return re.findall(r"PKV_API\s+[\w\s\*]+?\b(pkv_\w+)\s*\(", text)
+    """Names of the entry points the headers under include/ declare (PKV_API)."""
+    names = []
+    for h in sorted(os.listdir(_INCLUDE)):
+        if h.endswith(".h"):
+            with open(os.path.join(_INCLUDE, h)) as f:
+                names += re.findall(r"PKV_API\s+[\w\s\*]+?\b(pkv_\w+)\s*\(", f.read())
+    return names
 
 
 def pkv_status_string(status: int) -> str:
@@ -255,3 +277,89 @@ def pkv_decode_attention(out, q, k_cache, v_cache, block_tables, context_lens, s
                                     _ptr(err_flags), _stream_handle(stream, dev)),
            "pkv_decode_attention")
     return out
+
+
+PKV_ERR_OUT_OF_BLOCKS = 5
+
+
+class BlockManager:
+    """Host block manager of libpkv (include/pkv_block_manager.h): block pool,
+    per-sequence tables, slots for new tokens, prefix sharing of full blocks.
+    Arrays go in and out as CPU torch tensors (int64 token ids and slots,
+    int32 tables and lengths)."""
+
+    def __init__(self, num_blocks: int, block_size: int, prefix_caching: bool = True):
+        self._lib = load_library()
+        h = ctypes.c_void_p()
+        _check(self._lib.pkv_bm_create(int(num_blocks), int(block_size), int(bool(prefix_caching)),
+                                       ctypes.byref(h)), "pkv_bm_create")
+        self._h = h
+        self.num_blocks, self.block_size = int(num_blocks), int(block_size)
+
+    def close(self):
+        if getattr(self, "_h", None):
+            self._lib.pkv_bm_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        self.close()
+
+    @staticmethod
+    def _i64(x):
+        t = torch.as_tensor(x, dtype=torch.int64).contiguous()
+        _require(t.device.type == "cpu", "host arrays only")
+        return t
+
+    def add_sequence(self, seq_id: int, token_ids):
+        """Admit a sequence with its prompt; returns (slot_mapping [n] int64 with
+        -1 for cached tokens, number of cached leading tokens)."""
+        tok = self._i64(token_ids)
+        slots = torch.empty(tok.numel(), dtype=torch.int64)
+        cached = ctypes.c_int64()
+        _check(self._lib.pkv_bm_add_sequence(self._h, int(seq_id), tok.data_ptr(), tok.numel(),
+                                             slots.data_ptr(), ctypes.byref(cached)),
+               "pkv_bm_add_sequence")
+        return slots, cached.value
+
+    def append_tokens(self, seq_ids, token_ids):
+        """One decode step: append token_ids[i] to seq_ids[i] (negative id =
+        padding); returns the new tokens' slots (-1 for padding)."""
+        ids, tok = self._i64(seq_ids), self._i64(token_ids)
+        _require(ids.numel() == tok.numel(), "seq_ids and token_ids differ in length")
+        slots = torch.empty(ids.numel(), dtype=torch.int64)
+        _check(self._lib.pkv_bm_append_tokens(self._h, ids.data_ptr(), tok.data_ptr(), ids.numel(),
+                                              slots.data_ptr()), "pkv_bm_append_tokens")
+        return slots
+
+    def free_sequence(self, seq_id: int):
+        _check(self._lib.pkv_bm_free_sequence(self._h, int(seq_id)), "pkv_bm_free_sequence")
+
+    def build_batch(self, seq_ids, max_blocks: int, tail: int = 99999):
+        """(block_tables [B, max_blocks] int32, context_lens [B] int32) of a batch."""
+        ids = self._i64(seq_ids)
+        tables = torch.empty((ids.numel(), max_blocks), dtype=torch.int32)
+        lens = torch.empty(ids.numel(), dtype=torch.int32)
+        _check(self._lib.pkv_bm_build_batch(self._h, ids.data_ptr(), ids.numel(), int(max_blocks),
+                                            int(tail), tables.data_ptr(), lens.data_ptr()),
+               "pkv_bm_build_batch")
+        return tables, lens
+
+    def sequence_info(self, seq_id: int):
+        """(context_len, block table as a list)."""
+        n, nb = ctypes.c_int64(), ctypes.c_int()
+        _check(self._lib.pkv_bm_sequence_info(self._h, int(seq_id), ctypes.byref(n), ctypes.byref(nb),
+                                              None, 0), "pkv_bm_sequence_info")
+        table = torch.empty(nb.value, dtype=torch.int32)
+        _check(self._lib.pkv_bm_sequence_info(self._h, int(seq_id), ctypes.byref(n), ctypes.byref(nb),
+                                              table.data_ptr() if nb.value else None, nb.value),
+               "pkv_bm_sequence_info")
+        return n.value, table.tolist()
+
+    def stats(self):
+        """(free blocks, registered cached blocks, live sequences)."""
+        a, b, c = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int64()
+        self._lib.pkv_bm_stats(self._h, ctypes.byref(a), ctypes.byref(b), ctypes.byref(c))
+        return a.value, b.value, c.value
+
+    def refcount(self, block: int) -> int:
+        return self._lib.pkv_bm_block_refcount(self._h, int(block))

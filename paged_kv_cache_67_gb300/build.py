@@ -1,6 +1,6 @@
 """Build libpkv.so (the C ABI of include/pkv.h) in-tree with nvcc for sm_103a.
 
-Each .cu file under csrc/ is compiled in parallel, then linked into
+Each .cu / .cpp file under csrc/ is compiled in parallel, then linked into
 _build/libpkv.so with the CUDA runtime linked statically.  The build is
 skipped when the library is newer than every source and header.
 
@@ -36,7 +36,7 @@ def nvcc() -> str:
 
 
 def _sources():
-    return sorted(glob.glob(os.path.join(CSRC, "*.cu")))
+    return sorted(glob.glob(os.path.join(CSRC, "*.cu")) + glob.glob(os.path.join(CSRC, "*.cpp")))
 
 
 def _deps():
@@ -59,7 +59,7 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     objs = []
 
     def compile_one(src):
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(BUILD, os.path.splitext(os.path.basename(src))[0] + ".o")
         cmd = [cc, *NVCC_FLAGS, *extra_flags, "-c", src, "-o", obj]
         if verbose:
             print(" ".join(cmd), flush=True)

@@ -321,6 +321,7 @@ PKV_API const char *pkv_status_string(pkv_status status) {
     case PKV_ERR_UNSUPPORTED: return "unsupported shape or dtype";
     case PKV_ERR_CUDA: return "CUDA error";
     case PKV_ERR_WORKSPACE: return "workspace missing or too small";
+    case PKV_ERR_OUT_OF_BLOCKS: return "not enough free cache blocks";
   }
   return "unknown status";
 }
