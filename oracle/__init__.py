@@ -1,5 +1,5 @@
-"""The oracle: plain fp64 CPU restatement of the paged KV-cache write and of
-paged decode attention.
+"""The oracle: plain fp64 CPU restatement of the paged KV-cache write, of
+paged decode attention and of paged causal prefill attention.
 
 TEST INFRASTRUCTURE ONLY.  The tests, ``__graft_entry__.smoke()`` and the
 CPU-baseline leg of ``bench.py`` may use it; the library (the package
@@ -72,6 +72,9 @@ def _declare(lib):
     lib.pkv_oracle_decode.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i64,
                                       i64, ctypes.c_double, c_int, i64, i64, i64, i64]
     lib.pkv_oracle_decode.restype = c_int
+    lib.pkv_oracle_prefill.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i64,
+                                       i64, ctypes.c_double, c_int, i64, i64]
+    lib.pkv_oracle_prefill.restype = c_int
     lib.pkv_oracle_round.argtypes = [vp, vp, i64, c_int]
     lib.pkv_oracle_round.restype = c_int
     lib.pkv_oracle_widen.argtypes = [vp, vp, i64, c_int]
@@ -140,6 +143,34 @@ def decode(q, k_cache, v_cache, block_tables, context_lens, scale: float,
                                  _ptr(block_tables), _ptr(context_lens), B, H, kvh, D, bs,
                                  max_blocks, nblk, float(scale), _DTYPE_CODE[q.dtype], b0, b1,
                                  h0, h1))
+    return out
+
+
+def prefill(q, k_cache, v_cache, block_tables, cu_seqlens_q, context_lens, scale: float,
+            seqs: tuple[int, int] | None = None, out=None, lib=None):
+    """Paged causal prefill attention; returns out [total_q, H, D] in q.dtype.
+
+    Sequence b's qlen = cu_seqlens_q[b+1] - cu_seqlens_q[b] queries are the
+    last qlen of its context_lens[b] tokens; query i (row cu_seqlens_q[b] + i)
+    attends to positions 0 .. context_lens[b] - qlen + i.  ``seqs=(b0, b1)``
+    restricts the work to those sequences (other rows of ``out`` unchanged)."""
+    lib = lib or load()
+    total_q, H, D = q.shape
+    nblk, bs, kvh, d2 = k_cache.shape
+    assert d2 == D and v_cache.shape == k_cache.shape
+    assert q.dtype == k_cache.dtype == v_cache.dtype
+    assert block_tables.dtype == torch.int32 and context_lens.dtype == torch.int32
+    assert cu_seqlens_q.dtype == torch.int32
+    B = context_lens.shape[0]
+    assert block_tables.shape[0] == B and cu_seqlens_q.shape == (B + 1,)
+    assert int(cu_seqlens_q[-1]) == total_q
+    if out is None:
+        out = torch.zeros_like(q)
+    b0, b1 = seqs if seqs is not None else (0, B)
+    _check(lib.pkv_oracle_prefill(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+                                  _ptr(block_tables), _ptr(cu_seqlens_q), _ptr(context_lens), B, H,
+                                  kvh, D, bs, block_tables.shape[1], nblk, float(scale),
+                                  _DTYPE_CODE[q.dtype], b0, b1))
     return out
 
 

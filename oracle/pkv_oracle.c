@@ -268,3 +268,78 @@ int pkv_oracle_decode(void *out, const void *q, const void *k_cache, const void 
   }
   return rc;
 }
+
+/*
+ * paged prefill attention (several new query tokens per sequence, causal)
+ * for the sequences b in [b_begin, b_end).  The pages only ask how the
+ * varlen prefill version would be written (course page "P09 · Paged KV 写入
+ * + decode attention（参考实现）", section 面试官追问); the reading taken
+ * here is the one decode is the one-query case of (same page, section 细节:
+ * the decode query is the newest token, already written, and sees the
+ * whole context including itself):
+ *   qlen = cu_seqlens_q[b+1] - cu_seqlens_q[b] new tokens, the LAST qlen
+ *   tokens of a context of n = context_lens[b] tokens (qlen <= n, all
+ *   already written to the cache);
+ *   query i (row cu_seqlens_q[b] + i of q / out) sits at logical position
+ *   p = n - qlen + i and attends to the tokens 0 .. p (causal);
+ *   kvh = h / (H / KVH); scores scaled before an exact softmax; rounded once.
+ * q and out are [total_q, H, D] with total_q = cu_seqlens_q[B].
+ */
+int pkv_oracle_prefill(void *out, const void *q, const void *k_cache, const void *v_cache,
+                       const int32_t *block_tables, const int32_t *cu_seqlens_q,
+                       const int32_t *context_lens, int64_t B, int64_t H, int64_t num_kv_heads,
+                       int64_t head_dim, int64_t block_size, int64_t max_blocks,
+                       int64_t num_blocks, double scale, int dtype, int64_t b_begin,
+                       int64_t b_end) {
+  if (B < 0 || H <= 0 || num_kv_heads <= 0 || H % num_kv_heads != 0 || head_dim <= 0 ||
+      block_size <= 0 || max_blocks < 0 || num_blocks < 0 || dtype < ORC_F32 ||
+      dtype > ORC_F16 || b_begin < 0 || b_end > B || b_begin > b_end || cu_seqlens_q[0] != 0)
+    return ORC_ERR_ARG;
+  const int64_t KVH = num_kv_heads, D = head_dim, bs = block_size;
+  const int64_t heads_per_kv = H / KVH;
+  int status = ORC_OK;
+
+  for (int64_t b = b_begin; b < b_end && status == ORC_OK; ++b) {
+    const int64_t qlen = (int64_t)cu_seqlens_q[b + 1] - cu_seqlens_q[b];
+    const int64_t n = context_lens[b];
+    if (qlen < 0 || n < qlen) { status = ORC_ERR_CONTEXT; break; }
+    const int64_t nb = (n + bs - 1) / bs;
+    if (nb > max_blocks) { status = ORC_ERR_CONTEXT; break; }
+    const int32_t *table = block_tables + b * max_blocks;
+    for (int64_t j = 0; j < nb; ++j)
+      if (table[j] < 0 || table[j] >= num_blocks) { status = ORC_ERR_BLOCK_RANGE; break; }
+    if (status != ORC_OK) break;
+
+    double *w = (double *)calloc((size_t)(n > 0 ? n : 1), sizeof(double));
+    if (!w) { status = ORC_ERR_NOMEM; break; }
+
+    for (int64_t i = 0; i < qlen; ++i) {
+      const int64_t p = n - qlen + i;           /* logical position of query i */
+      const int64_t lim = p + 1;                /* causal: tokens 0 .. p, p included */
+      const int64_t q_row = cu_seqlens_q[b] + i;
+      for (int64_t h = 0; h < H; ++h) {
+        const int64_t g = h / heads_per_kv;     /* GQA: repeat_interleave order */
+        const int64_t qbase = (q_row * H + h) * D;
+        double mx = -INFINITY;
+        for (int64_t t = 0; t < lim; ++t) {
+          const int64_t krow = ((table[t / bs] * bs + t % bs) * KVH + g) * D;
+          double qk = 0.0;
+          for (int64_t d = 0; d < D; ++d)
+            qk += load_elem(q, qbase + d, dtype) * load_elem(k_cache, krow + d, dtype);
+          w[t] = qk * scale;                    /* scaled before the softmax */
+          mx = w[t] > mx ? w[t] : mx;
+        }
+        double total = 0.0;
+        for (int64_t t = 0; t < lim; ++t) total += (w[t] = exp(w[t] - mx));
+        for (int64_t d = 0; d < D; ++d) {
+          double o = 0.0;
+          for (int64_t t = 0; t < lim; ++t)
+            o += w[t] * load_elem(v_cache, ((table[t / bs] * bs + t % bs) * KVH + g) * D + d, dtype);
+          store_elem(out, qbase + d, dtype, o / total);
+        }
+      }
+    }
+    free(w);
+  }
+  return status;
+}

@@ -419,9 +419,118 @@ def pin_widen(lib):
         assert same.all(), dt
 
 
+# ------------------------------------------------------------------ prefill
+
+def _prefill_case(seed, lens, qlens, H, KVH, D, bs, dtype):
+    """A paged case plus varlen queries: sequence b's queries are its last
+    qlens[b] positions."""
+    case = random_paged_case(seed, lens, H=H, KVH=KVH, D=D, bs=bs, dtype=dtype)
+    g = torch.Generator().manual_seed(seed + 1)
+    cu = [0]
+    for ql in qlens:
+        cu.append(cu[-1] + ql)
+    q = torch.randn((cu[-1], H, D), generator=g, dtype=torch.float64).to(dtype)
+    return case, q, torch.tensor(cu, dtype=torch.int32)
+
+
+def dense_causal(q, k, v, scale, n, is_causal=False):
+    """q [qlen, H, D] at positions n-qlen .. n-1; k/v [n, KVH, D]; SDPA in fp64
+    with an explicit mask (query at p sees keys 0..p), or SDPA's own causal
+    flag when the queries cover the whole context."""
+    qlen, H = q.shape[0], q.shape[1]
+    q64 = q.double().permute(1, 0, 2).unsqueeze(0)
+    k64 = k.double().permute(1, 0, 2).unsqueeze(0)
+    v64 = v.double().permute(1, 0, 2).unsqueeze(0)
+    gqa = k64.shape[1] != H
+    if is_causal:
+        assert qlen == n
+        o = F.scaled_dot_product_attention(q64, k64, v64, scale=scale, is_causal=True, enable_gqa=gqa)
+    else:
+        pos = torch.arange(n - qlen, n).unsqueeze(1)
+        mask = torch.arange(n).unsqueeze(0) <= pos          # [qlen, n]
+        o = F.scaled_dot_product_attention(q64, k64, v64, attn_mask=mask, scale=scale, enable_gqa=gqa)
+    return o.squeeze(0).permute(1, 0, 2)                     # [qlen, H, D]
+
+
+def pin_prefill_dense_causal(lib):
+    """Varlen causal prefill over shuffled paged blocks (NaN in unused rows,
+    garbage tails) equals masked dense SDPA on the contiguous rows; query
+    counts from 1 (decode) to the whole context, lengths on and off block
+    edges."""
+    lens = [1, 4, 9, 16, 13, 30]
+    qlens = [1, 4, 3, 16, 1, 11]
+    for dtype in (torch.float32, torch.bfloat16):
+        for H, KVH in ((4, 4), (4, 2), (6, 1)):
+            case, q, cu = _prefill_case(200 + H + KVH, lens, qlens, H, KVH, 16, 4, dtype)
+            out = oracle.prefill(q, case["k_cache"], case["v_cache"], case["block_tables"], cu,
+                                 case["context_lens"], 0.3, lib=lib)
+            for b, (n, ql) in enumerate(zip(lens, qlens)):
+                want = dense_causal(q[cu[b]:cu[b + 1]], *case["dense"][b], 0.3, n)
+                got = out[cu[b]:cu[b + 1]]
+                if dtype == torch.float32:
+                    _assert_close(got, want, 2e-6, 2e-6, f"prefill b={b}")
+                else:
+                    _assert_close(got, want, 1e-30, torch.finfo(dtype).eps, f"prefill {dtype} b={b}")
+
+
+def pin_prefill_full_is_causal(lib):
+    """Queries covering the whole context: SDPA's own causal flag."""
+    lens = [7, 12, 5]
+    case, q, cu = _prefill_case(301, lens, lens, 4, 2, 8, 4, torch.float32)
+    out = oracle.prefill(q, case["k_cache"], case["v_cache"], case["block_tables"], cu,
+                         case["context_lens"], 0.5, lib=lib)
+    for b, n in enumerate(lens):
+        want = dense_causal(q[cu[b]:cu[b + 1]], *case["dense"][b], 0.5, n, is_causal=True)
+        _assert_close(out[cu[b]:cu[b + 1]], want, 2e-6, 2e-6, f"full prefill b={b}")
+
+
+def pin_prefill_closed_forms(lib):
+    """Whole-context prefill: the first query sees only token 0 (its V row
+    exactly); with zero scale query i gets the mean of V rows 0..i; one
+    query per sequence is decode (the decode pins' function)."""
+    lens = [6, 11]
+    H, KVH = 4, 2
+    case, q, cu = _prefill_case(302, lens, lens, H, KVH, 8, 4, torch.bfloat16)
+    args = (case["k_cache"], case["v_cache"], case["block_tables"], cu, case["context_lens"])
+    out = oracle.prefill(q, *args, 2.3, lib=lib)
+    for b in range(2):
+        v0 = case["dense"][b][1][0]
+        for h in range(H):
+            assert torch.equal(out[cu[b], h], v0[h // (H // KVH)]), (b, h)
+    out = oracle.prefill(q, *args, 0.0, lib=lib)
+    for b, n in enumerate(lens):
+        dv = case["dense"][b][1].double()
+        for i in range(n):
+            mean = dv[:i + 1].mean(dim=0)
+            for h in range(H):
+                want = oracle.round_to(mean[h // (H // KVH)], torch.bfloat16, lib=lib)
+                assert torch.equal(out[cu[b] + i, h], want), (b, i, h)
+    # one query per sequence == decode
+    case1, q1, cu1 = _prefill_case(303, [5, 9, 1], [1, 1, 1], H, KVH, 8, 4, torch.float32)
+    got = oracle.prefill(q1, case1["k_cache"], case1["v_cache"], case1["block_tables"], cu1,
+                         case1["context_lens"], 0.4, lib=lib)
+    want = oracle.decode(q1, case1["k_cache"], case1["v_cache"], case1["block_tables"],
+                         case1["context_lens"], 0.4, lib=lib)
+    assert torch.equal(got, want)
+
+
+def pin_prefill_errors(lib):
+    case, q, cu = _prefill_case(304, [3, 4], [2, 2], 2, 1, 4, 2, torch.float32)
+    args = (case["k_cache"], case["v_cache"], case["block_tables"])
+    bad_lens = torch.tensor([1, 4], dtype=torch.int32)        # more queries than context
+    for cu_, lens_ in ((cu, bad_lens), (torch.tensor([1, 3, 4], dtype=torch.int32), case["context_lens"])):
+        try:
+            oracle.prefill(q if int(cu_[-1]) == q.shape[0] else q[:int(cu_[-1])], *args, cu_, lens_,
+                           1.0, lib=lib)
+        except oracle.OracleError:
+            continue
+        raise AssertionError("accepted an invalid prefill batch")
+
+
 ALL_PINS = [
     pin_example1_write, pin_key_answer_slot7, pin_I1_sentinel, pin_example2_decode,
     pin_example2_softmax, pin_key_answer_n5_truncation, pin_gqa_mapping,
     pin_I2_tail_never_read, pin_I4_dense_equality, pin_shared_prefix, pin_closed_forms,
-    pin_empty_context, pin_error_codes, pin_rounding, pin_widen,
+    pin_empty_context, pin_error_codes, pin_rounding, pin_widen, pin_prefill_dense_causal,
+    pin_prefill_full_is_causal, pin_prefill_closed_forms, pin_prefill_errors,
 ]

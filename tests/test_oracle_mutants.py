@@ -42,6 +42,13 @@ MUTANTS = {
                         "store_elem(out, qoff + d, dtype, acc / (double)n);")],
     "round_by_truncation": [("double r = nearbyint(ldexp(x, -q));", "double r = trunc(ldexp(x, -q));")],
     "subnormals_not_fixed_quantum": [("if (q < emin - p + 1) q = emin - p + 1;", "")],
+    "prefill_top_left_causal": [("const int64_t p = n - qlen + i;", "const int64_t p = i;")],
+    "prefill_excludes_self": [("const int64_t lim = p + 1;", "const int64_t lim = p > 0 ? p : 1;")],
+    "prefill_no_causal_mask": [("const int64_t lim = p + 1;", "const int64_t lim = n;")],
+    "prefill_ignores_row_offsets": [("const int64_t q_row = cu_seqlens_q[b] + i;",
+                                     "const int64_t q_row = i;")],
+    "prefill_gqa_repeat": [("const int64_t g = h / heads_per_kv;", "const int64_t g = h % KVH;")],
+    "prefill_scale_dropped": [("w[t] = qk * scale;", "w[t] = qk;")],
     "empty_context_not_zero": [("for (int64_t d = 0; d < D; ++d) store_elem(out, qoff + d, dtype, 0.0);",
                                 "for (int64_t d = 0; d < D; ++d) store_elem(out, qoff + d, dtype, 1.0);")],
 }
