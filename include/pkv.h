@@ -86,6 +86,11 @@ typedef enum pkv_dtype {
                                             sequence unspecified */
 #define PKV_FLAG_TIMEOUT 0x20            /* a bounded wait for an asynchronous copy ran out
                                             (should never happen); outputs unspecified */
+#define PKV_FLAG_QUERY_LEN 0x80          /* prefill: a sequence with qlen < 0, qlen > context_lens[b]
+                                            or a context longer than the table; skipped, its
+                                            output rows unspecified */
+#define PKV_FLAG_QUERY_OVER_HINT 0x100   /* prefill: a sequence has more queries than max_q_len;
+                                            rows past max_q_len are not computed */
 #define PKV_FLAG_APPEND_MISMATCH 0x40    /* pkv_write_decode_attention: a kept slot is not the
                                             slot of position context_lens[b] - 1 through
                                             block_tables (or context_lens[b] == 0); the token
@@ -258,6 +263,42 @@ PKV_API pkv_status pkv_write_decode_attention(
     int head_dim, int block_size, int max_blocks, int64_t num_blocks, float scale, pkv_dtype dt,
     int max_context_len, int partition_size, void *workspace, size_t workspace_bytes,
     int *err_flags, pkv_stream_t stream);
+
+/*
+ * pkv_prefill_attention -- paged causal prefill attention: several new query
+ * tokens per sequence (varlen), each attending to the context up to itself.
+ * Definition: the course page "P09 · Paged KV 写入 + decode attention（参考
+ * 实现）" asks how the varlen prefill version is written (section 面试官追问)
+ * without giving it; this library's reading is the multi-query form of its
+ * decode (section 细节: the decode query is the newest token, already
+ * written, and sees the whole context including itself):
+ *   qlen = cu_seqlens_q[b+1] - cu_seqlens_q[b] queries of sequence b are the
+ *   LAST qlen of its n = context_lens[b] tokens, all already written to the
+ *   cache (pkv_write); query i (row cu_seqlens_q[b] + i) sits at position
+ *   p = n - qlen + i and attends to tokens 0 .. p; head h uses KV head
+ *   h // (H / KVH); fp32 scores times scale, fp32 softmax, output in q's
+ *   dtype.  With qlen = 1 it is pkv_decode_attention.
+ *
+ *   out, q        [total_q, H, head_dim], total_q = cu_seqlens_q[B]
+ *   cu_seqlens_q  [B + 1] int32, cu_seqlens_q[0] = 0, non-decreasing
+ *   k_cache, v_cache, block_tables, context_lens: as in pkv_decode_attention
+ *   max_q_len     host-side upper bound on qlen (sizes the grid; 0 = total_q);
+ *                 a longer sequence raises PKV_FLAG_QUERY_OVER_HINT
+ *   err_flags     device int or NULL (PKV_FLAG_QUERY_LEN,
+ *                 PKV_FLAG_QUERY_OVER_HINT, PKV_FLAG_BLOCK_OUT_OF_RANGE,
+ *                 PKV_FLAG_TIMEOUT)
+ * Supported: bf16 / fp16, head_dim 64 or 128, block_size a multiple of 16,
+ * q, out, caches 16-byte aligned (tensor-core kernel, tcgen05).  No
+ * workspace.  Errors: PKV_ERR_INVALID_ARG, PKV_ERR_UNSUPPORTED, PKV_ERR_CUDA.
+ * B == 0 or total_q == 0 enqueues nothing.
+ */
+PKV_API pkv_status pkv_prefill_attention(void *out, const void *q, const void *k_cache,
+                                         const void *v_cache, const int32_t *block_tables,
+                                         const int32_t *cu_seqlens_q, const int32_t *context_lens,
+                                         int B, int64_t total_q, int H, int num_kv_heads,
+                                         int head_dim, int block_size, int max_blocks,
+                                         int64_t num_blocks, float scale, pkv_dtype dt,
+                                         int max_q_len, int *err_flags, pkv_stream_t stream);
 
 /*
  * pkv_decode_plan -- the partition size and the partitions per sequence that

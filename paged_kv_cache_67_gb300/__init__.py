@@ -14,6 +14,8 @@ from ._binding import (  # noqa: F401
     FLAG_CONTEXT_NEGATIVE,
     FLAG_CONTEXT_OVER_HINT,
     FLAG_CONTEXT_TOO_LONG,
+    FLAG_QUERY_LEN,
+    FLAG_QUERY_OVER_HINT,
     FLAG_SLOT_OUT_OF_RANGE,
     FLAG_TIMEOUT,
     PKV_ERR_OUT_OF_BLOCKS,
@@ -26,6 +28,7 @@ from ._binding import (  # noqa: F401
     pkv_decode_attention,
     pkv_decode_plan,
     pkv_decode_workspace_size,
+    pkv_prefill_attention,
     pkv_status_string,
     pkv_version,
     pkv_write,

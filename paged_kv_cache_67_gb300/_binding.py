@@ -30,6 +30,8 @@ FLAG_CONTEXT_NEGATIVE = 0x8
 FLAG_CONTEXT_OVER_HINT = 0x10
 FLAG_TIMEOUT = 0x20
 FLAG_APPEND_MISMATCH = 0x40
+FLAG_QUERY_LEN = 0x80
+FLAG_QUERY_OVER_HINT = 0x100
 
 _lock = threading.Lock()
 _lib = None
@@ -73,6 +75,10 @@ def load_library():
                                                    ctypes.c_float, c_int, c_int, c_int, vp, c_size,
                                                    vp, vp]
         lib.pkv_write_decode_attention.restype = c_int
+        lib.pkv_prefill_attention.argtypes = [vp, vp, vp, vp, vp, vp, vp, c_int, i64, c_int, c_int,
+                                              c_int, c_int, c_int, i64, ctypes.c_float, c_int, c_int,
+                                              vp, vp]
+        lib.pkv_prefill_attention.restype = c_int
         P = ctypes.POINTER
         lib.pkv_bm_create.argtypes = [i64, c_int, c_int, P(vp)]
         lib.pkv_bm_create.restype = c_int
@@ -243,6 +249,38 @@ def pkv_write_decode_attention(out, q, k, v, slot_mapping, k_cache, v_cache, blo
         _ptr(block_tables), _ptr(context_lens), B, H, kvh, D, bs, block_tables.shape[1], nb,
         float(scale), _DT[q.dtype], int(max_context_len), int(partition_size), ws_ptr, ws_bytes,
         _ptr(err_flags), _stream_handle(stream, dev)), "pkv_write_decode_attention")
+    return out
+
+
+def pkv_prefill_attention(out, q, k_cache, v_cache, block_tables, cu_seqlens_q, context_lens,
+                          scale: float, max_q_len: int = 0, err_flags=None, stream=None):
+    """Paged causal prefill attention into ``out`` [total_q, H, D] (returned):
+    sequence b's queries are rows cu_seqlens_q[b] .. cu_seqlens_q[b+1]-1 of
+    ``q``, the last tokens of its context_lens[b] (already written)."""
+    lib = load_library()
+    _require(q.dim() == 3 and out.shape == q.shape, "q and out must be [total_q, H, D]")
+    total_q, H, D = q.shape
+    _require(k_cache.dim() == 4 and v_cache.shape == k_cache.shape and k_cache.shape[3] == D,
+             "caches must be [nb, bs, KVH, D]")
+    nb, bs, kvh, _ = k_cache.shape
+    for t in (out, q, k_cache, v_cache, block_tables, cu_seqlens_q, context_lens):
+        _require(t.is_contiguous(), "tensors must be contiguous")
+    _require(q.dtype == out.dtype == k_cache.dtype == v_cache.dtype and q.dtype in _DT, "dtype mismatch")
+    B = context_lens.shape[0]
+    _require(block_tables.dtype == torch.int32 and block_tables.dim() == 2 and block_tables.shape[0] == B,
+             "block_tables must be int32 [B, max_blocks]")
+    _require(context_lens.dtype == torch.int32 and context_lens.dim() == 1, "context_lens must be int32 [B]")
+    _require(cu_seqlens_q.dtype == torch.int32 and cu_seqlens_q.shape == (B + 1,),
+             "cu_seqlens_q must be int32 [B + 1]")
+    dev = q.device
+    _require(dev.type == "cuda" and all(t.device == dev for t in (out, k_cache, v_cache, block_tables,
+                                                                   cu_seqlens_q, context_lens)),
+             "all tensors must be on the same CUDA device")
+    _check(lib.pkv_prefill_attention(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+                                     _ptr(block_tables), _ptr(cu_seqlens_q), _ptr(context_lens), B,
+                                     total_q, H, kvh, D, bs, block_tables.shape[1], nb, float(scale),
+                                     _DT[q.dtype], int(max_q_len), _ptr(err_flags),
+                                     _stream_handle(stream, dev)), "pkv_prefill_attention")
     return out
 
 

@@ -314,6 +314,37 @@ PKV_API pkv_status pkv_write_decode_attention(
                       partition_size, workspace, workspace_bytes, err_flags, stream, &app);
 }
 
+PKV_API pkv_status pkv_prefill_attention(void *out, const void *q, const void *k_cache,
+                                         const void *v_cache, const int32_t *block_tables,
+                                         const int32_t *cu_seqlens_q, const int32_t *context_lens,
+                                         int B, int64_t total_q, int H, int num_kv_heads,
+                                         int head_dim, int block_size, int max_blocks,
+                                         int64_t num_blocks, float scale, pkv_dtype dt,
+                                         int max_q_len, int *err_flags, pkv_stream_t stream) {
+  if (B < 0 || B > 65535 || total_q < 0 || total_q > 0x7fffffffLL || H <= 0 || H > 65535 ||
+      num_kv_heads <= 0 || H % num_kv_heads != 0 || head_dim <= 0 || block_size <= 0 ||
+      max_blocks < 0 || num_blocks < 0 || num_blocks > 0x7fffffffLL || max_q_len < 0)
+    return PKV_ERR_INVALID_ARG;
+  if (dt != PKV_F32 && dt != PKV_BF16 && dt != PKV_F16) return PKV_ERR_INVALID_ARG;
+  if (dt == PKV_F32 || (head_dim != 64 && head_dim != 128) || block_size % 16 != 0)
+    return PKV_ERR_UNSUPPORTED;
+  if (B == 0 || total_q == 0) return PKV_OK;
+  if (!out || !q || !k_cache || !v_cache || !block_tables || !cu_seqlens_q || !context_lens)
+    return PKV_ERR_INVALID_ARG;
+  const void *ptrs[4] = {out, q, k_cache, v_cache};
+  for (const void *p : ptrs)
+    if (reinterpret_cast<uintptr_t>(p) % 16) return PKV_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(block_tables) % 4 || reinterpret_cast<uintptr_t>(cu_seqlens_q) % 4 ||
+      reinterpret_cast<uintptr_t>(context_lens) % 4)
+    return PKV_ERR_INVALID_ARG;
+  const long long mq = max_q_len > 0 ? max_q_len : total_q;
+  const long long q_tiles = (mq + 127) / 128;
+  if (q_tiles > 65535) return PKV_ERR_UNSUPPORTED;
+  return launch_prefill_tc(out, q, k_cache, v_cache, block_tables, cu_seqlens_q, context_lens, B,
+                           H, num_kv_heads, head_dim, block_size, max_blocks, num_blocks, scale, dt,
+                           (int)q_tiles, err_flags, reinterpret_cast<cudaStream_t>(stream));
+}
+
 PKV_API const char *pkv_status_string(pkv_status status) {
   switch (status) {
     case PKV_OK: return "ok";

@@ -461,7 +461,7 @@ static CUtensorMapDataType map_type(pkv_dtype dt) {
 
 // Tensor map of a [num_blocks, bs, KVH, D] cache: dims innermost first, box of
 // 64 elements x 1 head x 16 rows x 1 block, 128-byte swizzle.
-static bool encode_cache_map(CUtensorMap *map, const void *cache, pkv_dtype dt, long long num_blocks,
+bool encode_cache_map(CUtensorMap *map, const void *cache, pkv_dtype dt, long long num_blocks,
                              int bs, int KVH, int D) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
@@ -473,19 +473,6 @@ static bool encode_cache_map(CUtensorMap *map, const void *cache, pkv_dtype dt, 
   return fn(map, map_type(dt), 4, const_cast<void *>(cache), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-// One-time opt-in to the kernel's dynamic shared memory, per device.
-template <typename K>
-static bool allow_smem(K kern, size_t bytes, int *configured) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return false;
-  if (dev < 64 && configured[dev] >= (int)bytes) return true;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) !=
-      cudaSuccess)
-    return false;
-  if (dev < 64) configured[dev] = (int)bytes;
-  return true;
 }
 
 template <int D, typename T, bool kAppend>

@@ -2,6 +2,7 @@
 // libpkv (not part of the public C ABI).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -44,6 +45,31 @@ pkv_status launch_write(void *k_cache, void *v_cache, const void *k, const void 
                         const int64_t *slot_mapping, int64_t T, int64_t k_stride, int64_t v_stride,
                         int64_t num_blocks, int bs, int KVH, int D, int elem, int *err,
                         cudaStream_t stream);
+
+// Tensor map of a [num_blocks, bs, KVH, D] 16-bit cache: box of 64 elements
+// x 1 head x 16 rows x 1 block, 128-byte swizzle (false if unavailable).
+bool encode_cache_map(CUtensorMap *map, const void *cache, pkv_dtype dt, long long num_blocks,
+                      int bs, int KVH, int D);
+
+// One-time opt-in to a kernel's dynamic shared memory, per device
+// (`configured` is the kernel's own per-device record).
+template <typename K>
+inline bool allow_smem(K kern, size_t bytes, int *configured) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  if (dev < 64 && configured[dev] >= (int)bytes) return true;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) !=
+      cudaSuccess)
+    return false;
+  if (dev < 64) configured[dev] = (int)bytes;
+  return true;
+}
+
+pkv_status launch_prefill_tc(void *out, const void *q, const void *k_cache, const void *v_cache,
+                             const int32_t *tables, const int32_t *cu_q, const int32_t *lens,
+                             int B, int H, int KVH, int D, int bs, int max_blocks,
+                             long long num_blocks, float scale, pkv_dtype dt, int q_tiles,
+                             int *err, cudaStream_t stream);
 
 struct DecodeArgs;
 pkv_status launch_decode_simt(const DecodeArgs &a, const DecodePlan &plan, pkv_dtype dt,

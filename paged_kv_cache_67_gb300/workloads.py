@@ -302,3 +302,95 @@ def write_bytes(slot_mapping, KVH: int, D: int, elem: int) -> int:
     s = torch.as_tensor(slot_mapping).cpu()
     kept = int((s >= 0).sum())
     return kept * 4 * KVH * D * elem + 8 * s.numel()
+
+
+# ------------------------------------------------------------------ prefill
+
+@dataclass(frozen=True)
+class PrefillConfig:
+    name: str
+    B: int                      # sequences
+    H: int
+    KVH: int
+    D: int
+    bs: int
+    dtype: torch.dtype
+    len_lo: int                 # context lengths uniform in [len_lo, len_hi]
+    len_hi: int
+    chunk_lo: int               # sequences 1, 3, 5, ...: a chunk of this many new
+    chunk_hi: int               # queries on top of a cached prefix; the others whole
+    pool_factor: float = 1.25
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.D)
+
+    @property
+    def table_width(self) -> int:
+        return -(-self.len_hi // self.bs)
+
+
+# A Llama-3-8B-shaped varlen prefill batch: half the sequences prefill their
+# whole prompt, half prefill a chunk on top of a cached prefix.
+PREFILL_CONFIGS = {
+    "prefill_bf16": PrefillConfig("prefill_bf16", B=16, H=32, KVH=8, D=128, bs=16,
+                                  dtype=torch.bfloat16, len_lo=512, len_hi=4096, chunk_lo=128,
+                                  chunk_hi=512),
+}
+
+
+@dataclass
+class PrefillInputs:
+    cfg: PrefillConfig
+    q: torch.Tensor             # [total_q, H, D]
+    k_cache: torch.Tensor       # [num_blocks, bs, KVH, D], every context token written
+    v_cache: torch.Tensor
+    block_tables: torch.Tensor  # [B, max_blocks] int32, garbage past ceil(n/bs)
+    context_lens: torch.Tensor  # [B] int32
+    cu_seqlens_q: torch.Tensor  # [B + 1] int32
+    scale: float
+    max_q_len: int
+    num_blocks: int
+
+
+def make_prefill_inputs(cfg: PrefillConfig, seed: int, device="cpu") -> PrefillInputs:
+    """Lengths, shuffled block assignment and tables on the CPU from ``seed``;
+    pool and queries with a generator on ``device`` (compare the CUDA path
+    and the oracle on the SAME tensors, copied)."""
+    g = torch.Generator().manual_seed(seed)
+    lens = torch.randint(cfg.len_lo, cfg.len_hi + 1, (cfg.B,), generator=g, dtype=torch.int64)
+    qlens = lens.clone()
+    chunk = torch.randint(cfg.chunk_lo, cfg.chunk_hi + 1, (cfg.B,), generator=g, dtype=torch.int64)
+    qlens[1::2] = torch.minimum(chunk[1::2], lens[1::2])
+    need = [-(-int(n) // cfg.bs) for n in lens]
+    num_blocks = max(1, math.ceil(cfg.pool_factor * sum(need)))
+    perm = torch.randperm(num_blocks, generator=g)
+    shim = DecodeConfig(cfg.name, cfg.B, cfg.H, cfg.KVH, cfg.D, cfg.bs, cfg.dtype, "uniform",
+                        cfg.len_lo, cfg.len_hi)
+    tables = _garbage_tail(shim, (cfg.B, cfg.table_width), num_blocks, g)
+    cursor = 0
+    for b, nb in enumerate(need):
+        tables[b, :nb] = perm[cursor:cursor + nb].to(torch.int32)
+        cursor += nb
+    cu = torch.zeros(cfg.B + 1, dtype=torch.int32)
+    cu[1:] = torch.cumsum(qlens, 0).to(torch.int32)
+    dg = torch.Generator(device=device).manual_seed(seed + 7919)
+    shape = (num_blocks, cfg.bs, cfg.KVH, cfg.D)
+    k_cache = _randn(shape, cfg.dtype, dg, device)
+    v_cache = _randn(shape, cfg.dtype, dg, device)
+    q = _randn((int(cu[-1]), cfg.H, cfg.D), cfg.dtype, dg, device)
+    return PrefillInputs(cfg, q, k_cache, v_cache, tables, lens.to(torch.int32), cu, cfg.scale,
+                         int(qlens.max()), num_blocks)
+
+
+def prefill_flops(context_lens, cu_seqlens_q, H: int, D: int) -> int:
+    """Multiply-add flops of one causal prefill call: query i of a sequence
+    with n tokens and qlen queries sees n - qlen + i + 1 keys; each key costs
+    2 * D flops for q.k and 2 * D for p.v, per query head."""
+    total = 0
+    for b in range(len(context_lens)):
+        n = int(context_lens[b])
+        ql = int(cu_seqlens_q[b + 1]) - int(cu_seqlens_q[b])
+        keys = ql * (n - ql) + ql * (ql + 1) // 2
+        total += 4 * D * H * keys
+    return total
