@@ -528,6 +528,82 @@ def run_gpu(args, world, rank, local):
     return line
 
 
+def run_prefill(args, world, rank, local):
+    """Causal varlen prefill attention over the paged cache: TFLOP/s of the
+    tensor-core kernel against the measured bf16 matmul peak."""
+    from paged_kv_cache_67_gb300 import build as libbuild
+    import paged_kv_cache_67_gb300 as pkv
+
+    libbuild.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    cfg = wl.PREFILL_CONFIGS[args.workload]
+    inp = wl.make_prefill_inputs(cfg, seed=1234 + rank, device=dev)
+    tables, cu, lens = inp.block_tables.to(dev), inp.cu_seqlens_q.to(dev), inp.context_lens.to(dev)
+    out = torch.empty_like(inp.q)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    flops = wl.prefill_flops(inp.context_lens, inp.cu_seqlens_q, cfg.H, cfg.D)
+
+    def step():
+        pkv.pkv_prefill_attention(out, inp.q, inp.k_cache, inp.v_cache, tables, cu, lens, inp.scale,
+                                  max_q_len=inp.max_q_len, err_flags=err, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        t_start.record(stream)
+        for a, b in evs:
+            a.record(stream)
+            step()
+            b.record(stream)
+        t_end.record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    if int(err.item()) != 0:
+        raise RuntimeError(f"device error flags {int(err.item()):#x}")
+    elapsed = t_start.elapsed_time(t_end) * 1e-3
+    k_ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    value, tmax, _ = aggregate(elapsed, flops * args.steps / 1e12, world, dev)
+    if rank != 0:
+        return None
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            pk = json.load(f)
+        peak, peak_s, src = float(pk["bf16_tflops"]), float(pk["bf16_tflops_sustained"]), "measured"
+    except Exception:
+        peak, peak_s, src = 1900.0, 1700.0, "fallback"
+    achieved = flops / (k_ms * 1e-3) / 1e12
+    line = {
+        "metric": "paged causal prefill attn achieved TFLOP/s", "value": round(value, 1),
+        "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(tmax / args.steps * 1e3, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": (f"{args.workload}: B={cfg.B} H={cfg.H} KVH={cfg.KVH} D={cfg.D} "
+                                f"block_size={cfg.bs}, context_lens U[{cfg.len_lo},{cfg.len_hi}], even "
+                                f"sequences prefill the whole prompt, odd ones a chunk of "
+                                f"U[{cfg.chunk_lo},{cfg.chunk_hi}] queries on a cached prefix; "
+                                f"{int(inp.cu_seqlens_q[-1])} queries"),
+                   "flops_per_step": flops,
+                   "l2": "q, out and K/V larger than L2, no flush"},
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak,
+                     "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+                     "frac_of_sustained": round(achieved / peak_s, 4), "traffic": None,
+                     "kernel": "pkv_prefill_tc_kernel<128, bf16>",
+                     "peak_source": f"{src} (MEASURED_PEAKS.json bf16_tflops)",
+                     "kernel_us": round(k_ms * 1e3, 2)},
+        "e2e": None, "gpu_launches": args.steps, "clocks": clocks.summary(), "cpu_baseline": None,
+    }
+    print(json.dumps(line), flush=True)
+    return line
+
+
 def run_e2e(args, world, dev, pkv, inp, steps, out, ws, err, stream, max_ctx, fused, total_bytes):
     """The same steps end to end through the public API: each step's inputs
     copied in from pinned host memory, the output read back and waited for."""
@@ -580,7 +656,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only-decode", action="store_true",
                     help="warm-up + timed steps only (no bulk fill, e2e or CPU baseline): for profiling")
-    ap.add_argument("--workload", default=WORKLOAD, choices=sorted(wl.CONFIGS),
+    ap.add_argument("--workload", default=WORKLOAD,
+                    choices=sorted(wl.CONFIGS) + sorted(wl.PREFILL_CONFIGS),
                     help="the batch the steps run on (default: the Llama-3-8B-shaped decode)")
     ap.add_argument("--mode", default="fused", choices=["fused", "two-launch"],
                     help="fused: one pkv_write_decode_attention launch per step; two-launch: "
@@ -594,6 +671,8 @@ def main():
     try:
         if args.impl == "reference":
             run_reference(args, world, rank)
+        elif args.workload in wl.PREFILL_CONFIGS:
+            run_prefill(args, world, rank, local)
         else:
             run_gpu(args, world, rank, local)
     finally:

@@ -338,7 +338,7 @@ PKV_API pkv_status pkv_prefill_attention(void *out, const void *q, const void *k
       reinterpret_cast<uintptr_t>(context_lens) % 4)
     return PKV_ERR_INVALID_ARG;
   const long long mq = max_q_len > 0 ? max_q_len : total_q;
-  const long long q_tiles = (mq + 127) / 128;
+  const long long q_tiles = (mq + 255) / 256;  // 256 queries (two 128-row tiles) per CTA
   if (q_tiles > 65535) return PKV_ERR_UNSUPPORTED;
   return launch_prefill_tc(out, q, k_cache, v_cache, block_tables, cu_seqlens_q, context_lens, B,
                            H, num_kv_heads, head_dim, block_size, max_blocks, num_blocks, scale, dt,

@@ -15,20 +15,23 @@
 // The tile-wise online softmax is the block-wise one of the interview note
 // "PagedAttention kernel: paged KV cache 与 block table", section 代码.
 //
-// Work decomposition.  CTA = (query head, 128-query tile, sequence), the
-// heaviest tiles (latest queries) first; 6 warps:
-//   warp 0     producer: per 128-token KV tile, 32 lanes issue one tiled TMA
+// Work decomposition.  CTA = (query head, 256 queries, sequence), the
+// latest (heaviest) query tiles first; 10 warps:
+//   warp 0     producer: per 64-token KV tile, 16 lanes issue one tiled TMA
 //              load each (a 16-token chunk of one 64-column region of K or V
-//              of this KV head, 128-byte swizzle) into a 2-stage ring;
-//   warp 1     MMA issuer (one thread): S = Q . K^T (M = 128 queries,
-//              N = 128 tokens, fp32 in tensor memory), then O += P . V
-//              (N = D), S of the next tile issued before P . V of this one;
-//   warps 2-5  softmax, one query row per thread (its tensor-memory lane):
-//              stage Q, then per tile read S, mask (causal, end of context),
-//              update the running max -- the reference max moves only when
-//              the row max grows by more than 2^8, and only then is the
-//              O row in tensor memory rescaled -- write P = 2^(s - m) as
-//              bf16/fp16 into a swizzled shared tile, and finally O / l.
+//              of this KV head, 128-byte swizzle) into a 3-stage ring;
+//   warp 1     MMA issuer (one thread), alternating between the two query
+//              tiles: S_g = Q_g . K^T (M = 128, N = 64 tokens, fp32 in tensor
+//              memory), then O_g += P_g . V (N = D); the next tile's S_g is
+//              issued before this tile's P_g . V, so while one warpgroup
+//              works on its scores the tensor core serves the other;
+//   warps 2-5, 6-9  two softmax warpgroups, one per 128-query tile, one query
+//              row per thread (its tensor-memory lane): stage Q, then per KV
+//              tile read S, mask (causal, end of context), update the running
+//              max -- the reference max moves only when the row max grows by
+//              more than 2^8, and only then is the O row in tensor memory
+//              rescaled -- write P = 2^(s - m) as bf16/fp16 into a swizzled
+//              shared tile, and finally O / l.
 // Every wait on an mbarrier is bounded; on time-out the CTA raises
 // PKV_FLAG_TIMEOUT, lets its copies and products land (bounded) and exits.
 #include <string.h>
@@ -41,12 +44,14 @@
 
 namespace pkv {
 
-constexpr int kPfRows = 128;     // query rows per CTA (MMA M)
-constexpr int kPfTile = 128;     // KV tokens per tile
-constexpr int kPfStages = 2;     // K/V ring depth
-constexpr int kPfWarps = 6;
+constexpr int kPfRows = 128;     // query rows per softmax warpgroup (MMA M)
+constexpr int kPfGroups = 2;     // query tiles per CTA, one softmax warpgroup each
+constexpr int kPfTile = 64;      // KV tokens per tile
+constexpr int kPfStages = 3;     // K/V ring depth
+constexpr int kPfWarps = 2 + 4 * kPfGroups;
 constexpr int kPfThreads = 32 * kPfWarps;
-constexpr int kRegionBytes = 128 * 128;  // 128 rows x 64 elements of 16 bits
+constexpr int kQRegion = kPfRows * 128;   // 128 query rows x 64 elements of 16 bits
+constexpr int kKVRegion = kPfTile * 128;  // 64 token rows x 64 elements
 
 struct PrefillArgs {
   void *out;
@@ -57,20 +62,21 @@ struct PrefillArgs {
   int *err;
   long long num_blocks;
   int B, H, KVH, D, G, bs, max_blocks;
-  int q_tiles;        // 128-query tiles per sequence the grid covers (gridDim.y)
+  int q_tiles;        // 256-query tiles per sequence the grid covers (gridDim.y)
   float scale_log2;   // scale * log2(e)
 };
 
 template <int D>
 struct PfShape {
   static constexpr int kRegions = D / 64;
-  static constexpr int kTileBytes = kRegions * kRegionBytes;      // one 128-row operand
-  static constexpr int kQOff = 0;
-  static constexpr int kKVOff = kQOff + kTileBytes;               // [stage][K, V]
-  static constexpr int kPOff = kKVOff + kPfStages * 2 * kTileBytes;
-  static constexpr int kBarOff = kPOff + 2 * kRegionBytes;        // P: 128 tokens
-  static constexpr int kSmem = kBarOff + 256 + 1024;              // + alignment slack
-  static constexpr uint32_t kTmemCols = 256;                      // S: 128, O: D
+  static constexpr int kQBytes = kRegions * kQRegion;           // one warpgroup's query tile
+  static constexpr int kKVBytes = kRegions * kKVRegion;         // one K (or V) tile
+  static constexpr int kQOff = 0;                               // [group]
+  static constexpr int kKVOff = kQOff + kPfGroups * kQBytes;    // [stage][K, V]
+  static constexpr int kPOff = kKVOff + kPfStages * 2 * kKVBytes;  // [group] 128 x 64 tokens
+  static constexpr int kBarOff = kPOff + kPfGroups * kQRegion;
+  static constexpr int kSmem = kBarOff + 256 + 1024;            // + alignment slack
+  static constexpr uint32_t kTmemCols = 512;  // S: 2 x 64, O: 2 x D (from column 128)
 };
 
 // Tiled 4-D TMA load global -> shared with the default L2 policy (the K/V
@@ -117,14 +123,14 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t *bars = reinterpret_cast<uint64_t *>(sm + Sh::kBarOff);
   uint64_t *q_full = bars + 0;
-  uint64_t *kv_full = bars + 1;    // [2]
-  uint64_t *kv_empty = bars + 3;   // [2]
-  uint64_t *s_full = bars + 5;
-  uint64_t *p_full = bars + 6;
-  uint64_t *o_done = bars + 7;
-  uint64_t *mma_done = bars + 8;
-  uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(bars + 12);
-  int *abort_flag = reinterpret_cast<int *>(bars + 13);
+  uint64_t *kv_full = bars + 1;    // [kPfStages]
+  uint64_t *kv_empty = bars + 4;   // [kPfStages]
+  uint64_t *s_full = bars + 7;     // [kPfGroups]
+  uint64_t *p_full = bars + 9;     // [kPfGroups]
+  uint64_t *o_done = bars + 11;    // [kPfGroups]
+  uint64_t *mma_done = bars + 13;
+  uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(bars + 16);
+  int *abort_flag = reinterpret_cast<int *>(bars + 17);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int h = blockIdx.x, b = blockIdx.z;
@@ -138,24 +144,30 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     if (lead) raise_flag(a.err, PKV_FLAG_QUERY_LEN);
     return;
   }
-  if (qlen > a.q_tiles * kPfRows && lead) raise_flag(a.err, PKV_FLAG_QUERY_OVER_HINT);
-  const int i0 = qt * kPfRows;
+  if (qlen > a.q_tiles * kPfGroups * kPfRows && lead) raise_flag(a.err, PKV_FLAG_QUERY_OVER_HINT);
+  const int i0 = qt * kPfGroups * kPfRows;
   if (i0 >= qlen) return;
-  const int rows = min(kPfRows, qlen - i0);
+  const int rows = min(kPfGroups * kPfRows, qlen - i0);
   const int p_first = n - qlen + i0;               // position of query row 0
-  const int p_last = p_first + rows - 1;           // position of the last real row
-  const int ntiles = p_last / kPfTile + 1;
+  // tiles each warpgroup needs: up to the position of its last real row
+  const int rows1 = rows - kPfRows;                // rows of the second tile (may be <= 0)
+  const int ntiles0 = (p_first + min(kPfRows, rows) - 1) / kPfTile + 1;
+  const int ntiles1 = rows1 > 0 ? (p_first + kPfRows + rows1 - 1) / kPfTile + 1 : 0;
+  const int ntiles = max(ntiles0, ntiles1);
+  auto tiles_of = [&](int g) { return g == 0 ? ntiles0 : ntiles1; };
   const int kvh = h / a.G;
 
   if (tid == 0) {
-    mbar_init(q_full, 128);
+    mbar_init(q_full, 4 * 32 * kPfGroups);
     for (int s = 0; s < kPfStages; ++s) {
       mbar_init(&kv_full[s], 1);
       mbar_init(&kv_empty[s], 1);
     }
-    mbar_init(s_full, 1);
-    mbar_init(p_full, 128);
-    mbar_init(o_done, 1);
+    for (int g = 0; g < kPfGroups; ++g) {
+      mbar_init(&s_full[g], 1);
+      mbar_init(&p_full[g], 128);
+      mbar_init(&o_done[g], 1);
+    }
     mbar_init(mma_done, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -165,20 +177,19 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
-  const uint32_t tmem_s = tmem, tmem_o = tmem + 128;
   constexpr bool bf16 = std::is_same<T, __nv_bfloat16>::value;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    const int per_tensor = 8 * Sh::kRegions;       // boxes of K (or V) per tile
+    const int per_tensor = 4 * Sh::kRegions;     // boxes of K (or V) per 64-token tile
     const bool issuer = lane < 2 * per_tensor;
     const bool is_v = lane >= per_tensor;
-    const int region = (lane % per_tensor) >> 3, chunk = lane & 7;
+    const int region = (lane % per_tensor) >> 2, chunk = lane & 3;
     int issued = 0;
     for (int j = 0; j < ntiles; ++j) {
-      const int stage = j & 1;
+      const int stage = j % kPfStages;
       if (j >= kPfStages) {
-        const bool ok = mbar_wait_bounded(&kv_empty[stage], ((j >> 1) - 1) & 1);
+        const bool ok = mbar_wait_bounded(&kv_empty[stage], (j / kPfStages - 1) & 1);
         if (!__all_sync(0xffffffffu, ok) || *(volatile int *)abort_flag) {
           if (lane == 0) {
             raise_flag(a.err, PKV_FLAG_TIMEOUT);
@@ -188,7 +199,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         }
       }
       const int tok0 = j * kPfTile;
-      const int valid_chunks = min(8, (n - tok0 + 15) >> 4);
+      const int valid_chunks = min(4, (n - tok0 + 15) >> 4);
       if (lane == 0)
         mbar_arrive_expect_tx(&kv_full[stage],
                               (uint32_t)(valid_chunks * 2 * Sh::kRegions * 2048));
@@ -201,8 +212,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           raise_flag(a.err, PKV_FLAG_BLOCK_OUT_OF_RANGE);
           phys = 0;
         }
-        uint8_t *dst = sm + Sh::kKVOff + stage * 2 * Sh::kTileBytes + (is_v ? Sh::kTileBytes : 0) +
-                       region * kRegionBytes + chunk * 2048;
+        uint8_t *dst = sm + Sh::kKVOff + stage * 2 * Sh::kKVBytes + (is_v ? Sh::kKVBytes : 0) +
+                       region * kKVRegion + chunk * 2048;
         tma_load_4d_keep(dst, is_v ? &tmV : &tmK, &kv_full[stage], region * 64, kvh, t - lb * a.bs,
                          phys);
       }
@@ -210,50 +221,54 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     }
     // the last fills land before the CTA can end (bounded)
     for (int j = max(0, issued - kPfStages); j < issued; ++j)
-      mbar_wait_bounded(&kv_full[j & 1], (j >> 1) & 1);
+      mbar_wait_bounded(&kv_full[j % kPfStages], (j / kPfStages) & 1);
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       const uint32_t idesc_s = umma_idesc_f16(128, kPfTile, bf16, false);
       const uint32_t idesc_o = umma_idesc_f16(128, D, bf16, true);
-      const uint32_t q_base = smem_u32(sm + Sh::kQOff), p_base = smem_u32(sm + Sh::kPOff);
       auto kv_base = [&](int j, bool v) {
-        return smem_u32(sm + Sh::kKVOff + (j & 1) * 2 * Sh::kTileBytes + (v ? Sh::kTileBytes : 0));
+        return smem_u32(sm + Sh::kKVOff + (j % kPfStages) * 2 * Sh::kKVBytes +
+                        (v ? Sh::kKVBytes : 0));
       };
-      auto issue_s = [&](int j) {  // S = Q . K_j^T over D in 16-wide steps
-        const uint32_t kb = kv_base(j, false);
+      auto issue_s = [&](int g, int j) {  // S_g = Q_g . K_j^T over D in 16-wide steps
+        const uint32_t qb = smem_u32(sm + Sh::kQOff + g * Sh::kQBytes), kb = kv_base(j, false);
 #pragma unroll
-        for (int k = 0; k < D / 16; ++k) {
-          const uint32_t off = (k >> 2) * kRegionBytes + (k & 3) * 32;
-          umma_f16(tmem_s, umma_desc_sw128(q_base + off, 16, 1024),
-                   umma_desc_sw128(kb + off, 16, 1024), idesc_s, k > 0);
-        }
-        umma_commit(s_full);
+        for (int k = 0; k < D / 16; ++k)
+          umma_f16(tmem + 64 * g, umma_desc_sw128(qb + (k >> 2) * kQRegion + (k & 3) * 32, 16, 1024),
+                   umma_desc_sw128(kb + (k >> 2) * kKVRegion + (k & 3) * 32, 16, 1024), idesc_s,
+                   k > 0);
+        umma_commit(&s_full[g]);
+      };
+      auto issue_pv = [&](int g, int j) {  // O_g += P_g . V_j over 16-token steps
+        const uint32_t pb = smem_u32(sm + Sh::kPOff + g * kQRegion), vb = kv_base(j, true);
+#pragma unroll
+        for (int k = 0; k < kPfTile / 16; ++k)
+          umma_f16(tmem + 128 + D * g, umma_desc_sw128(pb + k * 32, 16, 1024),
+                   umma_desc_sw128(vb + k * 2048, kKVRegion, 1024), idesc_o, (j > 0 || k > 0));
+        umma_commit(&o_done[g]);
       };
       bool ok = mbar_wait_bounded(q_full, 0) && mbar_wait_bounded(&kv_full[0], 0);
       if (ok) {
         tc_fence_after();
-        issue_s(0);
+        for (int g = 0; g < kPfGroups; ++g)
+          if (tiles_of(g) > 0) issue_s(g, 0);
       }
       for (int j = 0; ok && j < ntiles; ++j) {
-        ok = mbar_wait_bounded(p_full, j & 1) && !*(volatile int *)abort_flag;
-        if (!ok) break;
-        tc_fence_after();
-        if (j + 1 < ntiles) {
-          ok = mbar_wait_bounded(&kv_full[(j + 1) & 1], ((j + 1) >> 1) & 1);
+        for (int g = 0; g < kPfGroups && ok; ++g) {
+          if (j >= tiles_of(g)) continue;
+          ok = mbar_wait_bounded(&p_full[g], j & 1) && !*(volatile int *)abort_flag;
           if (!ok) break;
           tc_fence_after();
-          issue_s(j + 1);
+          if (j + 1 < tiles_of(g)) {  // S of the next tile into this group's S columns
+            ok = mbar_wait_bounded(&kv_full[(j + 1) % kPfStages], ((j + 1) / kPfStages) & 1);
+            if (!ok) break;
+            tc_fence_after();
+            issue_s(g, j + 1);
+          }
+          issue_pv(g, j);
         }
-        const uint32_t vb = kv_base(j, true);
-#pragma unroll
-        for (int k = 0; k < kPfTile / 16; ++k) {  // O += P_j . V_j over 16-token steps
-          const uint32_t poff = (k >> 2) * kRegionBytes + (k & 3) * 32;
-          umma_f16(tmem_o, umma_desc_sw128(p_base + poff, 16, 1024),
-                   umma_desc_sw128(vb + k * 2048, kRegionBytes, 1024), idesc_o, (j > 0 || k > 0));
-        }
-        umma_commit(o_done);
-        umma_commit(&kv_empty[j & 1]);
+        if (ok) umma_commit(&kv_empty[j % kPfStages]);
       }
       if (!ok) {
         raise_flag(a.err, PKV_FLAG_TIMEOUT);
@@ -265,21 +280,25 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ softmax
+    const int g = (warp - 2) >> 2;                      // warpgroup = query tile
     const int quarter = warp & 3;
-    const int r = 32 * quarter + lane;                  // query row = tensor-memory lane
+    const int r = 32 * quarter + lane;                  // row in the tile = tensor-memory lane
+    const int rr = g * kPfRows + r;                     // row in the CTA
     const uint32_t lane_off = (uint32_t)(32 * quarter) << 16;
-    const bool real_row = r < rows;
-    const int p_row = p_first + (real_row ? r : rows - 1);  // padding rows mirror the last row
-    const size_t q_row = (size_t)(q0 + i0 + (real_row ? r : 0)) * a.H + h;
+    const uint32_t tmem_s = tmem + 64 * g, tmem_o = tmem + 128 + D * g;
+    const bool real_row = rr < rows;
+    const int p_row = p_first + (real_row ? rr : rows - 1);  // padding rows mirror the last row
+    const size_t q_row = (size_t)(q0 + i0 + (real_row ? rr : 0)) * a.H + h;
+    const int my_tiles = tiles_of(g);
 
-    // stage this row of Q into the swizzled K-major tile
+    // stage this row of Q into the group's swizzled K-major tile
     {
       const uint4 *src = reinterpret_cast<const uint4 *>(reinterpret_cast<const T *>(a.q) + q_row * D);
+      uint8_t *qt_base = sm + Sh::kQOff + g * Sh::kQBytes + r * 128;
 #pragma unroll
       for (int c = 0; c < D / 8; ++c) {
         const uint4 v = real_row ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
-        *reinterpret_cast<uint4 *>(sm + Sh::kQOff + (c >> 3) * kRegionBytes + r * 128 +
-                                   (((c & 7) ^ (r & 7)) << 4)) = v;
+        *reinterpret_cast<uint4 *>(qt_base + (c >> 3) * kQRegion + (((c & 7) ^ (r & 7)) << 4)) = v;
       }
       fence_proxy_async_shared();
       mbar_arrive(q_full);
@@ -287,23 +306,24 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 
     float m_used = -INFINITY, l = 0.f;
     bool ok = true;
-    for (int j = 0; j < ntiles; ++j) {
-      ok = mbar_wait_bounded(s_full, j & 1);
+    for (int j = 0; j < my_tiles; ++j) {
+      ok = mbar_wait_bounded(&s_full[g], j & 1);
       if (!__all_sync(0xffffffffu, ok) || *(volatile int *)abort_flag) {
         ok = false;
         break;
       }
       tc_fence_after();
       const int t0 = j * kPfTile;
-      // pass 1: the row max of the scaled scores of tokens t <= p_row
+      float s[kPfTile];
+      tmem_ld32(tmem_s + lane_off, *reinterpret_cast<float(*)[32]>(s));
+      tmem_ld32(tmem_s + lane_off + 32, *reinterpret_cast<float(*)[32]>(s + 32));
+      // causal mask and row max of the scaled scores
+      const bool full = t0 + kPfTile - 1 <= p_row;      // no masked token in this tile
       float mx = -INFINITY;
 #pragma unroll
-      for (int cc = 0; cc < kPfTile / 32; ++cc) {
-        float v[32];
-        tmem_ld32(tmem_s + lane_off + 32 * cc, v);
-#pragma unroll
-        for (int i = 0; i < 32; ++i)
-          if (t0 + 32 * cc + i <= p_row) mx = fmaxf(mx, v[i] * a.scale_log2);
+      for (int i = 0; i < kPfTile; ++i) {
+        s[i] = (full || t0 + i <= p_row) ? s[i] * a.scale_log2 : -INFINITY;
+        mx = fmaxf(mx, s[i]);
       }
       // the reference max moves only when the row max exceeds it by 2^8
       const float m_new = (mx > m_used + 8.f) ? mx : m_used;
@@ -314,7 +334,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 
       // P_{j-1} . V_{j-1} must be done: P's tile is rewritten and O is read
       if (j > 0) {
-        ok = mbar_wait_bounded(o_done, (j - 1) & 1);
+        ok = mbar_wait_bounded(&o_done[g], (j - 1) & 1);
         if (!__all_sync(0xffffffffu, ok)) break;
         tc_fence_after();
         if (rescale) {
@@ -328,48 +348,38 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           }
         }
       }
-      // the last tile's V rows past the context are zeroed (they may hold
+      // the tile's V rows past the context are zeroed (they may hold
       // anything, and 0 * NaN would poison the product)
       if (t0 + kPfTile > n) {
-        ok = mbar_wait_bounded(&kv_full[j & 1], (j >> 1) & 1);
+        ok = mbar_wait_bounded(&kv_full[j % kPfStages], (j / kPfStages) & 1);
         if (!__all_sync(0xffffffffu, ok)) break;
-        if (r >= n - t0) {
-          uint8_t *vrow = sm + Sh::kKVOff + (j & 1) * 2 * Sh::kTileBytes + Sh::kTileBytes + r * 128;
+        if (r < kPfTile && r >= n - t0) {
+          uint8_t *vrow = sm + Sh::kKVOff + (j % kPfStages) * 2 * Sh::kKVBytes + Sh::kKVBytes + r * 128;
 #pragma unroll
-          for (int g = 0; g < Sh::kRegions; ++g)
+          for (int rg = 0; rg < Sh::kRegions; ++rg)
 #pragma unroll
             for (int c = 0; c < 8; ++c)
-              *reinterpret_cast<uint4 *>(vrow + g * kRegionBytes + c * 16) = make_uint4(0, 0, 0, 0);
+              *reinterpret_cast<uint4 *>(vrow + rg * kKVRegion + c * 16) = make_uint4(0, 0, 0, 0);
         }
       }
-      // pass 2: P = 2^(s - m) (0 past p_row), rounded to the input type, into
-      // the swizzled K-major P tile; l sums the rounded weights
+      // P = 2^(s - m) rounded to the input type into the group's swizzled
+      // K-major P tile (64 tokens = one 128-byte row); l sums the rounded weights
+      uint8_t *prow = sm + Sh::kPOff + g * kQRegion + r * 128;
 #pragma unroll
-      for (int cc = 0; cc < kPfTile / 32; ++cc) {
-        float v[32];
-        tmem_ld32(tmem_s + lane_off + 32 * cc, v);
-        uint32_t pk[16];
+      for (int c = 0; c < 8; ++c) {
+        uint32_t pk[4];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int t = t0 + 32 * cc + 2 * i;
-          const float e0 = t <= p_row ? fast_exp2(v[2 * i] * a.scale_log2 - m_used) : 0.f;
-          const float e1 = t + 1 <= p_row ? fast_exp2(v[2 * i + 1] * a.scale_log2 - m_used) : 0.f;
-          pk[i] = PackPair<T>::run(e0, e1, l);
-        }
-        uint8_t *prow = sm + Sh::kPOff + (cc >> 1) * kRegionBytes + r * 128;
-#pragma unroll
-        for (int c4 = 0; c4 < 4; ++c4) {
-          const int chunk = (cc & 1) * 4 + c4;
-          *reinterpret_cast<uint4 *>(prow + ((chunk ^ (r & 7)) << 4)) =
-              make_uint4(pk[4 * c4], pk[4 * c4 + 1], pk[4 * c4 + 2], pk[4 * c4 + 3]);
-        }
+        for (int e = 0; e < 4; ++e)
+          pk[e] = PackPair<T>::run(fast_exp2(s[8 * c + 2 * e] - m_used),
+                                   fast_exp2(s[8 * c + 2 * e + 1] - m_used), l);
+        *reinterpret_cast<uint4 *>(prow + ((c ^ (r & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
       }
       fence_proxy_async_shared();
       tc_fence_before();
-      mbar_arrive(p_full);
+      mbar_arrive(&p_full[g]);
     }
-    if (ok) ok = mbar_wait_bounded(o_done, (ntiles - 1) & 1);
-    if (__all_sync(0xffffffffu, ok) && !*(volatile int *)abort_flag) {
+    if (ok && my_tiles > 0) ok = mbar_wait_bounded(&o_done[g], (my_tiles - 1) & 1);
+    if (my_tiles > 0 && __all_sync(0xffffffffu, ok) && !*(volatile int *)abort_flag) {
       tc_fence_after();
       const float inv_l = 1.f / l;
       T *orow = reinterpret_cast<T *>(a.out) + q_row * D;
@@ -388,7 +398,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             dst[c4] = make_uint4(pk[4 * c4], pk[4 * c4 + 1], pk[4 * c4 + 2], pk[4 * c4 + 3]);
         }
       }
-    } else if (lane == 0) {
+    } else if (my_tiles > 0 && lane == 0) {
       raise_flag(a.err, PKV_FLAG_TIMEOUT);
       *(volatile int *)abort_flag = 1;
     }
