@@ -73,8 +73,8 @@ struct PfShape {
   static constexpr int kKVBytes = kRegions * kKVRegion;         // one K (or V) tile
   static constexpr int kQOff = 0;                               // [group]
   static constexpr int kKVOff = kQOff + kPfGroups * kQBytes;    // [stage][K, V]
-  static constexpr int kPOff = kKVOff + kPfStages * 2 * kKVBytes;  // [group] 128 x 64 tokens
-  static constexpr int kBarOff = kPOff + kPfGroups * kQRegion;
+  static constexpr int kPOff = kKVOff + kPfStages * 2 * kKVBytes;  // [group][2] 128 x 64 tokens
+  static constexpr int kBarOff = kPOff + kPfGroups * 2 * kQRegion;
   static constexpr int kSmem = kBarOff + 256 + 1024;            // + alignment slack
   static constexpr uint32_t kTmemCols = 512;  // S: 2 x 64, O: 2 x D (from column 128)
 };
@@ -91,24 +91,42 @@ __device__ __forceinline__ void tma_load_4d_keep(void *dst, const CUtensorMap *m
       : "memory");
 }
 
+// Blackwell paired fp32 arithmetic and the three-input max.
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  unsigned long long d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;"
+      : "=l"(d)
+      : "l"(*reinterpret_cast<unsigned long long *>(&a)), "l"(*reinterpret_cast<unsigned long long *>(&b)),
+        "l"(*reinterpret_cast<unsigned long long *>(&c)));
+  return *reinterpret_cast<float2 *>(&d);
+}
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
+  unsigned long long d;
+  asm("add.rn.f32x2 %0, %1, %2;"
+      : "=l"(d)
+      : "l"(*reinterpret_cast<unsigned long long *>(&a)), "l"(*reinterpret_cast<unsigned long long *>(&b)));
+  return *reinterpret_cast<float2 *>(&d);
+}
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 template <typename T>
 struct PackPair;
 template <>
 struct PackPair<__nv_bfloat16> {
-  // two fp32 -> packed bf16 pair (RNE); also adds the rounded values to sum
-  __device__ __forceinline__ static uint32_t run(float lo, float hi, float &sum) {
+  // two fp32 -> packed bf16 pair (round to nearest even)
+  __device__ __forceinline__ static uint32_t pack(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-    const float2 f = __bfloat1622float2(v);
-    sum += f.x + f.y;
     return *reinterpret_cast<uint32_t *>(&v);
   }
 };
 template <>
 struct PackPair<__half> {
-  __device__ __forceinline__ static uint32_t run(float lo, float hi, float &sum) {
+  __device__ __forceinline__ static uint32_t pack(float lo, float hi) {
     __half2 v = __floats2half2_rn(lo, hi);
-    const float2 f = __half22float2(v);
-    sum += f.x + f.y;
     return *reinterpret_cast<uint32_t *>(&v);
   }
 };
@@ -123,14 +141,16 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t *bars = reinterpret_cast<uint64_t *>(sm + Sh::kBarOff);
   uint64_t *q_full = bars + 0;
-  uint64_t *kv_full = bars + 1;    // [kPfStages]
-  uint64_t *kv_empty = bars + 4;   // [kPfStages]
-  uint64_t *s_full = bars + 7;     // [kPfGroups]
-  uint64_t *p_full = bars + 9;     // [kPfGroups]
-  uint64_t *o_done = bars + 11;    // [kPfGroups]
-  uint64_t *mma_done = bars + 13;
-  uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(bars + 16);
-  int *abort_flag = reinterpret_cast<int *>(bars + 17);
+  uint64_t *k_full = bars + 1;     // [kPfStages]: K and V of a stage arrive and are
+  uint64_t *v_full = bars + 4;     // [kPfStages]  released separately, so the next
+  uint64_t *k_empty = bars + 7;    // [kPfStages]  keys are fetched as soon as the
+  uint64_t *v_empty = bars + 10;   // [kPfStages]  scores that read a slot are done
+  uint64_t *s_full = bars + 13;    // [kPfGroups][2]: S buffers of each group
+  uint64_t *p_full = bars + 17;    // [kPfGroups][2]: P buffers of each group
+  uint64_t *o_done = bars + 21;    // [kPfGroups][2]: P . V of an even / odd tile done
+  uint64_t *mma_done = bars + 25;
+  uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(bars + 26);
+  int *abort_flag = reinterpret_cast<int *>(bars + 27);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int h = blockIdx.x, b = blockIdx.z;
@@ -160,13 +180,18 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   if (tid == 0) {
     mbar_init(q_full, 4 * 32 * kPfGroups);
     for (int s = 0; s < kPfStages; ++s) {
-      mbar_init(&kv_full[s], 1);
-      mbar_init(&kv_empty[s], 1);
+      mbar_init(&k_full[s], 1);
+      mbar_init(&v_full[s], 1);
+      mbar_init(&k_empty[s], 1);
+      mbar_init(&v_empty[s], 1);
     }
     for (int g = 0; g < kPfGroups; ++g) {
-      mbar_init(&s_full[g], 1);
-      mbar_init(&p_full[g], 128);
-      mbar_init(&o_done[g], 1);
+      mbar_init(&s_full[2 * g], 1);
+      mbar_init(&s_full[2 * g + 1], 1);
+      for (int k = 0; k < 2; ++k) {
+        mbar_init(&p_full[2 * g + k], 128);
+        mbar_init(&o_done[2 * g + k], 1);
+      }
     }
     mbar_init(mma_done, 1);
     *abort_flag = 0;
@@ -181,47 +206,54 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
+    // per tile: the K boxes (lanes 0 .. per_tensor-1) once the keys of tile
+    // j-3 are no longer read, then the V boxes (the next lanes) once the
+    // values of tile j-3 are no longer read
     const int per_tensor = 4 * Sh::kRegions;     // boxes of K (or V) per 64-token tile
-    const bool issuer = lane < 2 * per_tensor;
-    const bool is_v = lane >= per_tensor;
     const int region = (lane % per_tensor) >> 2, chunk = lane & 3;
     int issued = 0;
-    for (int j = 0; j < ntiles; ++j) {
+    bool ok = true;
+    for (int j = 0; j < ntiles && ok; ++j) {
       const int stage = j % kPfStages;
-      if (j >= kPfStages) {
-        const bool ok = mbar_wait_bounded(&kv_empty[stage], (j / kPfStages - 1) & 1);
-        if (!__all_sync(0xffffffffu, ok) || *(volatile int *)abort_flag) {
-          if (lane == 0) {
-            raise_flag(a.err, PKV_FLAG_TIMEOUT);
-            *(volatile int *)abort_flag = 1;
-          }
-          break;
-        }
-      }
       const int tok0 = j * kPfTile;
       const int valid_chunks = min(4, (n - tok0 + 15) >> 4);
-      if (lane == 0)
-        mbar_arrive_expect_tx(&kv_full[stage],
-                              (uint32_t)(valid_chunks * 2 * Sh::kRegions * 2048));
-      __syncwarp();
-      if (issuer && chunk < valid_chunks) {
-        const int t = tok0 + 16 * chunk;
-        const int lb = t / a.bs;
-        int phys = __ldg(a.tables + (size_t)b * a.max_blocks + lb);
-        if (phys < 0 || (long long)phys >= a.num_blocks) {
-          raise_flag(a.err, PKV_FLAG_BLOCK_OUT_OF_RANGE);
-          phys = 0;
+      const uint32_t bytes = (uint32_t)(valid_chunks * Sh::kRegions * 2048);
+      for (int v = 0; v < 2 && ok; ++v) {
+        if (j >= kPfStages) {
+          const bool got = mbar_wait_bounded(v ? &v_empty[stage] : &k_empty[stage],
+                                             (j / kPfStages - 1) & 1);
+          if (!__all_sync(0xffffffffu, got) || *(volatile int *)abort_flag) {
+            if (lane == 0) {
+              raise_flag(a.err, PKV_FLAG_TIMEOUT);
+              *(volatile int *)abort_flag = 1;
+            }
+            ok = false;
+            break;
+          }
         }
-        uint8_t *dst = sm + Sh::kKVOff + stage * 2 * Sh::kKVBytes + (is_v ? Sh::kKVBytes : 0) +
-                       region * kKVRegion + chunk * 2048;
-        tma_load_4d_keep(dst, is_v ? &tmV : &tmK, &kv_full[stage], region * 64, kvh, t - lb * a.bs,
-                         phys);
+        uint64_t *full = v ? &v_full[stage] : &k_full[stage];
+        if (lane == 0) mbar_arrive_expect_tx(full, bytes);
+        __syncwarp();
+        if (lane >= v * per_tensor && lane < (v + 1) * per_tensor && chunk < valid_chunks) {
+          const int t = tok0 + 16 * chunk;
+          const int lb = t / a.bs;
+          int phys = __ldg(a.tables + (size_t)b * a.max_blocks + lb);
+          if (phys < 0 || (long long)phys >= a.num_blocks) {
+            raise_flag(a.err, PKV_FLAG_BLOCK_OUT_OF_RANGE);
+            phys = 0;
+          }
+          uint8_t *dst = sm + Sh::kKVOff + stage * 2 * Sh::kKVBytes + (v ? Sh::kKVBytes : 0) +
+                         region * kKVRegion + chunk * 2048;
+          tma_load_4d_keep(dst, v ? &tmV : &tmK, full, region * 64, kvh, t - lb * a.bs, phys);
+        }
       }
-      ++issued;
+      if (ok) ++issued;
     }
     // the last fills land before the CTA can end (bounded)
-    for (int j = max(0, issued - kPfStages); j < issued; ++j)
-      mbar_wait_bounded(&kv_full[j % kPfStages], (j / kPfStages) & 1);
+    for (int j = max(0, issued - kPfStages); j < issued; ++j) {
+      mbar_wait_bounded(&k_full[j % kPfStages], (j / kPfStages) & 1);
+      mbar_wait_bounded(&v_full[j % kPfStages], (j / kPfStages) & 1);
+    }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
@@ -231,44 +263,60 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         return smem_u32(sm + Sh::kKVOff + (j % kPfStages) * 2 * Sh::kKVBytes +
                         (v ? Sh::kKVBytes : 0));
       };
-      auto issue_s = [&](int g, int j) {  // S_g = Q_g . K_j^T over D in 16-wide steps
+      auto issue_s = [&](int g, int j) {  // S_g = Q_g . K_j^T into S buffer j & 1, 16-wide steps
         const uint32_t qb = smem_u32(sm + Sh::kQOff + g * Sh::kQBytes), kb = kv_base(j, false);
+        const uint32_t dst = tmem + 64 * (2 * g + (j & 1));
 #pragma unroll
         for (int k = 0; k < D / 16; ++k)
-          umma_f16(tmem + 64 * g, umma_desc_sw128(qb + (k >> 2) * kQRegion + (k & 3) * 32, 16, 1024),
+          umma_f16(dst, umma_desc_sw128(qb + (k >> 2) * kQRegion + (k & 3) * 32, 16, 1024),
                    umma_desc_sw128(kb + (k >> 2) * kKVRegion + (k & 3) * 32, 16, 1024), idesc_s,
                    k > 0);
-        umma_commit(&s_full[g]);
+        umma_commit(&s_full[2 * g + (j & 1)]);
       };
       auto issue_pv = [&](int g, int j) {  // O_g += P_g . V_j over 16-token steps
-        const uint32_t pb = smem_u32(sm + Sh::kPOff + g * kQRegion), vb = kv_base(j, true);
+        const uint32_t pb = smem_u32(sm + Sh::kPOff + (2 * g + (j & 1)) * kQRegion), vb = kv_base(j, true);
 #pragma unroll
         for (int k = 0; k < kPfTile / 16; ++k)
-          umma_f16(tmem + 128 + D * g, umma_desc_sw128(pb + k * 32, 16, 1024),
+          umma_f16(tmem + 256 + D * g, umma_desc_sw128(pb + k * 32, 16, 1024),
                    umma_desc_sw128(vb + k * 2048, kKVRegion, 1024), idesc_o, (j > 0 || k > 0));
-        umma_commit(&o_done[g]);
+        umma_commit(&o_done[2 * g + (j & 1)]);
       };
-      bool ok = mbar_wait_bounded(q_full, 0) && mbar_wait_bounded(&kv_full[0], 0);
-      if (ok) {
+      // S of the first two tiles of both groups up front (two S buffers per
+      // group); then per tile and group: once P_g(j) is written, P_g(j) . V_j,
+      // then S_g(j+2) into the buffer S_g(j) used
+      bool ok = mbar_wait_bounded(q_full, 0);
+      for (int j = 0; ok && j < 2 && j < ntiles; ++j) {
+        ok = mbar_wait_bounded(&k_full[j], 0);
+        if (!ok) break;
         tc_fence_after();
         for (int g = 0; g < kPfGroups; ++g)
-          if (tiles_of(g) > 0) issue_s(g, 0);
+          if (j < tiles_of(g)) issue_s(g, j);
+        umma_commit(&k_empty[j]);
       }
       for (int j = 0; ok && j < ntiles; ++j) {
+        bool v_ready = false;
         for (int g = 0; g < kPfGroups && ok; ++g) {
           if (j >= tiles_of(g)) continue;
-          ok = mbar_wait_bounded(&p_full[g], j & 1) && !*(volatile int *)abort_flag;
+          ok = mbar_wait_bounded(&p_full[2 * g + (j & 1)], (j >> 1) & 1) &&
+               !*(volatile int *)abort_flag;
           if (!ok) break;
+          if (!v_ready) {
+            ok = mbar_wait_bounded(&v_full[j % kPfStages], (j / kPfStages) & 1);
+            if (!ok) break;
+            v_ready = true;
+          }
           tc_fence_after();
-          if (j + 1 < tiles_of(g)) {  // S of the next tile into this group's S columns
-            ok = mbar_wait_bounded(&kv_full[(j + 1) % kPfStages], ((j + 1) / kPfStages) & 1);
+          issue_pv(g, j);
+          if (j + 2 < tiles_of(g)) {
+            ok = mbar_wait_bounded(&k_full[(j + 2) % kPfStages], ((j + 2) / kPfStages) & 1);
             if (!ok) break;
             tc_fence_after();
-            issue_s(g, j + 1);
+            issue_s(g, j + 2);
           }
-          issue_pv(g, j);
         }
-        if (ok) umma_commit(&kv_empty[j % kPfStages]);
+        if (!ok) break;
+        umma_commit(&v_empty[j % kPfStages]);
+        if (j + 2 < ntiles) umma_commit(&k_empty[(j + 2) % kPfStages]);
       }
       if (!ok) {
         raise_flag(a.err, PKV_FLAG_TIMEOUT);
@@ -285,7 +333,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     const int r = 32 * quarter + lane;                  // row in the tile = tensor-memory lane
     const int rr = g * kPfRows + r;                     // row in the CTA
     const uint32_t lane_off = (uint32_t)(32 * quarter) << 16;
-    const uint32_t tmem_s = tmem + 64 * g, tmem_o = tmem + 128 + D * g;
+    const uint32_t tmem_o = tmem + 256 + D * g;
     const bool real_row = rr < rows;
     const int p_row = p_first + (real_row ? rr : rows - 1);  // padding rows mirror the last row
     const size_t q_row = (size_t)(q0 + i0 + (real_row ? rr : 0)) * a.H + h;
@@ -304,27 +352,40 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       mbar_arrive(q_full);
     }
 
+    // scores are kept raw; with scale > 0 the max commutes with the scale
+    // and one fused multiply-add per pair gives s * scale * log2(e) - m
+    const float sl2 = a.scale_log2;
+    const bool pos_scale = sl2 > 0.f;
     float m_used = -INFINITY, l = 0.f;
     bool ok = true;
     for (int j = 0; j < my_tiles; ++j) {
-      ok = mbar_wait_bounded(&s_full[g], j & 1);
+      ok = mbar_wait_bounded(&s_full[2 * g + (j & 1)], (j >> 1) & 1);
       if (!__all_sync(0xffffffffu, ok) || *(volatile int *)abort_flag) {
         ok = false;
         break;
       }
       tc_fence_after();
       const int t0 = j * kPfTile;
-      float s[kPfTile];
-      tmem_ld32(tmem_s + lane_off, *reinterpret_cast<float(*)[32]>(s));
-      tmem_ld32(tmem_s + lane_off + 32, *reinterpret_cast<float(*)[32]>(s + 32));
-      // causal mask and row max of the scaled scores
-      const bool full = t0 + kPfTile - 1 <= p_row;      // no masked token in this tile
+      const uint32_t tmem_s = tmem + 64 * (2 * g + (j & 1));
+      const bool masked = t0 + kPfTile - 1 > p_row;   // the causal edge crosses this tile
+      // pass 1: row max (scores raw when scale > 0: the max commutes with it)
       float mx = -INFINITY;
 #pragma unroll
-      for (int i = 0; i < kPfTile; ++i) {
-        s[i] = (full || t0 + i <= p_row) ? s[i] * a.scale_log2 : -INFINITY;
-        mx = fmaxf(mx, s[i]);
+      for (int hlf = 0; hlf < 2; ++hlf) {
+        float s[32];
+        tmem_ld32(tmem_s + lane_off + 32 * hlf, s);
+        if (!pos_scale) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) s[i] *= sl2;
+        }
+        if (masked) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) s[i] = t0 + 32 * hlf + i <= p_row ? s[i] : -INFINITY;
+        }
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) mx = max3f(mx, s[i], s[i + 1]);
       }
+      if (pos_scale) mx *= sl2;
       // the reference max moves only when the row max exceeds it by 2^8
       const float m_new = (mx > m_used + 8.f) ? mx : m_used;
       const float alpha = fast_exp2(m_used - m_new);  // 0 on the first tile
@@ -332,26 +393,28 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       l *= alpha;
       m_used = m_new;
 
-      // P_{j-1} . V_{j-1} must be done: P's tile is rewritten and O is read
-      if (j > 0) {
-        ok = mbar_wait_bounded(&o_done[g], (j - 1) & 1);
+      if (rescale) {
+        // O must be final for tile j-1 before it is rescaled
+        ok = mbar_wait_bounded(&o_done[2 * g + ((j - 1) & 1)], ((j - 1) >> 1) & 1);
         if (!__all_sync(0xffffffffu, ok)) break;
         tc_fence_after();
-        if (rescale) {
 #pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
-            float v[32];
-            tmem_ld32(tmem_o + lane_off + 32 * c, v);
+        for (int c = 0; c < D / 32; ++c) {
+          float v[32];
+          tmem_ld32(tmem_o + lane_off + 32 * c, v);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] *= alpha;
-            tmem_st32(tmem_o + lane_off + 32 * c, v);
-          }
+          for (int i = 0; i < 32; ++i) v[i] *= alpha;
+          tmem_st32(tmem_o + lane_off + 32 * c, v);
         }
+      } else if (j >= 2) {
+        // this P buffer was last read by P . V of tile j-2
+        ok = mbar_wait_bounded(&o_done[2 * g + (j & 1)], ((j - 2) >> 1) & 1);
+        if (!__all_sync(0xffffffffu, ok)) break;
       }
       // the tile's V rows past the context are zeroed (they may hold
       // anything, and 0 * NaN would poison the product)
       if (t0 + kPfTile > n) {
-        ok = mbar_wait_bounded(&kv_full[j % kPfStages], (j / kPfStages) & 1);
+        ok = mbar_wait_bounded(&v_full[j % kPfStages], (j / kPfStages) & 1);
         if (!__all_sync(0xffffffffu, ok)) break;
         if (r < kPfTile && r >= n - t0) {
           uint8_t *vrow = sm + Sh::kKVOff + (j % kPfStages) * 2 * Sh::kKVBytes + Sh::kKVBytes + r * 128;
@@ -362,23 +425,48 @@ __global__ void __launch_bounds__(kPfThreads, 1)
               *reinterpret_cast<uint4 *>(vrow + rg * kKVRegion + c * 16) = make_uint4(0, 0, 0, 0);
         }
       }
-      // P = 2^(s - m) rounded to the input type into the group's swizzled
-      // K-major P tile (64 tokens = one 128-byte row); l sums the rounded weights
-      uint8_t *prow = sm + Sh::kPOff + g * kQRegion + r * 128;
+      // pass 2: P = 2^(s * scale * log2(e) - m), rounded to the input type,
+      // into the group's swizzled K-major P buffer (64 tokens = one 128-byte
+      // row); l sums the unrounded weights
+      const float mul = pos_scale ? sl2 : 1.f;
+      float2 lsum = make_float2(0.f, 0.f);
+      uint8_t *prow = sm + Sh::kPOff + (2 * g + (j & 1)) * kQRegion + r * 128;
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        uint32_t pk[4];
+      for (int hlf = 0; hlf < 2; ++hlf) {
+        float s[32];
+        tmem_ld32(tmem_s + lane_off + 32 * hlf, s);
+        if (!pos_scale) {
 #pragma unroll
-        for (int e = 0; e < 4; ++e)
-          pk[e] = PackPair<T>::run(fast_exp2(s[8 * c + 2 * e] - m_used),
-                                   fast_exp2(s[8 * c + 2 * e + 1] - m_used), l);
-        *reinterpret_cast<uint4 *>(prow + ((c ^ (r & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          for (int i = 0; i < 32; ++i) s[i] *= sl2;
+        }
+        if (masked) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) s[i] = t0 + 32 * hlf + i <= p_row ? s[i] : -INFINITY;
+        }
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t pk[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            float2 x = ffma2(make_float2(s[8 * c + 2 * e], s[8 * c + 2 * e + 1]),
+                             make_float2(mul, mul), make_float2(-m_used, -m_used));
+            x.x = fast_exp2(x.x);
+            x.y = fast_exp2(x.y);
+            lsum = fadd2(lsum, x);
+            pk[e] = PackPair<T>::pack(x.x, x.y);
+          }
+          const int chunk = 4 * hlf + c;
+          *reinterpret_cast<uint4 *>(prow + ((chunk ^ (r & 7)) << 4)) =
+              make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        }
       }
+      l += lsum.x + lsum.y;
       fence_proxy_async_shared();
       tc_fence_before();
-      mbar_arrive(&p_full[g]);
+      mbar_arrive(&p_full[2 * g + (j & 1)]);
     }
-    if (ok && my_tiles > 0) ok = mbar_wait_bounded(&o_done[g], (my_tiles - 1) & 1);
+    if (ok && my_tiles > 0)
+      ok = mbar_wait_bounded(&o_done[2 * g + ((my_tiles - 1) & 1)], ((my_tiles - 1) >> 1) & 1);
     if (my_tiles > 0 && __all_sync(0xffffffffu, ok) && !*(volatile int *)abort_flag) {
       tc_fence_after();
       const float inv_l = 1.f / l;
@@ -389,9 +477,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         tmem_ld32(tmem_o + lane_off + 32 * c, v);
         if (real_row) {
           uint32_t pk[16];
-          float unused = 0.f;
 #pragma unroll
-          for (int i = 0; i < 16; ++i) pk[i] = PackPair<T>::run(v[2 * i] * inv_l, v[2 * i + 1] * inv_l, unused);
+          for (int i = 0; i < 16; ++i) pk[i] = PackPair<T>::pack(v[2 * i] * inv_l, v[2 * i + 1] * inv_l);
           uint4 *dst = reinterpret_cast<uint4 *>(orow + 32 * c);
 #pragma unroll
           for (int c4 = 0; c4 < 4; ++c4)
