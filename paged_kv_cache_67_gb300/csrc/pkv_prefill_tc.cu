@@ -47,7 +47,7 @@ namespace pkv {
 constexpr int kPfRows = 128;     // query rows per softmax warpgroup (MMA M)
 constexpr int kPfGroups = 2;     // query tiles per CTA, one softmax warpgroup each
 constexpr int kPfTile = 64;      // KV tokens per tile
-constexpr int kPfStages = 3;     // K/V ring depth
+constexpr int kPfStages = 4;     // K/V ring depth
 constexpr int kPfWarps = 2 + 4 * kPfGroups;
 constexpr int kPfThreads = 32 * kPfWarps;
 constexpr int kQRegion = kPfRows * 128;   // 128 query rows x 64 elements of 16 bits
@@ -73,10 +73,11 @@ struct PfShape {
   static constexpr int kKVBytes = kRegions * kKVRegion;         // one K (or V) tile
   static constexpr int kQOff = 0;                               // [group]
   static constexpr int kKVOff = kQOff + kPfGroups * kQBytes;    // [stage][K, V]
-  static constexpr int kPOff = kKVOff + kPfStages * 2 * kKVBytes;  // [group][2] 128 x 64 tokens
-  static constexpr int kBarOff = kPOff + kPfGroups * 2 * kQRegion;
+  static constexpr int kBarOff = kKVOff + kPfStages * 2 * kKVBytes;
   static constexpr int kSmem = kBarOff + 256 + 1024;            // + alignment slack
-  static constexpr uint32_t kTmemCols = 512;  // S: 2 x 64, O: 2 x D (from column 128)
+  // tensor memory, 256 columns per group: S (64 fp32 columns), two P buffers
+  // (64 tokens as 32 packed columns each), O (D fp32 columns)
+  static constexpr uint32_t kTmemCols = 512;
 };
 
 // Tiled 4-D TMA load global -> shared with the default L2 policy (the K/V
@@ -142,15 +143,15 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   uint64_t *bars = reinterpret_cast<uint64_t *>(sm + Sh::kBarOff);
   uint64_t *q_full = bars + 0;
   uint64_t *k_full = bars + 1;     // [kPfStages]: K and V of a stage arrive and are
-  uint64_t *v_full = bars + 4;     // [kPfStages]  released separately, so the next
-  uint64_t *k_empty = bars + 7;    // [kPfStages]  keys are fetched as soon as the
-  uint64_t *v_empty = bars + 10;   // [kPfStages]  scores that read a slot are done
-  uint64_t *s_full = bars + 13;    // [kPfGroups][2]: S buffers of each group
-  uint64_t *p_full = bars + 17;    // [kPfGroups][2]: P buffers of each group
-  uint64_t *o_done = bars + 21;    // [kPfGroups][2]: P . V of an even / odd tile done
-  uint64_t *mma_done = bars + 25;
-  uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(bars + 26);
-  int *abort_flag = reinterpret_cast<int *>(bars + 27);
+  uint64_t *v_full = bars + 5;     // [kPfStages]  released separately, so the next
+  uint64_t *k_empty = bars + 9;    // [kPfStages]  keys are fetched as soon as the
+  uint64_t *v_empty = bars + 13;   // [kPfStages]  scores that read a slot are done
+  uint64_t *s_full = bars + 17;    // [kPfGroups]: S of the group's current tile
+  uint64_t *p_full = bars + 19;    // [kPfGroups][2]: P buffers of each group
+  uint64_t *o_done = bars + 23;    // [kPfGroups][2]: P . V of an even / odd tile done
+  uint64_t *mma_done = bars + 27;
+  uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(bars + 28);
+  int *abort_flag = reinterpret_cast<int *>(bars + 29);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int h = blockIdx.x, b = blockIdx.z;
@@ -186,8 +187,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       mbar_init(&v_empty[s], 1);
     }
     for (int g = 0; g < kPfGroups; ++g) {
-      mbar_init(&s_full[2 * g], 1);
-      mbar_init(&s_full[2 * g + 1], 1);
+      mbar_init(&s_full[g], 1);
       for (int k = 0; k < 2; ++k) {
         mbar_init(&p_full[2 * g + k], 128);
         mbar_init(&o_done[2 * g + k], 1);
@@ -263,38 +263,35 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         return smem_u32(sm + Sh::kKVOff + (j % kPfStages) * 2 * Sh::kKVBytes +
                         (v ? Sh::kKVBytes : 0));
       };
-      auto issue_s = [&](int g, int j) {  // S_g = Q_g . K_j^T into S buffer j & 1, 16-wide steps
+      auto issue_s = [&](int g, int j) {  // S_g = Q_g . K_j^T over D in 16-wide steps
         const uint32_t qb = smem_u32(sm + Sh::kQOff + g * Sh::kQBytes), kb = kv_base(j, false);
-        const uint32_t dst = tmem + 64 * (2 * g + (j & 1));
 #pragma unroll
         for (int k = 0; k < D / 16; ++k)
-          umma_f16(dst, umma_desc_sw128(qb + (k >> 2) * kQRegion + (k & 3) * 32, 16, 1024),
+          umma_f16(tmem + 256 * g, umma_desc_sw128(qb + (k >> 2) * kQRegion + (k & 3) * 32, 16, 1024),
                    umma_desc_sw128(kb + (k >> 2) * kKVRegion + (k & 3) * 32, 16, 1024), idesc_s,
                    k > 0);
-        umma_commit(&s_full[2 * g + (j & 1)]);
+        umma_commit(&s_full[g]);
       };
-      auto issue_pv = [&](int g, int j) {  // O_g += P_g . V_j over 16-token steps
-        const uint32_t pb = smem_u32(sm + Sh::kPOff + (2 * g + (j & 1)) * kQRegion), vb = kv_base(j, true);
+      auto issue_pv = [&](int g, int j) {  // O_g += P_g . V_j, P from tensor memory
+        const uint32_t pt = tmem + 256 * g + 64 + 32 * (j & 1), vb = kv_base(j, true);
 #pragma unroll
         for (int k = 0; k < kPfTile / 16; ++k)
-          umma_f16(tmem + 256 + D * g, umma_desc_sw128(pb + k * 32, 16, 1024),
-                   umma_desc_sw128(vb + k * 2048, kKVRegion, 1024), idesc_o, (j > 0 || k > 0));
+          umma_f16_tmem_a(tmem + 256 * g + 128, pt + 8 * k,
+                          umma_desc_sw128(vb + k * 2048, kKVRegion, 1024), idesc_o, (j > 0 || k > 0));
         umma_commit(&o_done[2 * g + (j & 1)]);
       };
-      // S of the first two tiles of both groups up front (two S buffers per
-      // group); then per tile and group: once P_g(j) is written, P_g(j) . V_j,
-      // then S_g(j+2) into the buffer S_g(j) used
-      bool ok = mbar_wait_bounded(q_full, 0);
-      for (int j = 0; ok && j < 2 && j < ntiles; ++j) {
-        ok = mbar_wait_bounded(&k_full[j], 0);
-        if (!ok) break;
+      // S of the first tile of both groups; then per tile and group: once
+      // P_g(j) is in tensor memory (and S_g(j) read), P_g(j) . V_j, then
+      // S_g(j+1) into the group's S columns
+      bool ok = mbar_wait_bounded(q_full, 0) && mbar_wait_bounded(&k_full[0], 0);
+      if (ok) {
         tc_fence_after();
         for (int g = 0; g < kPfGroups; ++g)
-          if (j < tiles_of(g)) issue_s(g, j);
-        umma_commit(&k_empty[j]);
+          if (tiles_of(g) > 0) issue_s(g, 0);
+        umma_commit(&k_empty[0]);
       }
       for (int j = 0; ok && j < ntiles; ++j) {
-        bool v_ready = false;
+        bool v_ready = false, k_ready = false;
         for (int g = 0; g < kPfGroups && ok; ++g) {
           if (j >= tiles_of(g)) continue;
           ok = mbar_wait_bounded(&p_full[2 * g + (j & 1)], (j >> 1) & 1) &&
@@ -307,16 +304,19 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           }
           tc_fence_after();
           issue_pv(g, j);
-          if (j + 2 < tiles_of(g)) {
-            ok = mbar_wait_bounded(&k_full[(j + 2) % kPfStages], ((j + 2) / kPfStages) & 1);
-            if (!ok) break;
-            tc_fence_after();
-            issue_s(g, j + 2);
+          if (j + 1 < tiles_of(g)) {
+            if (!k_ready) {
+              ok = mbar_wait_bounded(&k_full[(j + 1) % kPfStages], ((j + 1) / kPfStages) & 1);
+              if (!ok) break;
+              k_ready = true;
+              tc_fence_after();
+            }
+            issue_s(g, j + 1);
           }
         }
         if (!ok) break;
         umma_commit(&v_empty[j % kPfStages]);
-        if (j + 2 < ntiles) umma_commit(&k_empty[(j + 2) % kPfStages]);
+        if (j + 1 < ntiles) umma_commit(&k_empty[(j + 1) % kPfStages]);
       }
       if (!ok) {
         raise_flag(a.err, PKV_FLAG_TIMEOUT);
@@ -333,7 +333,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     const int r = 32 * quarter + lane;                  // row in the tile = tensor-memory lane
     const int rr = g * kPfRows + r;                     // row in the CTA
     const uint32_t lane_off = (uint32_t)(32 * quarter) << 16;
-    const uint32_t tmem_o = tmem + 256 + D * g;
+    const uint32_t tmem_o = tmem + 256 * g + 128;
     const bool real_row = rr < rows;
     const int p_row = p_first + (real_row ? rr : rows - 1);  // padding rows mirror the last row
     const size_t q_row = (size_t)(q0 + i0 + (real_row ? rr : 0)) * a.H + h;
@@ -359,32 +359,29 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     float m_used = -INFINITY, l = 0.f;
     bool ok = true;
     for (int j = 0; j < my_tiles; ++j) {
-      ok = mbar_wait_bounded(&s_full[2 * g + (j & 1)], (j >> 1) & 1);
+      ok = mbar_wait_bounded(&s_full[g], j & 1);
       if (!__all_sync(0xffffffffu, ok) || *(volatile int *)abort_flag) {
         ok = false;
         break;
       }
       tc_fence_after();
       const int t0 = j * kPfTile;
-      const uint32_t tmem_s = tmem + 64 * (2 * g + (j & 1));
+      const uint32_t tmem_s = tmem + 256 * g;
       const bool masked = t0 + kPfTile - 1 > p_row;   // the causal edge crosses this tile
-      // pass 1: row max (scores raw when scale > 0: the max commutes with it)
+      // the row's 64 scores in one load; raw when scale > 0 (the max commutes)
+      float s[kPfTile];
+      tmem_ld64(tmem_s + lane_off, s);
+      if (!pos_scale) {
+#pragma unroll
+        for (int i = 0; i < kPfTile; ++i) s[i] *= sl2;
+      }
+      if (masked) {
+#pragma unroll
+        for (int i = 0; i < kPfTile; ++i) s[i] = t0 + i <= p_row ? s[i] : -INFINITY;
+      }
       float mx = -INFINITY;
 #pragma unroll
-      for (int hlf = 0; hlf < 2; ++hlf) {
-        float s[32];
-        tmem_ld32(tmem_s + lane_off + 32 * hlf, s);
-        if (!pos_scale) {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) s[i] *= sl2;
-        }
-        if (masked) {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) s[i] = t0 + 32 * hlf + i <= p_row ? s[i] : -INFINITY;
-        }
-#pragma unroll
-        for (int i = 0; i < 32; i += 2) mx = max3f(mx, s[i], s[i + 1]);
-      }
+      for (int i = 0; i < kPfTile; i += 2) mx = max3f(mx, s[i], s[i + 1]);
       if (pos_scale) mx *= sl2;
       // the reference max moves only when the row max exceeds it by 2^8
       const float m_new = (mx > m_used + 8.f) ? mx : m_used;
@@ -425,43 +422,25 @@ __global__ void __launch_bounds__(kPfThreads, 1)
               *reinterpret_cast<uint4 *>(vrow + rg * kKVRegion + c * 16) = make_uint4(0, 0, 0, 0);
         }
       }
-      // pass 2: P = 2^(s * scale * log2(e) - m), rounded to the input type,
-      // into the group's swizzled K-major P buffer (64 tokens = one 128-byte
-      // row); l sums the unrounded weights
+      // P = 2^(s * scale * log2(e) - m), rounded to the input type, into
+      // this tile's P buffer in tensor memory (two tokens per column); l
+      // sums the unrounded weights
       const float mul = pos_scale ? sl2 : 1.f;
       float2 lsum = make_float2(0.f, 0.f);
-      uint8_t *prow = sm + Sh::kPOff + (2 * g + (j & 1)) * kQRegion + r * 128;
+      uint32_t pk[32];
 #pragma unroll
-      for (int hlf = 0; hlf < 2; ++hlf) {
-        float s[32];
-        tmem_ld32(tmem_s + lane_off + 32 * hlf, s);
-        if (!pos_scale) {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) s[i] *= sl2;
-        }
-        if (masked) {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) s[i] = t0 + 32 * hlf + i <= p_row ? s[i] : -INFINITY;
-        }
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t pk[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            float2 x = ffma2(make_float2(s[8 * c + 2 * e], s[8 * c + 2 * e + 1]),
-                             make_float2(mul, mul), make_float2(-m_used, -m_used));
-            x.x = fast_exp2(x.x);
-            x.y = fast_exp2(x.y);
-            lsum = fadd2(lsum, x);
-            pk[e] = PackPair<T>::pack(x.x, x.y);
-          }
-          const int chunk = 4 * hlf + c;
-          *reinterpret_cast<uint4 *>(prow + ((chunk ^ (r & 7)) << 4)) =
-              make_uint4(pk[0], pk[1], pk[2], pk[3]);
-        }
+      for (int i = 0; i < 32; ++i) {
+        float2 x = ffma2(make_float2(s[2 * i], s[2 * i + 1]), make_float2(mul, mul),
+                         make_float2(-m_used, -m_used));
+        x.x = fast_exp2(x.x);
+        x.y = fast_exp2(x.y);
+        lsum = fadd2(lsum, x);
+        pk[i] = PackPair<T>::pack(x.x, x.y);
       }
+      tmem_st32u(tmem + 256 * g + 64 + 32 * (j & 1) + lane_off, pk);
       l += lsum.x + lsum.y;
-      fence_proxy_async_shared();
+      // the zeroed V rows (generic writes) before the product reads them
+      if (t0 + kPfTile > n) fence_proxy_async_shared();
       tc_fence_before();
       mbar_arrive(&p_full[2 * g + (j & 1)]);
     }
