@@ -46,12 +46,12 @@ namespace pkv {
 
 constexpr int kPfRows = 128;     // query rows per softmax warpgroup (MMA M)
 constexpr int kPfGroups = 2;     // query tiles per CTA, one softmax warpgroup each
-constexpr int kPfTile = 64;      // KV tokens per tile
-constexpr int kPfStages = 4;     // K/V ring depth
+constexpr int kPfTile = 128;     // KV tokens per tile
+constexpr int kPfStages = 2;     // K/V ring depth
 constexpr int kPfWarps = 2 + 4 * kPfGroups;
 constexpr int kPfThreads = 32 * kPfWarps;
 constexpr int kQRegion = kPfRows * 128;   // 128 query rows x 64 elements of 16 bits
-constexpr int kKVRegion = kPfTile * 128;  // 64 token rows x 64 elements
+constexpr int kKVRegion = kPfTile * 128;  // 128 token rows x 64 elements
 
 struct PrefillArgs {
   void *out;
@@ -75,8 +75,9 @@ struct PfShape {
   static constexpr int kKVOff = kQOff + kPfGroups * kQBytes;    // [stage][K, V]
   static constexpr int kBarOff = kKVOff + kPfStages * 2 * kKVBytes;
   static constexpr int kSmem = kBarOff + 256 + 1024;            // + alignment slack
-  // tensor memory, 256 columns per group: S (64 fp32 columns), two P buffers
-  // (64 tokens as 32 packed columns each), O (D fp32 columns)
+  // tensor memory, 256 columns per group: S (128 fp32 columns; P, 128
+  // tokens as 64 packed columns, is written over its first half once S is
+  // read), O (D fp32 columns)
   static constexpr uint32_t kTmemCols = 512;
 };
 
@@ -143,15 +144,15 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   uint64_t *bars = reinterpret_cast<uint64_t *>(sm + Sh::kBarOff);
   uint64_t *q_full = bars + 0;
   uint64_t *k_full = bars + 1;     // [kPfStages]: K and V of a stage arrive and are
-  uint64_t *v_full = bars + 5;     // [kPfStages]  released separately, so the next
-  uint64_t *k_empty = bars + 9;    // [kPfStages]  keys are fetched as soon as the
-  uint64_t *v_empty = bars + 13;   // [kPfStages]  scores that read a slot are done
-  uint64_t *s_full = bars + 17;    // [kPfGroups]: S of the group's current tile
-  uint64_t *p_full = bars + 19;    // [kPfGroups][2]: P buffers of each group
-  uint64_t *o_done = bars + 23;    // [kPfGroups][2]: P . V of an even / odd tile done
-  uint64_t *mma_done = bars + 27;
-  uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(bars + 28);
-  int *abort_flag = reinterpret_cast<int *>(bars + 29);
+  uint64_t *v_full = bars + 3;     // [kPfStages]  released separately, so the next
+  uint64_t *k_empty = bars + 5;    // [kPfStages]  keys are fetched as soon as the
+  uint64_t *v_empty = bars + 7;    // [kPfStages]  scores that read a slot are done
+  uint64_t *s_full = bars + 9;     // [kPfGroups]: S of the group's current tile
+  uint64_t *p_full = bars + 11;    // [kPfGroups]: P of the group's current tile
+  uint64_t *o_done = bars + 13;    // [kPfGroups]: P . V of the group's current tile done
+  uint64_t *mma_done = bars + 15;
+  uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(bars + 16);
+  int *abort_flag = reinterpret_cast<int *>(bars + 17);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int h = blockIdx.x, b = blockIdx.z;
@@ -188,10 +189,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     }
     for (int g = 0; g < kPfGroups; ++g) {
       mbar_init(&s_full[g], 1);
-      for (int k = 0; k < 2; ++k) {
-        mbar_init(&p_full[2 * g + k], 128);
-        mbar_init(&o_done[2 * g + k], 1);
-      }
+      mbar_init(&p_full[g], 128);
+      mbar_init(&o_done[g], 1);
     }
     mbar_init(mma_done, 1);
     *abort_flag = 0;
@@ -206,17 +205,16 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    // per tile: the K boxes (lanes 0 .. per_tensor-1) once the keys of tile
-    // j-3 are no longer read, then the V boxes (the next lanes) once the
-    // values of tile j-3 are no longer read
-    const int per_tensor = 4 * Sh::kRegions;     // boxes of K (or V) per 64-token tile
-    const int region = (lane % per_tensor) >> 2, chunk = lane & 3;
+    // per tile: the K boxes (one per lane) once the keys of tile j-2 are no
+    // longer read, then the V boxes once the values of tile j-2 are not
+    const int per_tensor = 8 * Sh::kRegions;     // boxes of K (or V) per 128-token tile
+    const int region = (lane % per_tensor) >> 3, chunk = lane & 7;
     int issued = 0;
     bool ok = true;
     for (int j = 0; j < ntiles && ok; ++j) {
       const int stage = j % kPfStages;
       const int tok0 = j * kPfTile;
-      const int valid_chunks = min(4, (n - tok0 + 15) >> 4);
+      const int valid_chunks = min(8, (n - tok0 + 15) >> 4);
       const uint32_t bytes = (uint32_t)(valid_chunks * Sh::kRegions * 2048);
       for (int v = 0; v < 2 && ok; ++v) {
         if (j >= kPfStages) {
@@ -234,7 +232,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         uint64_t *full = v ? &v_full[stage] : &k_full[stage];
         if (lane == 0) mbar_arrive_expect_tx(full, bytes);
         __syncwarp();
-        if (lane >= v * per_tensor && lane < (v + 1) * per_tensor && chunk < valid_chunks) {
+        if (lane < per_tensor && chunk < valid_chunks) {
           const int t = tok0 + 16 * chunk;
           const int lb = t / a.bs;
           int phys = __ldg(a.tables + (size_t)b * a.max_blocks + lb);
@@ -273,16 +271,17 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         umma_commit(&s_full[g]);
       };
       auto issue_pv = [&](int g, int j) {  // O_g += P_g . V_j, P from tensor memory
-        const uint32_t pt = tmem + 256 * g + 64 + 32 * (j & 1), vb = kv_base(j, true);
+        const uint32_t vb = kv_base(j, true);
 #pragma unroll
         for (int k = 0; k < kPfTile / 16; ++k)
-          umma_f16_tmem_a(tmem + 256 * g + 128, pt + 8 * k,
+          umma_f16_tmem_a(tmem + 256 * g + 128, tmem + 256 * g + 8 * k,
                           umma_desc_sw128(vb + k * 2048, kKVRegion, 1024), idesc_o, (j > 0 || k > 0));
-        umma_commit(&o_done[2 * g + (j & 1)]);
+        umma_commit(&o_done[g]);
       };
-      // S of the first tile of both groups; then per tile and group: once
-      // P_g(j) is in tensor memory (and S_g(j) read), P_g(j) . V_j, then
-      // S_g(j+1) into the group's S columns
+      // S of the first tile of both groups; then per tile: P_g(j) . V_j for
+      // both groups as their P arrive, then -- once a group's product has
+      // read P, which lies over its S columns -- S_g(j+1).  The wait for a
+      // group's product overlaps the other group's product on the tensor core.
       bool ok = mbar_wait_bounded(q_full, 0) && mbar_wait_bounded(&k_full[0], 0);
       if (ok) {
         tc_fence_after();
@@ -291,11 +290,10 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         umma_commit(&k_empty[0]);
       }
       for (int j = 0; ok && j < ntiles; ++j) {
-        bool v_ready = false, k_ready = false;
+        bool v_ready = false;
         for (int g = 0; g < kPfGroups && ok; ++g) {
           if (j >= tiles_of(g)) continue;
-          ok = mbar_wait_bounded(&p_full[2 * g + (j & 1)], (j >> 1) & 1) &&
-               !*(volatile int *)abort_flag;
+          ok = mbar_wait_bounded(&p_full[g], j & 1) && !*(volatile int *)abort_flag;
           if (!ok) break;
           if (!v_ready) {
             ok = mbar_wait_bounded(&v_full[j % kPfStages], (j / kPfStages) & 1);
@@ -304,18 +302,23 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           }
           tc_fence_after();
           issue_pv(g, j);
-          if (j + 1 < tiles_of(g)) {
-            if (!k_ready) {
-              ok = mbar_wait_bounded(&k_full[(j + 1) % kPfStages], ((j + 1) / kPfStages) & 1);
-              if (!ok) break;
-              k_ready = true;
-              tc_fence_after();
-            }
-            issue_s(g, j + 1);
-          }
         }
         if (!ok) break;
         umma_commit(&v_empty[j % kPfStages]);
+        bool k_ready = false;
+        for (int g = 0; g < kPfGroups && ok; ++g) {
+          if (j + 1 >= tiles_of(g)) continue;
+          ok = mbar_wait_bounded(&o_done[g], j & 1);   // P_g(j) has been read
+          if (!ok) break;
+          if (!k_ready) {
+            ok = mbar_wait_bounded(&k_full[(j + 1) % kPfStages], ((j + 1) / kPfStages) & 1);
+            if (!ok) break;
+            k_ready = true;
+          }
+          tc_fence_after();
+          issue_s(g, j + 1);
+        }
+        if (!ok) break;
         if (j + 1 < ntiles) umma_commit(&k_empty[(j + 1) % kPfStages]);
       }
       if (!ok) {
@@ -366,22 +369,25 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       }
       tc_fence_after();
       const int t0 = j * kPfTile;
-      const uint32_t tmem_s = tmem + 256 * g;
-      const bool masked = t0 + kPfTile - 1 > p_row;   // the causal edge crosses this tile
-      // the row's 64 scores in one load; raw when scale > 0 (the max commutes)
-      float s[kPfTile];
-      tmem_ld64(tmem_s + lane_off, s);
-      if (!pos_scale) {
-#pragma unroll
-        for (int i = 0; i < kPfTile; ++i) s[i] *= sl2;
-      }
-      if (masked) {
-#pragma unroll
-        for (int i = 0; i < kPfTile; ++i) s[i] = t0 + i <= p_row ? s[i] : -INFINITY;
-      }
+      const uint32_t tmem_sp = tmem + 256 * g + lane_off;  // S, then P over its first half
+      // pass 1: row max (scores raw when scale > 0: the max commutes)
       float mx = -INFINITY;
 #pragma unroll
-      for (int i = 0; i < kPfTile; i += 2) mx = max3f(mx, s[i], s[i + 1]);
+      for (int hf = 0; hf < 2; ++hf) {
+        const int tb = t0 + 64 * hf;
+        float s[64];
+        tmem_ld64(tmem_sp + 64 * hf, s);
+        if (!pos_scale) {
+#pragma unroll
+          for (int i = 0; i < 64; ++i) s[i] *= sl2;
+        }
+        if (tb + 63 > p_row) {
+#pragma unroll
+          for (int i = 0; i < 64; ++i) s[i] = tb + i <= p_row ? s[i] : -INFINITY;
+        }
+#pragma unroll
+        for (int i = 0; i < 64; i += 2) mx = max3f(mx, s[i], s[i + 1]);
+      }
       if (pos_scale) mx *= sl2;
       // the reference max moves only when the row max exceeds it by 2^8
       const float m_new = (mx > m_used + 8.f) ? mx : m_used;
@@ -389,12 +395,9 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       const bool rescale = __any_sync(0xffffffffu, m_new != m_used) && j > 0;
       l *= alpha;
       m_used = m_new;
-
+      // O is final for tile j-1 here: S_g(j) was issued after P_g(j-1) . V
+      // had completed
       if (rescale) {
-        // O must be final for tile j-1 before it is rescaled
-        ok = mbar_wait_bounded(&o_done[2 * g + ((j - 1) & 1)], ((j - 1) >> 1) & 1);
-        if (!__all_sync(0xffffffffu, ok)) break;
-        tc_fence_after();
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           float v[32];
@@ -403,17 +406,14 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           for (int i = 0; i < 32; ++i) v[i] *= alpha;
           tmem_st32(tmem_o + lane_off + 32 * c, v);
         }
-      } else if (j >= 2) {
-        // this P buffer was last read by P . V of tile j-2
-        ok = mbar_wait_bounded(&o_done[2 * g + (j & 1)], ((j - 2) >> 1) & 1);
-        if (!__all_sync(0xffffffffu, ok)) break;
       }
       // the tile's V rows past the context are zeroed (they may hold
       // anything, and 0 * NaN would poison the product)
-      if (t0 + kPfTile > n) {
+      const bool past_end = t0 + kPfTile > n;
+      if (past_end) {
         ok = mbar_wait_bounded(&v_full[j % kPfStages], (j / kPfStages) & 1);
         if (!__all_sync(0xffffffffu, ok)) break;
-        if (r < kPfTile && r >= n - t0) {
+        if (r >= n - t0) {
           uint8_t *vrow = sm + Sh::kKVOff + (j % kPfStages) * 2 * Sh::kKVBytes + Sh::kKVBytes + r * 128;
 #pragma unroll
           for (int rg = 0; rg < Sh::kRegions; ++rg)
@@ -422,30 +422,44 @@ __global__ void __launch_bounds__(kPfThreads, 1)
               *reinterpret_cast<uint4 *>(vrow + rg * kKVRegion + c * 16) = make_uint4(0, 0, 0, 0);
         }
       }
-      // P = 2^(s * scale * log2(e) - m), rounded to the input type, into
-      // this tile's P buffer in tensor memory (two tokens per column); l
-      // sums the unrounded weights
+      // pass 2: P = 2^(s * scale * log2(e) - m), rounded to the input type,
+      // two tokens per column over S columns already read (P columns
+      // 16 q4 .. +15 lie below S columns 32 q4 read in this or an earlier
+      // step); l sums the unrounded weights
       const float mul = pos_scale ? sl2 : 1.f;
       float2 lsum = make_float2(0.f, 0.f);
-      uint32_t pk[32];
+#pragma unroll 1
+      for (int q4 = 0; q4 < 4; ++q4) {   // 32 tokens at a time: P columns 16 q4 .. +15
+        const int tb = t0 + 32 * q4;
+        float s[32];
+        tmem_ld32(tmem_sp + 32 * q4, s);
+        if (!pos_scale) {
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        float2 x = ffma2(make_float2(s[2 * i], s[2 * i + 1]), make_float2(mul, mul),
-                         make_float2(-m_used, -m_used));
-        x.x = fast_exp2(x.x);
-        x.y = fast_exp2(x.y);
-        lsum = fadd2(lsum, x);
-        pk[i] = PackPair<T>::pack(x.x, x.y);
+          for (int i = 0; i < 32; ++i) s[i] *= sl2;
+        }
+        if (tb + 31 > p_row) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) s[i] = tb + i <= p_row ? s[i] : -INFINITY;
+        }
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          float2 x = ffma2(make_float2(s[2 * i], s[2 * i + 1]), make_float2(mul, mul),
+                           make_float2(-m_used, -m_used));
+          x.x = fast_exp2(x.x);
+          x.y = fast_exp2(x.y);
+          lsum = fadd2(lsum, x);
+          pk[i] = PackPair<T>::pack(x.x, x.y);
+        }
+        tmem_st16u(tmem_sp + 16 * q4, pk);
       }
-      tmem_st32u(tmem + 256 * g + 64 + 32 * (j & 1) + lane_off, pk);
       l += lsum.x + lsum.y;
       // the zeroed V rows (generic writes) before the product reads them
-      if (t0 + kPfTile > n) fence_proxy_async_shared();
+      if (past_end) fence_proxy_async_shared();
       tc_fence_before();
-      mbar_arrive(&p_full[2 * g + (j & 1)]);
+      mbar_arrive(&p_full[g]);
     }
-    if (ok && my_tiles > 0)
-      ok = mbar_wait_bounded(&o_done[2 * g + ((my_tiles - 1) & 1)], ((my_tiles - 1) >> 1) & 1);
+    if (ok && my_tiles > 0) ok = mbar_wait_bounded(&o_done[g], (my_tiles - 1) & 1);
     if (my_tiles > 0 && __all_sync(0xffffffffu, ok) && !*(volatile int *)abort_flag) {
       tc_fence_after();
       const float inv_l = 1.f / l;
