@@ -278,10 +278,10 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                           umma_desc_sw128(vb + k * 2048, kKVRegion, 1024), idesc_o, (j > 0 || k > 0));
         umma_commit(&o_done[g]);
       };
-      // S of the first tile of both groups; then per tile: P_g(j) . V_j for
-      // both groups as their P arrive, then -- once a group's product has
-      // read P, which lies over its S columns -- S_g(j+1).  The wait for a
-      // group's product overlaps the other group's product on the tensor core.
+      // S of the first tile of both groups; then per tile and group: P_g(j) . V_j
+      // as soon as P_g(j) arrives, then -- once that product has read P, which
+      // lies over the group's S columns -- S_g(j+1).  While one group's
+      // softmax runs, the tensor core serves the other group.
       bool ok = mbar_wait_bounded(q_full, 0) && mbar_wait_bounded(&k_full[0], 0);
       if (ok) {
         tc_fence_after();
@@ -290,7 +290,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         umma_commit(&k_empty[0]);
       }
       for (int j = 0; ok && j < ntiles; ++j) {
-        bool v_ready = false;
+        bool v_ready = false, k_ready = false;
         for (int g = 0; g < kPfGroups && ok; ++g) {
           if (j >= tiles_of(g)) continue;
           ok = mbar_wait_bounded(&p_full[g], j & 1) && !*(volatile int *)abort_flag;
@@ -302,23 +302,22 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           }
           tc_fence_after();
           issue_pv(g, j);
+          if (j + 1 < tiles_of(g)) {
+            // the next S goes over P_g(j): wait until the product has read it
+            // (the other group's product or scores keep the tensor core busy)
+            ok = mbar_wait_bounded(&o_done[g], j & 1);
+            if (!ok) break;
+            if (!k_ready) {
+              ok = mbar_wait_bounded(&k_full[(j + 1) % kPfStages], ((j + 1) / kPfStages) & 1);
+              if (!ok) break;
+              k_ready = true;
+            }
+            tc_fence_after();
+            issue_s(g, j + 1);
+          }
         }
         if (!ok) break;
         umma_commit(&v_empty[j % kPfStages]);
-        bool k_ready = false;
-        for (int g = 0; g < kPfGroups && ok; ++g) {
-          if (j + 1 >= tiles_of(g)) continue;
-          ok = mbar_wait_bounded(&o_done[g], j & 1);   // P_g(j) has been read
-          if (!ok) break;
-          if (!k_ready) {
-            ok = mbar_wait_bounded(&k_full[(j + 1) % kPfStages], ((j + 1) / kPfStages) & 1);
-            if (!ok) break;
-            k_ready = true;
-          }
-          tc_fence_after();
-          issue_s(g, j + 1);
-        }
-        if (!ok) break;
         if (j + 1 < ntiles) umma_commit(&k_empty[(j + 1) % kPfStages]);
       }
       if (!ok) {
@@ -424,26 +423,26 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       }
       // pass 2: P = 2^(s * scale * log2(e) - m), rounded to the input type,
       // two tokens per column over S columns already read (P columns
-      // 16 q4 .. +15 lie below S columns 32 q4 read in this or an earlier
+      // 32 hf .. +31 lie below S columns 64 hf read in this or the earlier
       // step); l sums the unrounded weights
       const float mul = pos_scale ? sl2 : 1.f;
       float2 lsum = make_float2(0.f, 0.f);
 #pragma unroll 1
-      for (int q4 = 0; q4 < 4; ++q4) {   // 32 tokens at a time: P columns 16 q4 .. +15
-        const int tb = t0 + 32 * q4;
-        float s[32];
-        tmem_ld32(tmem_sp + 32 * q4, s);
+      for (int hf = 0; hf < 2; ++hf) {   // 64 tokens at a time: P columns 32 hf .. +31
+        const int tb = t0 + 64 * hf;
+        float s[64];
+        tmem_ld64(tmem_sp + 64 * hf, s);
         if (!pos_scale) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) s[i] *= sl2;
+          for (int i = 0; i < 64; ++i) s[i] *= sl2;
         }
-        if (tb + 31 > p_row) {
+        if (tb + 63 > p_row) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) s[i] = tb + i <= p_row ? s[i] : -INFINITY;
+          for (int i = 0; i < 64; ++i) s[i] = tb + i <= p_row ? s[i] : -INFINITY;
         }
-        uint32_t pk[16];
+        uint32_t pk[32];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
+        for (int i = 0; i < 32; ++i) {
           float2 x = ffma2(make_float2(s[2 * i], s[2 * i + 1]), make_float2(mul, mul),
                            make_float2(-m_used, -m_used));
           x.x = fast_exp2(x.x);
@@ -451,7 +450,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           lsum = fadd2(lsum, x);
           pk[i] = PackPair<T>::pack(x.x, x.y);
         }
-        tmem_st16u(tmem_sp + 16 * q4, pk);
+        tmem_st32u(tmem_sp + 32 * hf, pk);
       }
       l += lsum.x + lsum.y;
       // the zeroed V rows (generic writes) before the product reads them
