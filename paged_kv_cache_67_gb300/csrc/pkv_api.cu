@@ -2,6 +2,8 @@
 // checks, the decode plan (kernel choice, partition size, workspace
 // layout) and the launches.  Nothing here allocates device memory.
 #include <math.h>
+
+#include <algorithm>
 #include <string.h>
 
 #include "pkv_device.cuh"
@@ -339,10 +341,12 @@ PKV_API pkv_status pkv_prefill_attention(void *out, const void *q, const void *k
     return PKV_ERR_INVALID_ARG;
   const long long mq = max_q_len > 0 ? max_q_len : total_q;
   const long long q_tiles = (mq + 255) / 256;  // 256 queries (two 128-row tiles) per CTA
-  if (q_tiles > 65535) return PKV_ERR_UNSUPPORTED;
+  // CTAs per head: at least the (sequence, tile) pairs, sum ceil(qlen / 256) <= total_q / 256 + B
+  const long long ctas = std::min<long long>((total_q + 255) / 256 + B, (long long)B * q_tiles);
+  if (q_tiles > 65535 || ctas > 65535) return PKV_ERR_UNSUPPORTED;
   return launch_prefill_tc(out, q, k_cache, v_cache, block_tables, cu_seqlens_q, context_lens, B,
                            H, num_kv_heads, head_dim, block_size, max_blocks, num_blocks, scale, dt,
-                           (int)q_tiles, err_flags, reinterpret_cast<cudaStream_t>(stream));
+                           (int)q_tiles, (int)ctas, err_flags, reinterpret_cast<cudaStream_t>(stream));
 }
 
 PKV_API const char *pkv_status_string(pkv_status status) {

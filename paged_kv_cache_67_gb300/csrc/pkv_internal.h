@@ -69,7 +69,7 @@ pkv_status launch_prefill_tc(void *out, const void *q, const void *k_cache, cons
                              const int32_t *tables, const int32_t *cu_q, const int32_t *lens,
                              int B, int H, int KVH, int D, int bs, int max_blocks,
                              long long num_blocks, float scale, pkv_dtype dt, int q_tiles,
-                             int *err, cudaStream_t stream);
+                             int ctas_per_head, int *err, cudaStream_t stream);
 
 struct DecodeArgs;
 pkv_status launch_decode_simt(const DecodeArgs &a, const DecodePlan &plan, pkv_dtype dt,

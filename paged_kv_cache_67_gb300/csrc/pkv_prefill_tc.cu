@@ -62,7 +62,7 @@ struct PrefillArgs {
   int *err;
   long long num_blocks;
   int B, H, KVH, D, G, bs, max_blocks;
-  int q_tiles;        // 256-query tiles per sequence the grid covers (gridDim.y)
+  int q_tiles;        // 256-query tiles per sequence served (from the host's bound on qlen)
   float scale_log2;   // scale * log2(e)
 };
 
@@ -155,21 +155,69 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   int *abort_flag = reinterpret_cast<int *>(bars + 17);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int h = blockIdx.x, b = blockIdx.z;
-  const int qt = a.q_tiles - 1 - (int)blockIdx.y;  // latest (heaviest) tiles first
+  const int h = blockIdx.x;
+  constexpr int kCtaRows = kPfGroups * kPfRows;
 
-  // ---- the sequence and this CTA's query rows (uniform: before any barrier)
+  // ---- checks of the whole batch, by one warp of one CTA
+  auto seq_ok = [&](int bb, int ql) {
+    const int nn = __ldg(a.lens + bb);
+    return ql >= 0 && nn >= ql && (long long)nn <= (long long)a.max_blocks * a.bs;
+  };
+  if (h == 0 && blockIdx.y == 0 && warp == 0) {
+    int bad = 0, over = 0;
+    for (int bb = lane; bb < a.B; bb += 32) {
+      const int ql = __ldg(a.cu_q + bb + 1) - __ldg(a.cu_q + bb);
+      bad |= !seq_ok(bb, ql);
+      over |= ql > a.q_tiles * kCtaRows;
+    }
+    if (__any_sync(0xffffffffu, bad) && lane == 0) raise_flag(a.err, PKV_FLAG_QUERY_LEN);
+    if (__any_sync(0xffffffffu, over) && lane == 0) raise_flag(a.err, PKV_FLAG_QUERY_OVER_HINT);
+  }
+
+  // ---- which (sequence, 256-query tile) this CTA serves: the k-th of the
+  // real pairs in the order (tile index descending, then sequence), so the
+  // latest (heaviest) tiles start first and no CTA is launched for nothing.
+  // Every warp finds it on its own (uniform, before any barrier).
+  int b = -1, qt = 0;
+  {
+    int k = blockIdx.y;
+    if (a.B <= 32) {  // one sequence per lane: the query counts stay in registers
+      const int ql = lane < a.B ? __ldg(a.cu_q + lane + 1) - __ldg(a.cu_q + lane) : 0;
+      for (int t = a.q_tiles - 1; t >= 0; --t) {
+        const unsigned m = __ballot_sync(0xffffffffu, ql > t * kCtaRows);
+        const int c = __popc(m);
+        if (k < c) {
+          b = (int)__fns(m, 0, k + 1);  // position of the k-th set bit
+          qt = t;
+          break;
+        }
+        k -= c;
+      }
+    } else {
+      for (int t = a.q_tiles - 1; t >= 0 && b < 0; --t) {
+        int cnt = 0;
+        for (int base = 0; base < a.B; base += 32) {
+          const int bb = base + lane;
+          const bool has = bb < a.B && __ldg(a.cu_q + bb + 1) - __ldg(a.cu_q + bb) > t * kCtaRows;
+          const unsigned m = __ballot_sync(0xffffffffu, has);
+          const int c = __popc(m);
+          if (k < cnt + c) {
+            b = base + (int)__fns(m, 0, k - cnt + 1);
+            qt = t;
+            break;
+          }
+          cnt += c;
+        }
+        if (b < 0) k -= cnt;
+      }
+    }
+  }
+  if (b < 0) return;
   const int q0 = __ldg(a.cu_q + b), qlen = __ldg(a.cu_q + b + 1) - q0;
   const int n = __ldg(a.lens + b);
-  const bool lead = h == 0 && blockIdx.y == 0 && tid == 0;
-  if (qlen < 0 || n < qlen || (long long)n > (long long)a.max_blocks * a.bs) {
-    if (lead) raise_flag(a.err, PKV_FLAG_QUERY_LEN);
-    return;
-  }
-  if (qlen > a.q_tiles * kPfGroups * kPfRows && lead) raise_flag(a.err, PKV_FLAG_QUERY_OVER_HINT);
-  const int i0 = qt * kPfGroups * kPfRows;
-  if (i0 >= qlen) return;
-  const int rows = min(kPfGroups * kPfRows, qlen - i0);
+  if (!seq_ok(b, qlen)) return;
+  const int i0 = qt * kCtaRows;
+  const int rows = min(kCtaRows, qlen - i0);
   const int p_first = n - qlen + i0;               // position of query row 0
   // tiles each warpgroup needs: up to the position of its last real row
   const int rows1 = rows - kPfRows;                // rows of the second tile (may be <= 0)
@@ -216,6 +264,18 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       const int tok0 = j * kPfTile;
       const int valid_chunks = min(8, (n - tok0 + 15) >> 4);
       const uint32_t bytes = (uint32_t)(valid_chunks * Sh::kRegions * 2048);
+      // the tile's table entries: lane c < 8 loads chunk c's, broadcast to the
+      // lanes that issue that chunk's boxes (K and V, every region)
+      int phys = 0;
+      if (lane < valid_chunks) {
+        const int lb = (tok0 + 16 * lane) / a.bs;
+        phys = __ldg(a.tables + (size_t)b * a.max_blocks + lb);
+        if (phys < 0 || (long long)phys >= a.num_blocks) {
+          raise_flag(a.err, PKV_FLAG_BLOCK_OUT_OF_RANGE);
+          phys = 0;
+        }
+      }
+      phys = __shfl_sync(0xffffffffu, phys, chunk);
       for (int v = 0; v < 2 && ok; ++v) {
         if (j >= kPfStages) {
           const bool got = mbar_wait_bounded(v ? &v_empty[stage] : &k_empty[stage],
@@ -235,11 +295,6 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         if (lane < per_tensor && chunk < valid_chunks) {
           const int t = tok0 + 16 * chunk;
           const int lb = t / a.bs;
-          int phys = __ldg(a.tables + (size_t)b * a.max_blocks + lb);
-          if (phys < 0 || (long long)phys >= a.num_blocks) {
-            raise_flag(a.err, PKV_FLAG_BLOCK_OUT_OF_RANGE);
-            phys = 0;
-          }
           uint8_t *dst = sm + Sh::kKVOff + stage * 2 * Sh::kKVBytes + (v ? Sh::kKVBytes : 0) +
                          region * kKVRegion + chunk * 2048;
           tma_load_4d_keep(dst, v ? &tmV : &tmK, full, region * 64, kvh, t - lb * a.bs, phys);
@@ -492,11 +547,11 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 
 template <int D, typename T>
 static pkv_status launch_prefill_t(const PrefillArgs &a, const CUtensorMap &mk,
-                                   const CUtensorMap &mv, cudaStream_t stream) {
+                                   const CUtensorMap &mv, int ctas_per_head, cudaStream_t stream) {
   auto kern = pkv_prefill_tc_kernel<D, T>;
   static int configured[64] = {0};
   if (!allow_smem(kern, PfShape<D>::kSmem, configured)) return PKV_ERR_CUDA;
-  dim3 grid(a.H, a.q_tiles, a.B);
+  dim3 grid(a.H, ctas_per_head, 1);
   kern<<<grid, kPfThreads, PfShape<D>::kSmem, stream>>>(mk, mv, a);
   return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
@@ -505,7 +560,7 @@ pkv_status launch_prefill_tc(void *out, const void *q, const void *k_cache, cons
                              const int32_t *tables, const int32_t *cu_q, const int32_t *lens,
                              int B, int H, int KVH, int D, int bs, int max_blocks,
                              long long num_blocks, float scale, pkv_dtype dt, int q_tiles,
-                             int *err, cudaStream_t stream) {
+                             int ctas_per_head, int *err, cudaStream_t stream) {
   CUtensorMap mk, mv;
   if (!encode_cache_map(&mk, k_cache, dt, num_blocks, bs, KVH, D) ||
       !encode_cache_map(&mv, v_cache, dt, num_blocks, bs, KVH, D))
@@ -529,10 +584,10 @@ pkv_status launch_prefill_tc(void *out, const void *q, const void *k_cache, cons
   a.q_tiles = q_tiles;
   a.scale_log2 = scale * kLog2e;
   const bool bf = dt == PKV_BF16;
-  if (D == 128) return bf ? launch_prefill_t<128, __nv_bfloat16>(a, mk, mv, stream)
-                          : launch_prefill_t<128, __half>(a, mk, mv, stream);
-  if (D == 64) return bf ? launch_prefill_t<64, __nv_bfloat16>(a, mk, mv, stream)
-                         : launch_prefill_t<64, __half>(a, mk, mv, stream);
+  if (D == 128) return bf ? launch_prefill_t<128, __nv_bfloat16>(a, mk, mv, ctas_per_head, stream)
+                          : launch_prefill_t<128, __half>(a, mk, mv, ctas_per_head, stream);
+  if (D == 64) return bf ? launch_prefill_t<64, __nv_bfloat16>(a, mk, mv, ctas_per_head, stream)
+                         : launch_prefill_t<64, __half>(a, mk, mv, ctas_per_head, stream);
   return PKV_ERR_UNSUPPORTED;
 }
 
