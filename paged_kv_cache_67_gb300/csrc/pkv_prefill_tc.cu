@@ -149,7 +149,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   uint64_t *v_empty = bars + 7;    // [kPfStages]  scores that read a slot are done
   uint64_t *s_full = bars + 9;     // [kPfGroups]: S of the group's current tile
   uint64_t *p_full = bars + 11;    // [kPfGroups]: P of the group's current tile
-  uint64_t *o_done = bars + 13;    // [kPfGroups]: P . V of the group's current tile done
+  uint64_t *o_done = bars + 13;    // [kPfGroups]: the group's last P . V done
   uint64_t *mma_done = bars + 15;
   uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(bars + 16);
   int *abort_flag = reinterpret_cast<int *>(bars + 17);
@@ -331,12 +331,14 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         for (int k = 0; k < kPfTile / 16; ++k)
           umma_f16_tmem_a(tmem + 256 * g + 128, tmem + 256 * g + 8 * k,
                           umma_desc_sw128(vb + k * 2048, kKVRegion, 1024), idesc_o, (j > 0 || k > 0));
-        umma_commit(&o_done[g]);
       };
-      // S of the first tile of both groups; then per tile and group: P_g(j) . V_j
-      // as soon as P_g(j) arrives, then -- once that product has read P, which
-      // lies over the group's S columns -- S_g(j+1).  While one group's
-      // softmax runs, the tensor core serves the other group.
+      // S of the first tile of both groups; then per tile and group, as soon
+      // as P_g(j) arrives: P_g(j) . V_j, then S_g(j+1).  The products of one
+      // thread run in issue order, so S_g(j+1) -- written over P_g(j) --
+      // starts after P_g(j) . V_j has read it, and the commit that signals
+      // S_g(j+1) also covers P_g(j) . V_j (O is final for tile j when the
+      // softmax sees S_g(j+1)).  One commit per group and tile, one per
+      // released K and V slot; O's completion is signalled once, at the end.
       bool ok = mbar_wait_bounded(q_full, 0) && mbar_wait_bounded(&k_full[0], 0);
       if (ok) {
         tc_fence_after();
@@ -358,17 +360,14 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           tc_fence_after();
           issue_pv(g, j);
           if (j + 1 < tiles_of(g)) {
-            // the next S goes over P_g(j): wait until the product has read it
-            // (the other group's product or scores keep the tensor core busy)
-            ok = mbar_wait_bounded(&o_done[g], j & 1);
-            if (!ok) break;
             if (!k_ready) {
               ok = mbar_wait_bounded(&k_full[(j + 1) % kPfStages], ((j + 1) / kPfStages) & 1);
               if (!ok) break;
               k_ready = true;
             }
-            tc_fence_after();
             issue_s(g, j + 1);
+          } else {
+            umma_commit(&o_done[g]);  // the group's last product
           }
         }
         if (!ok) break;
@@ -449,8 +448,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       const bool rescale = __any_sync(0xffffffffu, m_new != m_used) && j > 0;
       l *= alpha;
       m_used = m_new;
-      // O is final for tile j-1 here: S_g(j) was issued after P_g(j-1) . V
-      // had completed
+      // O is final for tile j-1 here: the commit that signalled S_g(j) also
+      // covers P_g(j-1) . V, issued before it
       if (rescale) {
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
@@ -513,7 +512,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       tc_fence_before();
       mbar_arrive(&p_full[g]);
     }
-    if (ok && my_tiles > 0) ok = mbar_wait_bounded(&o_done[g], (my_tiles - 1) & 1);
+    if (ok && my_tiles > 0) ok = mbar_wait_bounded(&o_done[g], 0);
     if (my_tiles > 0 && __all_sync(0xffffffffu, ok) && !*(volatile int *)abort_flag) {
       tc_fence_after();
       const float inv_l = 1.f / l;
