@@ -100,12 +100,20 @@ def decode_traffic(kernel, workload):
 
 
 def sources_sha256():
-    """Digest of the sources the decode kernels are built from."""
+    """Digest of what the decode kernels' launches are built from: the
+    tensor-core kernel's file, the shared device header and the plan
+    (partition choice) in the API file."""
     import hashlib
+    import re
+    csrc = os.path.join(ROOT, "paged_kv_cache_67_gb300", "csrc")
     h = hashlib.sha256()
-    for f in ("pkv_decode_tc.cu", "pkv_device.cuh", "pkv_api.cu"):
-        with open(os.path.join(ROOT, "paged_kv_cache_67_gb300", "csrc", f), "rb") as fh:
+    for f in ("pkv_decode_tc.cu", "pkv_device.cuh"):
+        with open(os.path.join(csrc, f), "rb") as fh:
             h.update(fh.read())
+    with open(os.path.join(csrc, "pkv_api.cu")) as fh:
+        api = fh.read()
+    m = re.search(r"\nbool make_plan\(.*?\n}\n", api, re.S)
+    h.update((m.group(0) if m else api).encode())
     return h.hexdigest()
 
 
