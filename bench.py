@@ -373,15 +373,28 @@ def run_gpu(args, world, rank, local):
     ws = pkv.DecodeWorkspace(cfg.B, cfg.H, cfg.KVH, cfg.D, cfg.bs, cfg.table_width, max_ctx, 0,
                              device=dev)
     stream = torch.cuda.current_stream(dev)
-    fused = args.mode == "fused"
+    fused = args.mode == "fused" and args.layout == "token-major"
     peak, peak_kind = hbm_peak()
+    kx = vx = None
+    if args.layout == "xpacked":
+        # the layout experiment: the same values in vLLM's packed layout
+        nb = inp.k_cache.shape[0]
+        kx = inp.k_cache.view(nb, cfg.bs, cfg.KVH, cfg.D // 8, 8).permute(0, 2, 3, 1, 4).contiguous()
+        vx = inp.v_cache.permute(0, 2, 3, 1).contiguous()
 
     def write(st):
+        if kx is not None:
+            pkv.pkv_write_xpacked(kx, vx, st["k"], st["v"], st["slots"], err_flags=err, stream=stream)
+            return
         pkv.pkv_write(inp.k_cache, inp.v_cache, st["k"], st["v"], st["slots"], err_flags=err,
                       stream=stream)
 
     def decode(st):
-        if fused:
+        if kx is not None:
+            pkv.pkv_decode_attention_xpacked(out, st["q"], kx, vx, st["tables"], st["lens"], inp.scale,
+                                             max_context_len=max_ctx, workspace=ws, err_flags=err,
+                                             stream=stream)
+        elif fused:
             pkv.pkv_write_decode_attention(out, st["q"], st["k"], st["v"], st["slots"],
                                            inp.k_cache, inp.v_cache, st["tables"], st["lens"],
                                            inp.scale, max_context_len=max_ctx, workspace=ws,
@@ -510,7 +523,8 @@ def run_gpu(args, world, rank, local):
     cpu = None
     if world == 1 and not args.only_decode and not args.no_cpu_baseline:
         cpu = cpu_baseline(inp, elem)
-    kname = kernel_name(cfg, args.mode)
+    kname = (kernel_name(cfg, args.mode) if kx is None else
+             f"pkv_decode_xpacked_kernel<{cfg.D}, bf16>")
     dt = {torch.bfloat16: "bf16", torch.float16: "fp16", torch.float32: "fp32"}[cfg.dtype]
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
@@ -672,9 +686,14 @@ def main():
                          "pkv_write then pkv_decode_attention")
     ap.add_argument("--graph", action="store_true",
                     help="replay the timed steps from one CUDA graph")
+    ap.add_argument("--layout", default="token-major", choices=["token-major", "xpacked"],
+                    help="xpacked: the layout experiment (caches in vLLM's packed layout, "
+                         "write + decode in two launches; with --only-decode)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.layout == "xpacked" and not args.only_decode:
+        ap.error("--layout xpacked goes with --only-decode")
     world, rank, local = dist_setup()
     try:
         if args.impl == "reference":

@@ -301,6 +301,40 @@ PKV_API pkv_status pkv_prefill_attention(void *out, const void *q, const void *k
                                          int max_q_len, int *err_flags, pkv_stream_t stream);
 
 /*
+ * The layout experiment: vLLM's packed cache layout, which the interview
+ * note "PagedAttention kernel: paged KV cache 与 block table" describes in
+ * section 深入原理 (K cache [num_blocks, num_kv_heads, head_size / x,
+ * block_size, x] with x = 16 / element size so that loads are aligned
+ * 16-byte vectors; V cache [num_blocks, num_kv_heads, head_size,
+ * block_size]).  For 16-bit types x = 8:
+ *   k_cache_x[blk][kvh][d / 8][off][d % 8],   v_cache_x[blk][kvh][d][off]
+ * holding the same values as the token-major caches of pkv_write /
+ * pkv_decode_attention.  Only block_size 16, bf16 / fp16.  The library's
+ * main path keeps the token-major layout; these two calls exist to measure
+ * the difference (one contiguous copy per (block, KV head) instead of
+ * head_dim / 64 tiled boxes).
+ *
+ * pkv_write_xpacked -- pkv_write into the packed layout (same arguments and
+ * errors; block_size must be 16, head_dim a multiple of 8, k and the
+ * caches 16-byte aligned, token strides multiples of 8 elements).
+ * pkv_decode_attention_xpacked -- pkv_decode_attention over packed caches
+ * (same arguments, workspace and errors; head_dim 64, 128 or 256; returns
+ * PKV_ERR_UNSUPPORTED for other shapes and for fp32).
+ */
+PKV_API pkv_status pkv_write_xpacked(void *k_cache_x, void *v_cache_x, const void *k, const void *v,
+                                     const int64_t *slot_mapping, int64_t num_tokens,
+                                     int64_t k_token_stride, int64_t v_token_stride,
+                                     int64_t num_blocks, int block_size, int num_kv_heads,
+                                     int head_dim, pkv_dtype dt, int *err_flags,
+                                     pkv_stream_t stream);
+PKV_API pkv_status pkv_decode_attention_xpacked(
+    void *out, const void *q, const void *k_cache_x, const void *v_cache_x,
+    const int32_t *block_tables, const int32_t *context_lens, int B, int H, int num_kv_heads,
+    int head_dim, int block_size, int max_blocks, int64_t num_blocks, float scale, pkv_dtype dt,
+    int max_context_len, int partition_size, void *workspace, size_t workspace_bytes,
+    int *err_flags, pkv_stream_t stream);
+
+/*
  * pkv_decode_plan -- the partition size and the partitions per sequence that
  * pkv_decode_attention would use for these arguments on a GPU with
  * num_sms SMs (host only, no CUDA call; for tests and tuning).  Returns the

@@ -26,6 +26,7 @@ from ._binding import (  # noqa: F401
     library_path,
     load_library,
     pkv_decode_attention,
+    pkv_decode_attention_xpacked,
     pkv_decode_plan,
     pkv_decode_workspace_size,
     pkv_prefill_attention,
@@ -33,4 +34,5 @@ from ._binding import (  # noqa: F401
     pkv_version,
     pkv_write,
     pkv_write_decode_attention,
+    pkv_write_xpacked,
 )

@@ -75,6 +75,11 @@ def load_library():
                                                    ctypes.c_float, c_int, c_int, c_int, vp, c_size,
                                                    vp, vp]
         lib.pkv_write_decode_attention.restype = c_int
+        lib.pkv_write_xpacked.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, c_int, c_int, c_int,
+                                          c_int, vp, vp]
+        lib.pkv_write_xpacked.restype = c_int
+        lib.pkv_decode_attention_xpacked.argtypes = lib.pkv_decode_attention.argtypes
+        lib.pkv_decode_attention_xpacked.restype = c_int
         lib.pkv_prefill_attention.argtypes = [vp, vp, vp, vp, vp, vp, vp, c_int, i64, c_int, c_int,
                                               c_int, c_int, c_int, i64, ctypes.c_float, c_int, c_int,
                                               vp, vp]
@@ -401,3 +406,45 @@ class BlockManager:
 
     def refcount(self, block: int) -> int:
         return self._lib.pkv_bm_block_refcount(self._h, int(block))
+
+
+# ------------------------------------------------------- layout experiment
+
+def pkv_write_xpacked(k_cache_x, v_cache_x, k, v, slot_mapping, err_flags=None, stream=None) -> None:
+    """write_kv into the packed layout: k_cache_x [nb, KVH, D/8, 16, 8],
+    v_cache_x [nb, KVH, D, 16]; k, v [T, KVH, D]; slot_mapping [T] int64."""
+    lib = load_library()
+    _require(k_cache_x.dim() == 5 and k_cache_x.shape[3] == 16 and k_cache_x.shape[4] == 8,
+             "k_cache_x must be [nb, KVH, D/8, 16, 8]")
+    nb, kvh, dg, bs, _ = k_cache_x.shape
+    d = dg * 8
+    _require(v_cache_x.shape == (nb, kvh, d, bs), "v_cache_x must be [nb, KVH, D, 16]")
+    _require(k.dim() == 3 and v.shape == k.shape and k.shape[1:] == (kvh, d), "k, v must be [T, KVH, D]")
+    _require(k.stride(2) == 1 and k.stride(1) == d and v.stride(2) == 1 and v.stride(1) == d,
+             "each token's [KVH, D] row must be contiguous")
+    _require(slot_mapping.dtype == torch.int64 and slot_mapping.numel() == k.shape[0], "slot_mapping int64 [T]")
+    dev = k.device
+    T = k.shape[0]
+    _check(lib.pkv_write_xpacked(_ptr(k_cache_x), _ptr(v_cache_x), _ptr(k), _ptr(v), _ptr(slot_mapping), T,
+                                 k.stride(0) if T > 0 else kvh * d, v.stride(0) if T > 0 else kvh * d,
+                                 nb, bs, kvh, d, _DT[k.dtype], _ptr(err_flags), _stream_handle(stream, dev)),
+           "pkv_write_xpacked")
+
+
+def pkv_decode_attention_xpacked(out, q, k_cache_x, v_cache_x, block_tables, context_lens, scale: float,
+                                 max_context_len: int = 0, partition_size: int = 0, workspace=None,
+                                 err_flags=None, stream=None):
+    """Paged decode attention over packed caches (see pkv_write_xpacked)."""
+    lib = load_library()
+    _require(q.dim() == 3 and out.shape == q.shape, "q and out must be [B, H, D]")
+    B, H, D = q.shape
+    nb, kvh, dg, bs, _ = k_cache_x.shape
+    _require(dg * 8 == D and v_cache_x.shape == (nb, kvh, D, bs), "packed caches do not match q")
+    ws_ptr, ws_bytes = _workspace_arg(workspace)
+    _check(lib.pkv_decode_attention_xpacked(_ptr(out), _ptr(q), _ptr(k_cache_x), _ptr(v_cache_x),
+                                            _ptr(block_tables), _ptr(context_lens), B, H, kvh, D, bs,
+                                            block_tables.shape[1], nb, float(scale), _DT[q.dtype],
+                                            int(max_context_len), int(partition_size), ws_ptr, ws_bytes,
+                                            _ptr(err_flags), _stream_handle(stream, q.device)),
+           "pkv_decode_attention_xpacked")
+    return out

@@ -194,7 +194,7 @@ static pkv_status decode_entry(void *out, const void *q, const void *k_cache, co
                                int max_blocks, int64_t num_blocks, float scale, pkv_dtype dt,
                                int max_context_len, int partition_size, void *workspace,
                                size_t workspace_bytes, int *err_flags, pkv_stream_t stream,
-                               const AppendIn *app) {
+                               const AppendIn *app, bool xpacked = false) {
   if (B < 0 || B > 65535 || H <= 0 || H > 65535 || num_kv_heads <= 0 || H % num_kv_heads != 0 ||
       head_dim <= 0 || block_size <= 0 || max_blocks < 0 || num_blocks < 0 ||
       num_blocks > 0x7fffffffLL || max_context_len < 0 || partition_size < 0 ||
@@ -223,6 +223,8 @@ static pkv_status decode_entry(void *out, const void *q, const void *k_cache, co
                  partition_size, dt, sms, smem_optin, aligned16, &plan))
     return PKV_ERR_INVALID_ARG;
   if ((long long)num_kv_heads * plan.gchunks > 65535) return PKV_ERR_UNSUPPORTED;
+  if (xpacked && (plan.kernel != 1 || block_size != 16 || head_dim == 192))
+    return PKV_ERR_UNSUPPORTED;
 
   DecodeArgs a;
   memset(&a, 0, sizeof a);
@@ -272,6 +274,7 @@ static pkv_status decode_entry(void *out, const void *q, const void *k_cache, co
     }
   }
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (xpacked) return launch_decode_xpacked(a, plan, dt, s);
   return plan.kernel ? launch_decode_tc(a, plan, dt, s) : launch_decode_simt(a, plan, dt, s);
 }
 
@@ -314,6 +317,39 @@ PKV_API pkv_status pkv_write_decode_attention(
   return decode_entry(out, q, k_cache, v_cache, block_tables, context_lens, B, H, num_kv_heads,
                       head_dim, block_size, max_blocks, num_blocks, scale, dt, max_context_len,
                       partition_size, workspace, workspace_bytes, err_flags, stream, &app);
+}
+
+PKV_API pkv_status pkv_write_xpacked(void *k_cache_x, void *v_cache_x, const void *k, const void *v,
+                                     const int64_t *slot_mapping, int64_t num_tokens,
+                                     int64_t k_token_stride, int64_t v_token_stride,
+                                     int64_t num_blocks, int block_size, int num_kv_heads,
+                                     int head_dim, pkv_dtype dt, int *err_flags,
+                                     pkv_stream_t stream) {
+  if (num_tokens < 0 || num_blocks < 0 || num_kv_heads <= 0 || head_dim <= 0)
+    return PKV_ERR_INVALID_ARG;
+  if (dt != PKV_F32 && dt != PKV_BF16 && dt != PKV_F16) return PKV_ERR_INVALID_ARG;
+  if (dt == PKV_F32 || block_size != 16 || head_dim % 8 != 0) return PKV_ERR_UNSUPPORTED;
+  const int64_t row = (int64_t)num_kv_heads * head_dim;
+  if (k_token_stride < row || v_token_stride < row || k_token_stride % 8 || v_token_stride % 8)
+    return PKV_ERR_INVALID_ARG;
+  if (num_tokens == 0) return PKV_OK;
+  if (!k_cache_x || !v_cache_x || !k || !v || !slot_mapping ||
+      reinterpret_cast<uintptr_t>(k) % 16 || reinterpret_cast<uintptr_t>(k_cache_x) % 16)
+    return PKV_ERR_INVALID_ARG;
+  return launch_write_xpacked(k_cache_x, v_cache_x, k, v, slot_mapping, num_tokens, k_token_stride,
+                              v_token_stride, num_blocks, num_kv_heads, head_dim, dt, err_flags,
+                              reinterpret_cast<cudaStream_t>(stream));
+}
+
+PKV_API pkv_status pkv_decode_attention_xpacked(
+    void *out, const void *q, const void *k_cache_x, const void *v_cache_x,
+    const int32_t *block_tables, const int32_t *context_lens, int B, int H, int num_kv_heads,
+    int head_dim, int block_size, int max_blocks, int64_t num_blocks, float scale, pkv_dtype dt,
+    int max_context_len, int partition_size, void *workspace, size_t workspace_bytes,
+    int *err_flags, pkv_stream_t stream) {
+  return decode_entry(out, q, k_cache_x, v_cache_x, block_tables, context_lens, B, H, num_kv_heads,
+                      head_dim, block_size, max_blocks, num_blocks, scale, dt, max_context_len,
+                      partition_size, workspace, workspace_bytes, err_flags, stream, nullptr, true);
 }
 
 PKV_API pkv_status pkv_prefill_attention(void *out, const void *q, const void *k_cache,

@@ -71,7 +71,14 @@ pkv_status launch_prefill_tc(void *out, const void *q, const void *k_cache, cons
                              long long num_blocks, float scale, pkv_dtype dt, int q_tiles,
                              int ctas_per_head, int *err, cudaStream_t stream);
 
+pkv_status launch_write_xpacked(void *kx, void *vx, const void *k, const void *v,
+                                const int64_t *slots, long long ntok, long long k_stride,
+                                long long v_stride, long long num_blocks, int KVH, int D,
+                                pkv_dtype dt, int *err, cudaStream_t stream);
+
 struct DecodeArgs;
+pkv_status launch_decode_xpacked(const DecodeArgs &a, const DecodePlan &plan, pkv_dtype dt,
+                                 cudaStream_t stream);
 pkv_status launch_decode_simt(const DecodeArgs &a, const DecodePlan &plan, pkv_dtype dt,
                               cudaStream_t stream);
 pkv_status launch_decode_tc(const DecodeArgs &a, const DecodePlan &plan, pkv_dtype dt,
