@@ -376,13 +376,15 @@ PKV_API pkv_status pkv_prefill_attention(void *out, const void *q, const void *k
       reinterpret_cast<uintptr_t>(context_lens) % 4)
     return PKV_ERR_INVALID_ARG;
   const long long mq = max_q_len > 0 ? max_q_len : total_q;
-  const long long q_tiles = (mq + 255) / 256;  // 256 queries (two 128-row tiles) per CTA
-  // CTAs per head: at least the (sequence, tile) pairs, sum ceil(qlen / 256) <= total_q / 256 + B
-  const long long ctas = std::min<long long>((total_q + 255) / 256 + B, (long long)B * q_tiles);
-  if (q_tiles > 65535 || ctas > 65535) return PKV_ERR_UNSUPPORTED;
+  const long long q_tiles = (mq + 255) / 256;  // 256 queries (two 128-row tiles) per work item
+  // (sequence, tile) pairs: sum ceil(qlen / 256) <= total_q / 256 + B; work
+  // items are (pair, head) and are counted in 32 bits
+  const long long pairs = std::min<long long>((total_q + 255) / 256 + B, (long long)B * q_tiles);
+  if (q_tiles > 65535 || pairs * H > 0x7fffffffLL) return PKV_ERR_UNSUPPORTED;
   return launch_prefill_tc(out, q, k_cache, v_cache, block_tables, cu_seqlens_q, context_lens, B,
-                           H, num_kv_heads, head_dim, block_size, max_blocks, num_blocks, scale, dt,
-                           (int)q_tiles, (int)ctas, err_flags, reinterpret_cast<cudaStream_t>(stream));
+                           total_q, H, num_kv_heads, head_dim, block_size, max_blocks, num_blocks,
+                           scale, dt, (int)q_tiles, (int)pairs, err_flags,
+                           reinterpret_cast<cudaStream_t>(stream));
 }
 
 PKV_API const char *pkv_status_string(pkv_status status) {

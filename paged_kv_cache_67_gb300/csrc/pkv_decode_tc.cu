@@ -475,6 +475,23 @@ bool encode_cache_map(CUtensorMap *map, const void *cache, pkv_dtype dt, long lo
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Tensor map of a [rows, H, D] 16-bit tensor (one row of H heads per token):
+// box of 64 elements x 1 head x box_rows rows, 128-byte swizzle; rows past
+// the end read as zero.
+bool encode_rows_map(CUtensorMap *map, const void *base, pkv_dtype dt, long long rows, int H, int D,
+                     int box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t el = 2;
+  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)rows};
+  cuuint64_t strides[2] = {D * el, (cuuint64_t)H * D * el};
+  cuuint32_t box[3] = {kBoxElems, 1, (cuuint32_t)box_rows};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, map_type(dt), 3, const_cast<void *>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int D, typename T, bool kAppend>
 static pkv_status launch_tc_k(const DecodeArgs &a, const DecodePlan &plan, const CUtensorMap &mk,
                               const CUtensorMap &mv, cudaStream_t stream) {

@@ -51,6 +51,11 @@ pkv_status launch_write(void *k_cache, void *v_cache, const void *k, const void 
 bool encode_cache_map(CUtensorMap *map, const void *cache, pkv_dtype dt, long long num_blocks,
                       int bs, int KVH, int D);
 
+// Tensor map of a [rows, H, D] 16-bit tensor: box of 64 elements x 1 head x
+// box_rows rows, 128-byte swizzle, zero past the last row.
+bool encode_rows_map(CUtensorMap *map, const void *base, pkv_dtype dt, long long rows, int H, int D,
+                     int box_rows);
+
 // One-time opt-in to a kernel's dynamic shared memory, per device
 // (`configured` is the kernel's own per-device record).
 template <typename K>
@@ -65,11 +70,13 @@ inline bool allow_smem(K kern, size_t bytes, int *configured) {
   return true;
 }
 
+// Persistent varlen prefill: pairs_bound bounds the (sequence, 256-query
+// tile) pairs, q_tiles the tiles of one sequence.
 pkv_status launch_prefill_tc(void *out, const void *q, const void *k_cache, const void *v_cache,
                              const int32_t *tables, const int32_t *cu_q, const int32_t *lens,
-                             int B, int H, int KVH, int D, int bs, int max_blocks,
-                             long long num_blocks, float scale, pkv_dtype dt, int q_tiles,
-                             int ctas_per_head, int *err, cudaStream_t stream);
+                             int B, long long total_q, int H, int KVH, int D, int bs,
+                             int max_blocks, long long num_blocks, float scale, pkv_dtype dt,
+                             int q_tiles, int pairs_bound, int *err, cudaStream_t stream);
 
 pkv_status launch_write_xpacked(void *kx, void *vx, const void *k, const void *v,
                                 const int64_t *slots, long long ntok, long long k_stride,

@@ -124,6 +124,46 @@ def test_error_flags_and_unsupported():
     assert e.value.status == 2
 
 
+def test_persistent_many_items_per_cta():
+    """Several hundred (head, sequence, 256-query) items, several per CTA of
+    the persistent grid, varied lengths (whole prompts and chunks on cached
+    prefixes) so that one CTA's items differ in shape."""
+    g = torch.Generator().manual_seed(77)
+    lens = torch.randint(1, 700, (24,), generator=g).tolist()
+    qlens = [n if b % 3 else max(1, n // 3) for b, n in enumerate(lens)]
+    check(77, lens, qlens, 16, 4, 64, 16, torch.bfloat16, "many items")
+
+
+def test_persistent_relaunch_and_graph_replay():
+    """The work counters are taken back by each launch's last CTA: back-to-back
+    launches and replays of one captured launch all give the oracle's result."""
+    case, q, cu = make_case(78, [300, 17, 529, 256], [300, 1, 200, 256], 8, 2, 128, 16,
+                            torch.bfloat16)
+    scale = 0.09
+    want = oracle.prefill(q, case["k_cache"], case["v_cache"], case["block_tables"], cu,
+                          case["context_lens"], scale)
+    for _ in range(3):
+        out, err = gpu_prefill(q, case, cu, scale)
+        assert err == 0
+        assert_close(out, want, torch.bfloat16, "relaunch")
+    d = {k: case[k].to(DEV) for k in ("k_cache", "v_cache", "block_tables", "context_lens")}
+    qd, cud = q.to(DEV), cu.to(DEV)
+    out = torch.zeros_like(qd)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=side):
+        pkv.pkv_prefill_attention(out, qd, d["k_cache"], d["v_cache"], d["block_tables"], cud,
+                                  d["context_lens"], scale, err_flags=err, stream=side)
+    for _ in range(3):
+        out.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+        assert_close(out, want, torch.bfloat16, "graph replay")
+
+
 def test_full_size_llama8b_prefill_sampled():
     """An 8B-shaped varlen prefill batch at the bench's size: a sample of
     sequences against the oracle."""
