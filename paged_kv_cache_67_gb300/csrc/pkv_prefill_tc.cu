@@ -21,18 +21,23 @@
 // SM) and CTA c takes item c, then the next unclaimed one from a counter in
 // device memory, so the tensor memory stays allocated, the next item's
 // queries and first K/V tiles load while the current one finishes, and the
-// epilogue of one item overlaps the first products of the next.  10 warps:
-//   warp 0     producer: claims items and publishes them to the CTA (a
-//              two-slot ring), then per 128-token KV tile issues the tiled
+// epilogue of one item overlaps the first products of the next.  11 warps:
+//   warp 10    scheduler: claims items, publishes each (its geometry
+//              worked out once) to the CTA through a two-slot ring as soon
+//              as a slot is free, and loads the item's two query tiles (TMA,
+//              128-byte swizzle) once the products that read the previous
+//              ones are done;
+//   warp 0     producer: per item and 128-token KV tile issues the tiled
 //              TMA loads of K and of V (16-token chunks of 64-column
 //              regions, 128-byte swizzle) into a two-stage ring that runs on
-//              across items, and each item's two query tiles (TMA, same
-//              swizzle) once the products that read the previous ones ended;
+//              across items;
 //   warp 1     MMA issuer (one thread): per group g (query tile),
 //              S_g = Q_g . K^T (M = 128, N = 128 tokens, fp32 in tensor
 //              memory); once the softmax wrote P_g over S_g, O_g += P_g . V
 //              (P from tensor memory, N = D), and right behind it the next
 //              tile's S_g; the products of one thread run in issue order;
+//              group 0 starts its next item while group 1 ends the current
+//              one;
 //   warps 2-5, 6-9  two softmax warpgroups, one per query tile, one query
 //              row per thread (its tensor-memory lane): per KV tile read S,
 //              mask (causal, end of context), update the running max -- the
@@ -57,11 +62,12 @@ constexpr int kPfRows = 128;     // query rows per softmax warpgroup (MMA M)
 constexpr int kPfGroups = 2;     // query tiles per item, one softmax warpgroup each
 constexpr int kPfTile = 128;     // KV tokens per tile
 constexpr int kPfStages = 2;     // K/V ring depth
-constexpr int kPfWarps = 2 + 4 * kPfGroups;
+constexpr int kSchedWarp = 2 + 4 * kPfGroups;  // after producer, MMA and softmax warps
+constexpr int kPfWarps = 3 + 4 * kPfGroups;
 constexpr int kPfThreads = 32 * kPfWarps;
 constexpr int kQRegion = kPfRows * 128;   // 128 query rows x 64 elements of 16 bits
 constexpr int kKVRegion = kPfTile * 128;  // 128 token rows x 64 elements
-constexpr int kItemReaders = 1 + 4 * kPfGroups;  // MMA thread + one lane per softmax warp
+constexpr int kItemReaders = 2 + 4 * kPfGroups;  // producer, MMA thread, one lane per softmax warp
 constexpr int kSchedSlots = 1024;         // work counters, one per launch in flight
 
 // Work counters of the persistent launches: slot s holds (next item to claim
@@ -117,6 +123,19 @@ __device__ __forceinline__ void tma_load_3d_keep(void *dst, const CUtensorMap *m
       : "memory");
 }
 
+// Whether the phase with the given parity has completed (never waits).
+__device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Blackwell paired fp32 arithmetic and the three-input max.
 __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
   unsigned long long d;
@@ -157,40 +176,44 @@ struct PackPair<__half> {
   }
 };
 
-// One work item as every role sees it.  kind: 1 work, 0 skipped (a sequence
-// whose lengths are invalid), -1 no more items.
-struct PfItem {
+// One work item as every role sees it (published in shared memory by the
+// scheduler warp).  kind: 1 work, 0 skipped (a sequence whose lengths are
+// invalid), -1 no more items.
+struct __align__(16) PfItem {
   int kind, h, b, qt;
-  int q0, qlen, n, rows, p_first;
-  int nt[kPfGroups];   // KV tiles each query tile needs (up to its last real row)
+  int q0, qlen, n, rows;   // q0: the item's first query row
+  int p_first;             // position of the item's query row 0
+  int nt[kPfGroups];       // KV tiles each query tile needs (up to its last real row)
   int ntiles;
 };
+static_assert(sizeof(PfItem) == 48, "three 16-byte words");
+
+__device__ __forceinline__ int nt_of(const PfItem &it, int g) { return g == 0 ? it.nt[0] : it.nt[1]; }
 
 __device__ __forceinline__ bool pf_seq_ok(const PrefillArgs &a, int bb, int ql) {
   const int nn = __ldg(a.lens + bb);
   return ql >= 0 && nn >= ql && (long long)nn <= (long long)a.max_blocks * a.bs;
 }
 
-__device__ __forceinline__ PfItem pf_item(const PrefillArgs &a, int4 d) {
+__device__ __forceinline__ PfItem pf_item(const PrefillArgs &a, int kind, int h, int b, int qt) {
   PfItem it;
-  it.kind = d.w;
-  it.h = d.x;
-  it.b = d.y;
-  it.qt = d.z;
-  it.ntiles = 0;
-  it.nt[0] = it.nt[1] = 0;
-  if (it.kind != 1) return it;
-  it.q0 = __ldg(a.cu_q + it.b);
-  it.qlen = __ldg(a.cu_q + it.b + 1) - it.q0;
-  it.n = __ldg(a.lens + it.b);
-  const int i0 = it.qt * kPfGroups * kPfRows;
+  memset(&it, 0, sizeof it);
+  it.kind = kind;
+  it.h = h;
+  it.b = b;
+  it.qt = qt;
+  if (kind != 1) return it;
+  it.q0 = __ldg(a.cu_q + b);
+  it.qlen = __ldg(a.cu_q + b + 1) - it.q0;
+  it.n = __ldg(a.lens + b);
+  const int i0 = qt * kPfGroups * kPfRows;
   it.rows = min(kPfGroups * kPfRows, it.qlen - i0);
-  it.p_first = it.n - it.qlen + i0;               // position of the item's query row 0
+  it.p_first = it.n - it.qlen + i0;
   const int rows1 = it.rows - kPfRows;            // rows of the second tile (may be <= 0)
   it.nt[0] = (it.p_first + min(kPfRows, it.rows) - 1) / kPfTile + 1;
   it.nt[1] = rows1 > 0 ? (it.p_first + kPfRows + rows1 - 1) / kPfTile + 1 : 0;
   it.ntiles = max(it.nt[0], it.nt[1]);
-  it.q0 += i0;                                    // first query row of the item
+  it.q0 += i0;
   return it;
 }
 
@@ -258,7 +281,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   uint64_t *mma_done = bars + 22;
   uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(bars + 23);
   int *abort_flag = reinterpret_cast<int *>(bars + 24);
-  int4 *items = reinterpret_cast<int4 *>(bars + 26);  // [2], 16-byte aligned
+  PfItem *items = reinterpret_cast<PfItem *>(bars + 26);  // [2], 16-byte aligned
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
@@ -296,9 +319,10 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     raise_flag(a.err, PKV_FLAG_TIMEOUT);
     *(volatile int *)abort_flag = 1;
   };
+  auto aborted = [&]() { return *(volatile int *)abort_flag != 0; };
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
+  if (warp == kSchedWarp) {
+    // ------------------------------------------------------------ scheduler
     // the pairs there are, and (one CTA) the checks of the whole batch
     int pairs = 0, bad = 0, over = 0;
     for (int bb = lane; bb < a.B; bb += 32) {
@@ -314,90 +338,105 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     if (__any_sync(0xffffffffu, bad) && lane == 0) raise_flag(a.err, PKV_FLAG_QUERY_LEN);
     if (__any_sync(0xffffffffu, over) && lane == 0) raise_flag(a.err, PKV_FLAG_QUERY_OVER_HINT);
     const unsigned total = (unsigned)pairs * (unsigned)a.H;
-
-    const int per_tensor = 8 * Sh::kRegions;     // boxes of K (or V) per 128-token tile
-    const int region = (lane % per_tensor) >> 3, chunk = lane & 7;
+    // claim items (CTA c starts with item c, then takes the next unclaimed
+    // one), publish each to the CTA as soon as a ring slot is free, and load
+    // its query tiles once the products that read the previous ones are done
     unsigned w = blockIdx.x;
     int it = 0, ig[kPfGroups] = {0, 0};
-    int k_issued = 0, v_issued = 0;              // ring tiles whose K / V loads were issued
     bool ok = true;
-    while (ok) {
-      // claim and publish the next item
-      int4 d = make_int4(0, -1, 0, -1);
+    while (true) {
+      PfItem item = pf_item(a, -1, 0, -1, 0);
       if (w < total) {
         int bb, qq;
         pf_pair(a, (int)(w / (unsigned)a.H), lane, &bb, &qq);
-        d = make_int4((int)(w % (unsigned)a.H), bb, qq, 0);
-        if (bb >= 0) {
+        const int hh = (int)(w % (unsigned)a.H);
+        if (bb < 0) {
+          item = pf_item(a, 0, hh, bb, qq);
+        } else {
           const int ql = __ldg(a.cu_q + bb + 1) - __ldg(a.cu_q + bb);
-          d.w = pf_seq_ok(a, bb, ql) ? 1 : 0;
+          item = pf_item(a, pf_seq_ok(a, bb, ql) ? 1 : 0, hh, bb, qq);
         }
       }
       const int slot = it & 1;
       if (it >= 2) {
-        const bool got = mbar_wait_bounded(&item_empty[slot], ((it >> 1) - 1) & 1);
-        if (!__all_sync(0xffffffffu, got)) {
-          if (lane == 0) abort_cta();
-          break;
-        }
+        ok = __all_sync(0xffffffffu, mbar_wait_bounded(&item_empty[slot], ((it >> 1) - 1) & 1));
+        if (!ok) break;
       }
       if (lane == 0) {
-        items[slot] = d;
+        items[slot] = item;
         mbar_arrive(&item_full[slot]);
       }
       __syncwarp();
       ++it;
-      if (d.w < 0) break;
-      const PfItem item = pf_item(a, d);
+      if (item.kind < 0) break;
+      if (item.kind == 1) {
+#pragma unroll
+        for (int g = 0; g < kPfGroups; ++g) {
+          if (!ok || item.nt[g] == 0) continue;
+          if (ig[g] > 0) {
+            ok = __all_sync(0xffffffffu, mbar_wait_bounded(&q_empty[g], (ig[g] - 1) & 1)) && !aborted();
+            if (!ok) break;
+          }
+          if (lane == 0) mbar_arrive_expect_tx(&q_full[g], (uint32_t)Sh::kQBytes);
+          __syncwarp();
+          if (lane < Sh::kRegions)
+            tma_load_3d_keep(sm + Sh::kQOff + g * Sh::kQBytes + lane * kQRegion, &tmQ, &q_full[g],
+                             64 * lane, item.h, item.q0 + kPfRows * g);
+          ++ig[g];
+        }
+        if (!ok) break;
+      }
+      unsigned nw = 0;
+      if (lane == 0) nw = atomicAdd(a.sched, 1u) + gridDim.x;
+      w = __shfl_sync(0xffffffffu, nw, 0);
+    }
+    if (!ok && lane == 0) abort_cta();
+    // the last query tiles land before the CTA can end (bounded)
+#pragma unroll
+    for (int g = 0; g < kPfGroups; ++g)
+      if (ig[g] > 0) mbar_wait_bounded(&q_full[g], (ig[g] - 1) & 1);
+  } else if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    // per item and 128-token KV tile: the K boxes (one per lane) once the
+    // keys two ring tiles back are no longer read, then the V boxes once
+    // the values two ring tiles back are not
+    const int per_tensor = 8 * Sh::kRegions;     // boxes of K (or V) per 128-token tile
+    const int region = (lane % per_tensor) >> 3, chunk = lane & 7;
+    int it = 0, k_issued = 0, v_issued = 0;     // items read, ring tiles whose K / V loads were issued
+    bool ok = true;
+    while (ok) {
+      const int slot = it & 1;
+      ok = __all_sync(0xffffffffu, mbar_wait_bounded(&item_full[slot], (it >> 1) & 1));
+      if (!ok) break;
+      const PfItem item = items[slot];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&item_empty[slot]);
+      ++it;
+      if (item.kind < 0) break;
       const int kvh = item.h / a.G;
       for (int j = 0; j < item.ntiles && ok; ++j) {
         const int ring = k_issued, stage = ring % kPfStages, use = ring / kPfStages;
         const int tok0 = j * kPfTile;
         const int valid_chunks = min(8, (item.n - tok0 + 15) >> 4);
         const uint32_t bytes = (uint32_t)(valid_chunks * Sh::kRegions * 2048);
-        // the tile's table entries: lane c < 8 loads chunk c's, broadcast to
-        // the lanes that issue that chunk's boxes (K and V, every region)
+        // the tile's table entries: lane c < 8 loads chunk c's (in flight
+        // during the wait below), broadcast to the lanes that issue that
+        // chunk's boxes (K and V, every region)
         int phys = 0;
-        if (lane < valid_chunks) {
-          const int lb = (tok0 + 16 * lane) / a.bs;
-          phys = __ldg(a.tables + (size_t)item.b * a.max_blocks + lb);
-          if (phys < 0 || (long long)phys >= a.num_blocks) {
-            raise_flag(a.err, PKV_FLAG_BLOCK_OUT_OF_RANGE);
-            phys = 0;
-          }
-        }
-        phys = __shfl_sync(0xffffffffu, phys, chunk);
+        if (lane < valid_chunks) phys = __ldg(a.tables + (size_t)item.b * a.max_blocks + (tok0 + 16 * lane) / a.bs);
         for (int v = 0; v < 2 && ok; ++v) {
-          if (v == 1 && j == 0) {
-            // the item's query tiles, once the products that read the
-            // previous ones are done
-#pragma unroll
-            for (int g = 0; g < kPfGroups; ++g) {
-              if (!ok || item.nt[g] == 0) continue;
-              if (ig[g] > 0) {
-                const bool got = mbar_wait_bounded(&q_empty[g], (ig[g] - 1) & 1);
-                if (!__all_sync(0xffffffffu, got) || *(volatile int *)abort_flag) {
-                  if (lane == 0) abort_cta();
-                  ok = false;
-                  break;
-                }
-              }
-              if (lane == 0) mbar_arrive_expect_tx(&q_full[g], (uint32_t)Sh::kQBytes);
-              __syncwarp();
-              if (lane < Sh::kRegions)
-                tma_load_3d_keep(sm + Sh::kQOff + g * Sh::kQBytes + lane * kQRegion, &tmQ,
-                                 &q_full[g], 64 * lane, item.h, item.q0 + kPfRows * g);
-              ++ig[g];
-            }
+          if (ring >= kPfStages) {
+            ok = __all_sync(0xffffffffu,
+                            mbar_wait_bounded(v ? &v_empty[stage] : &k_empty[stage], (use - 1) & 1)) &&
+                 !aborted();
             if (!ok) break;
           }
-          if (ring >= kPfStages) {
-            const bool got = mbar_wait_bounded(v ? &v_empty[stage] : &k_empty[stage], (use - 1) & 1);
-            if (!__all_sync(0xffffffffu, got) || *(volatile int *)abort_flag) {
-              if (lane == 0) abort_cta();
-              ok = false;
-              break;
+          if (v == 0) {
+            if (lane < valid_chunks && (phys < 0 || (long long)phys >= a.num_blocks)) {
+              raise_flag(a.err, PKV_FLAG_BLOCK_OUT_OF_RANGE);
+              phys = 0;
             }
+            phys = __shfl_sync(0xffffffffu, phys, chunk);
           }
           uint64_t *full = v ? &v_full[stage] : &k_full[stage];
           if (lane == 0) mbar_arrive_expect_tx(full, bytes);
@@ -412,19 +451,13 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           if (v) ++v_issued; else ++k_issued;
         }
       }
-      // the next item (claimed once this one's loads are all issued)
-      unsigned nw = 0;
-      if (lane == 0) nw = atomicAdd(a.sched, 1u) + gridDim.x;
-      w = __shfl_sync(0xffffffffu, nw, 0);
     }
+    if (!ok && lane == 0) abort_cta();
     // the last fills land before the CTA can end (bounded)
     for (int r = max(0, k_issued - kPfStages); r < k_issued; ++r)
       mbar_wait_bounded(&k_full[r % kPfStages], (r / kPfStages) & 1);
     for (int r = max(0, v_issued - kPfStages); r < v_issued; ++r)
       mbar_wait_bounded(&v_full[r % kPfStages], (r / kPfStages) & 1);
-#pragma unroll
-    for (int g = 0; g < kPfGroups; ++g)
-      if (ig[g] > 0) mbar_wait_bounded(&q_full[g], (ig[g] - 1) & 1);
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
@@ -458,41 +491,87 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       // j when the softmax sees S_g(j+1)).  The next item's first product
       // into O (no accumulate) comes after the softmax's first P of that
       // item, which the softmax writes only once it has read the previous O.
+      // Group 0 (the earlier query rows) needs no more KV tiles than group
+      // 1: once its last product of an item is issued, group 0's first S of
+      // the next item is issued as soon as that item, its query tile and its
+      // first keys are there, so group 0's softmax starts on the next item
+      // while group 1 finishes this one.
       int it = 0, ring0 = 0, ig[kPfGroups] = {0, 0}, tcnt[kPfGroups] = {0, 0};
+      PfItem nx;
+      bool have_nx = false;   // the next item is read already
+      bool early = false;     // ... and group 0's first S of it issued
       bool ok = true;
       while (ok) {
-        const int slot = it & 1;
-        ok = mbar_wait_bounded(&item_full[slot], (it >> 1) & 1);
-        if (!ok) break;
-        const int4 d = items[slot];
-        mbar_arrive(&item_empty[slot]);
-        ++it;
-        if (d.w < 0) break;
-        const PfItem item = pf_item(a, d);
+        PfItem item;
+        if (have_nx) {
+          item = nx;
+          have_nx = false;
+        } else {
+          const int slot = it & 1;
+          ok = mbar_wait_bounded(&item_full[slot], (it >> 1) & 1);
+          if (!ok) break;
+          item = items[slot];
+          mbar_arrive(&item_empty[slot]);
+          ++it;
+        }
+        if (item.kind < 0) break;
         if (item.ntiles == 0) continue;
+        const bool pre = early;
+        early = false;
         ok = mbar_wait_bounded(&k_full[ring0 % kPfStages], (ring0 / kPfStages) & 1);
 #pragma unroll
         for (int g = 0; g < kPfGroups; ++g)
-          if (ok && item.nt[g] > 0) ok = mbar_wait_bounded(&q_full[g], ig[g] & 1);
-        if (!ok || *(volatile int *)abort_flag) {
+          if (ok && item.nt[g] > 0 && !(g == 0 && pre)) ok = mbar_wait_bounded(&q_full[g], ig[g] & 1);
+        if (!ok || aborted()) {
           ok = false;
           break;
         }
         tc_fence_after();
 #pragma unroll
         for (int g = 0; g < kPfGroups; ++g) {
-          if (item.nt[g] == 0) continue;
+          if (item.nt[g] == 0 || (g == 0 && pre)) continue;
           issue_s(g, ring0);
           if (item.nt[g] == 1) umma_commit(&q_empty[g]);  // the group's last S of the item
         }
         umma_commit(&k_empty[ring0 % kPfStages]);
+        const int ring_next = ring0 + item.ntiles;
+        // group 0's first S of the next item, if everything it reads is
+        // there (never waits)
+        auto try_early = [&]() {
+          if (early) return;
+          if (!have_nx) {
+            const int slot = it & 1;
+            if (!mbar_test_wait(&item_full[slot], (it >> 1) & 1)) return;
+            nx = items[slot];
+            mbar_arrive(&item_empty[slot]);
+            ++it;
+            have_nx = true;
+          }
+          if (nx.kind != 1) return;
+          if (!mbar_test_wait(&k_full[ring_next % kPfStages], (ring_next / kPfStages) & 1) ||
+              !mbar_test_wait(&q_full[0], (ig[0] + 1) & 1))
+            return;
+          tc_fence_after();
+          issue_s(0, ring_next);
+          if (nx.nt[0] == 1) umma_commit(&q_empty[0]);
+          early = true;
+        };
         for (int j = 0; ok && j < item.ntiles; ++j) {
           const int ring = ring0 + j;
           bool v_ready = false, k_ready = false;
 #pragma unroll
           for (int g = 0; g < kPfGroups; ++g) {
             if (!ok || j >= item.nt[g]) continue;
-            ok = mbar_wait_bounded(&p_full[g], tcnt[g] & 1) && !*(volatile int *)abort_flag;
+            if (g == 1 && j + 1 >= item.nt[0]) {
+              // group 0 is done with this item: look for its next one while
+              // group 1's P is not there yet
+              const unsigned long long t0 = global_timer_ns();
+              while (!mbar_test_wait(&p_full[1], tcnt[1] & 1)) {
+                try_early();
+                if (global_timer_ns() - t0 > kWaitLimitNs) break;
+              }
+            }
+            ok = mbar_wait_bounded(&p_full[g], tcnt[g] & 1) && !aborted();
             ++tcnt[g];
             if (!ok) break;
             if (!v_ready) {
@@ -518,7 +597,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           umma_commit(&v_empty[ring % kPfStages]);
           if (j + 1 < item.ntiles) umma_commit(&k_empty[(ring + 1) % kPfStages]);
         }
-        ring0 += item.ntiles;
+        ring0 = ring_next;
 #pragma unroll
         for (int g = 0; g < kPfGroups; ++g) ig[g] += item.nt[g] > 0;
       }
@@ -550,13 +629,12 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         ok = false;
         break;
       }
-      const int4 d = items[slot];
+      const PfItem item = items[slot];
       __syncwarp();
       if (lane == 0) mbar_arrive(&item_empty[slot]);
       ++it;
-      if (d.w < 0) break;
-      const PfItem item = pf_item(a, d);
-      const int my_tiles = g == 0 ? item.nt[0] : item.nt[1];
+      if (item.kind < 0) break;
+      const int my_tiles = nt_of(item, g);
       if (my_tiles == 0) {
         ring0 += item.ntiles;
         continue;
@@ -568,7 +646,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       for (int j = 0; j < my_tiles; ++j) {
         ok = mbar_wait_bounded(&s_full[g], tcnt & 1);
         ++tcnt;
-        if (!__all_sync(0xffffffffu, ok) || *(volatile int *)abort_flag) {
+        if (!__all_sync(0xffffffffu, ok) || aborted()) {
           ok = false;
           break;
         }
@@ -669,7 +747,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       if (!ok) break;
       ok = mbar_wait_bounded(&o_done[g], ig & 1);
       ++ig;
-      if (!__all_sync(0xffffffffu, ok) || *(volatile int *)abort_flag) {
+      if (!__all_sync(0xffffffffu, ok) || aborted()) {
         ok = false;
         break;
       }
