@@ -351,6 +351,8 @@ def kernel_name(cfg, mode):
     P, _, kern = pkv.pkv_decode_plan(cfg.B, cfg.H, cfg.KVH, cfg.D, cfg.bs, cfg.table_width,
                                      dtype=cfg.dtype)
     t = {torch.bfloat16: "bf16", torch.float16: "fp16", torch.float32: "fp32"}[cfg.dtype]
+    if kern == 2:  # the fused step on this kernel is pkv_write followed by it
+        return f"pkv_decode_wide_kernel<{cfg.D}, {t}>"
     base = f"pkv_decode_tc_kernel<{cfg.D}, {t}" if kern == 1 else f"pkv_decode_simt_kernel<{t}"
     return base + (", append>" if mode == "fused" else ">")
 

@@ -176,8 +176,12 @@ PKV_API size_t pkv_decode_workspace_size(int B, int H, int num_kv_heads, int hea
  * Supported: H % num_kv_heads == 0; head_dim a multiple of 8 in [8, 512] (fp32:
  * a multiple of 4); block_size >= 1; q, out, caches 16-byte aligned.  bf16 /
  * fp16 with head_dim in {64, 128, 192, 256} and block_size a multiple of 16
- * run the tensor-core kernel; every other supported shape runs the
- * CUDA-core kernel.
+ * run a tensor-core kernel: groups of exactly 16 query heads per KV head at
+ * head_dim 128 or 256 (MQA-like) the wide-group kernel (persistent, one CTA
+ * per SM claiming (sequence, KV head, partition) items from a device
+ * counter; 5th-generation tensor cores with the KV tile's tokens as the
+ * product's M), the others the TMA + mma.sync kernel; every other supported
+ * shape runs the CUDA-core kernel.
  * Errors: PKV_ERR_INVALID_ARG, PKV_ERR_UNSUPPORTED, PKV_ERR_WORKSPACE,
  * PKV_ERR_CUDA.  B == 0 enqueues nothing.
  */
@@ -247,9 +251,11 @@ PKV_API pkv_status pkv_decode_attention_static(void *out, const void *q, const v
  * first part and raises PKV_FLAG_APPEND_MISMATCH when it does not hold.
  * The launch that reads position n-1 takes the new token's K/V from k/v
  * directly, so it does not wait for its own cache write; one CTA per
- * (sequence, KV head) writes the cache row.  The cache ends bit-identical
- * to pkv_write's; the output is bit-identical to pkv_write +
- * pkv_decode_attention with the same partition size.
+ * (sequence, KV head) writes the cache row.  (Shapes that run the
+ * wide-group kernel -- see pkv_decode_attention -- make this two launches:
+ * pkv_write's kernel, then that decode kernel, which checks the slots.)  The
+ * cache ends bit-identical to pkv_write's; the output is bit-identical to
+ * pkv_write + pkv_decode_attention with the same partition size.
  * Additional requirements: k, v, k_cache, v_cache 16-byte aligned;
  * head_dim * element size a multiple of 16 bytes; k_token_stride and
  * v_token_stride >= num_kv_heads * head_dim and multiples of 16 bytes.
@@ -339,7 +345,8 @@ PKV_API pkv_status pkv_decode_attention_xpacked(
  * pkv_decode_attention would use for these arguments on a GPU with
  * num_sms SMs (host only, no CUDA call; for tests and tuning).  Returns the
  * partition size in tokens (>= 16), or 0 for invalid sizes; *kernel is set to
- * 1 for the tensor-core kernel, 0 for the CUDA-core kernel.
+ * 2 for the wide-group tensor-core kernel, 1 for the TMA + mma.sync
+ * tensor-core kernel, 0 for the CUDA-core kernel.
  */
 PKV_API int pkv_decode_plan(int B, int H, int num_kv_heads, int head_dim, int block_size,
                             int max_blocks, int max_context_len, int partition_size,

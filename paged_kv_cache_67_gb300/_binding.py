@@ -184,7 +184,7 @@ def pkv_decode_workspace_size(B, H, num_kv_heads, head_dim, block_size, max_bloc
 def pkv_decode_plan(B, H, num_kv_heads, head_dim, block_size, max_blocks, max_context_len=0,
                     partition_size=0, dtype=torch.bfloat16, num_sms=152):
     """(partition_size, max_partitions, kernel) the library would use
-    (kernel 1 = TMA/tensor-core, 0 = CUDA-core); host only."""
+    (kernel 2 = wide-group tcgen05, 1 = TMA/tensor-core, 0 = CUDA-core); host only."""
     mp, kern = ctypes.c_int(0), ctypes.c_int(0)
     P = load_library().pkv_decode_plan(B, H, num_kv_heads, head_dim, block_size, max_blocks,
                                        max_context_len, partition_size, _DT[dtype], num_sms,

@@ -51,7 +51,7 @@ static int tc_stages(int D) { return D <= 64 ? 6 : (D <= 128 ? 3 : (D <= 192 ? 2
 
 bool make_plan(int B, int H, int KVH, int D, int bs, int max_blocks, int max_context_len,
                int partition_size, pkv_dtype dt, int num_sms, size_t smem_optin, bool aligned16,
-               DecodePlan *plan) {
+               DecodePlan *plan, bool allow_wide) {
   if (B < 0 || H <= 0 || KVH <= 0 || H % KVH != 0 || D <= 0 || D > 512 || bs <= 0 ||
       max_blocks < 0 || partition_size < 0 || partition_size % 16 != 0 || max_context_len < 0)
     return false;
@@ -89,6 +89,25 @@ bool make_plan(int B, int H, int KVH, int D, int bs, int max_blocks, int max_con
   p.max_parts = (int)(mp < 1 ? 1 : mp);
   p.stages = p.kernel ? tc_stages(D) : 0;
   p.smem_bytes = p.kernel ? tc_smem_bytes(D, p.stages) : simt_smem_bytes(D, p.heads_per_cta);
+  // Groups of exactly 16 query heads with D = 128 or 256 (MQA-like): the
+  // persistent kernel with tokens as the product's M; work items of at least
+  // 512 tokens (the automatic floor keeps them within the workspace).
+  if (allow_wide && p.kernel == 1 && G == 16 && (D == 128 || D == 256) &&
+      wide_smem_bytes(D) <= (smem_optin > 0 ? smem_optin : kDefaultSmemOptin)) {
+    p.kernel = 2;
+    p.heads_per_cta = 16;
+    p.gchunks = 1;
+    if (partition_size == 0) {
+      int P = 512;
+      const int floor_p = auto_partition_floor(cap);
+      if (P < floor_p) P = floor_p;
+      if (P > cap) P = round_up(cap, 16);
+      p.P = P;
+      p.max_parts = (int)((cap + P - 1) / P);
+    }
+    p.stages = 0;
+    p.smem_bytes = wide_smem_bytes(D);
+  }
   *plan = p;
   return true;
 }
@@ -220,7 +239,7 @@ static pkv_status decode_entry(void *out, const void *q, const void *k_cache, co
   if (!device_caps(&sms, &smem_optin)) return PKV_ERR_CUDA;
   DecodePlan plan;
   if (!make_plan(B, H, num_kv_heads, head_dim, block_size, max_blocks, max_context_len,
-                 partition_size, dt, sms, smem_optin, aligned16, &plan))
+                 partition_size, dt, sms, smem_optin, aligned16, &plan, !xpacked))
     return PKV_ERR_INVALID_ARG;
   if ((long long)num_kv_heads * plan.gchunks > 65535) return PKV_ERR_UNSUPPORTED;
   if (xpacked && (plan.kernel != 1 || block_size != 16 || head_dim == 192))
@@ -275,6 +294,19 @@ static pkv_status decode_entry(void *out, const void *q, const void *k_cache, co
   }
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (xpacked) return launch_decode_xpacked(a, plan, dt, s);
+  if (plan.kernel == 2) {
+    // the fused step on this kernel: the new rows are written first (one
+    // launch), the decode then reads them from the cache and checks each
+    // slot against position n - 1
+    if (app) {
+      const pkv_status st = launch_write(const_cast<void *>(k_cache), const_cast<void *>(v_cache),
+                                         app->k, app->v, app->slots, B,
+                                         app->k_stride, app->v_stride, num_blocks, block_size,
+                                         num_kv_heads, head_dim, (int)el, err_flags, s);
+      if (st != PKV_OK) return st;
+    }
+    return launch_decode_wide(a, dt, sms, s);
+  }
   return plan.kernel ? launch_decode_tc(a, plan, dt, s) : launch_decode_simt(a, plan, dt, s);
 }
 

@@ -1,0 +1,974 @@
+// pkv_decode_wide.cu -- paged decode attention for wide query groups (16
+// query heads per KV head: MQA and wide GQA) with bf16 / fp16 caches on
+// sm_103a, on the 5th-generation tensor cores with the roles of the
+// operands swapped.
+//
+// Definition (course page "P09 · Paged KV 写入 + decode attention（参考实现）",
+// section 题面速览 "decode 读" and the paged_decode_attention shape trace):
+// n = context_lens[b]; only block_tables[b, :ceil(n/bs)] is read; token t is
+// row t % bs of physical block tbl[t / bs]; exactly n tokens; query head h
+// uses KV head h / (H / KVH); fp32 scores scaled before an fp32 softmax;
+// weighted V sum cast to the output dtype.  The block-wise online softmax is
+// the one of the interview note "PagedAttention kernel: paged KV cache 与
+// block table", section 代码; its partitioned (v2) variant, section 深入原理,
+// is the split into work items, merged by log-sum-exp.
+//
+// Why swapped.  A decode query group is 16 rows at most -- below the
+// smallest M of a tensor-core product -- while a KV tile has many tokens.
+// So the products run with tokens as M:
+//   S^T [128 tokens x 16 heads]  = K_tile [128 x D] . Q_group^T [D x 16]
+//   O^T [D x 16 heads]          += V_tile^T [D x 128] . P^T [128 x 16]
+// (M = 128 tokens or 128 of the D values, N = 16 heads, accumulators in
+// tensor memory); the softmax thread of token lane t holds that token's 16
+// head scores, and the per-head max is a reduction over the 128 lanes, done
+// only when some score exceeds the running max by more than 2^8.
+//
+// Work decomposition.  A work item is (sequence, KV head, 16-head chunk,
+// partition of P tokens); the grid is persistent (at most one CTA per SM)
+// and CTAs claim items from a counter in device memory, the latest
+// partitions first, so long contexts spread over SMs and short ones fill
+// the gaps.  7 warps:
+//   warp 6     scheduler: claims items, publishes each to the CTA through a
+//              two-slot ring, loads the item's 16 query rows (TMA, 128-byte
+//              swizzle) once the last S^T of the previous item is done;
+//   warp 0     producer: per 128-token tile the tiled TMA loads of K, then
+//              of V (16-token chunks of 64-column regions, 128-byte
+//              swizzle), each into the next slot of one ring of K-or-V slots;
+//   warp 1     MMA issuer (one thread): S^T of the item's first two tiles,
+//              then per tile, once its P^T is written: O^T += V^T . P^T and
+//              the S^T two tiles ahead into the freed score buffer;
+//   warps 2-5  softmax, thread = token lane: scores from tensor memory,
+//              running max and per-lane weight sums per head, P^T written to
+//              shared memory; after the item's last tile the per-head sums
+//              are reduced and the item is finished -- output rows, or the
+//              partition's partials and, by the last partition of the
+//              sequence, the log-sum-exp merge.
+// Every wait on an mbarrier is bounded; on time-out the CTA raises
+// PKV_FLAG_TIMEOUT, lets its copies and products land (bounded) and exits.
+#include <string.h>
+
+#include <atomic>
+#include <type_traits>
+
+#include "pkv_device.cuh"
+#include "pkv_internal.h"
+#include "pkv_tcgen05.cuh"
+
+namespace pkv {
+
+constexpr int kWdTile = 128;             // tokens per KV tile (M of S^T)
+constexpr int kWdChunks = kWdTile / 16;  // 16-token chunks per tile
+constexpr int kWdHeads = 16;             // query heads per item (N)
+constexpr int kWdWarps = 7;
+constexpr int kWdThreads = 32 * kWdWarps;
+constexpr int kWdSchedWarp = 6;
+constexpr int kWdReaders = 2 + 4;        // producer, MMA thread, one lane per softmax warp
+constexpr int kWdSchedSlots = 1024;      // work counters, one per launch in flight
+constexpr int kWdRingBytes = 192 * 1024; // K-or-V slots
+
+// Work counters of the persistent launches: slot s holds (next item to claim
+// beyond the first gridDim.x, CTAs finished); the last CTA of a launch puts
+// both back to zero, so a slot is ready again for the launch after.
+__device__ unsigned g_wd_sched[2 * kWdSchedSlots];
+
+template <int D>
+struct WdShape {
+  static constexpr int kRegions = D / 64;
+  static constexpr int kRegionBytes = kWdTile * 128;            // 128 token rows x 64 elements
+  static constexpr int kTileBytes = kRegions * kRegionBytes;    // one K or V tile
+  static constexpr int kSlots = kWdRingBytes / kTileBytes;      // 3 at D = 256, 6 at D = 128
+  static constexpr int kQRegion = kWdHeads * 128;               // 16 query rows x 64 elements
+  static constexpr int kQBytes = kRegions * kQRegion;
+  static constexpr int kPRegion = kWdHeads * 128;               // P^T: 16 head rows x 64 tokens
+  static constexpr int kPBytes = 2 * kPRegion;                  // one 128-token P^T buffer
+  static constexpr int kQOff = kSlots * kTileBytes;
+  static constexpr int kPOff = kQOff + kQBytes;                 // [2]
+  static constexpr int kOOff = kPOff + 2 * kPBytes;             // [16][D] fp32 (finishing)
+  static constexpr int kMiscOff = kOOff + kWdHeads * D * 4;
+  static constexpr int kMiscBytes = 2048;   // barriers, item ring, reductions, claim tables
+  static constexpr int kSmem = kMiscOff + kMiscBytes + 1024;    // + alignment slack
+  // tensor memory: two S^T buffers (16 columns each), O^T (D / 128 blocks
+  // of 16 columns)
+  static constexpr uint32_t kTmemCols = 64;
+  static_assert(kSlots >= 3 && kSlots <= 6, "the ring has three to six slots");
+  static_assert(1168 + 2 * 65 * 4 <= kMiscBytes, "shared-memory misc area");
+  static_assert(kSmem <= 232448, "shared memory per block");
+  static_assert(32 + 16 * (D / 128) <= (int)kTmemCols, "tensor memory");
+};
+
+// One work item as every role sees it.  kind: 1 work, -1 no more items.
+struct __align__(16) WdItem {
+  int kind, b, kvh, hc;    // sequence, KV head, 16-head chunk of its group
+  int part, nparts;        // partition and partitions of the sequence
+  int t0, t1;              // the partition's tokens
+  int n, ntiles, pad0, pad1;
+};
+static_assert(sizeof(WdItem) == 48, "three 16-byte words");
+
+struct WdArgs {
+  DecodeArgs d;        // shapes, caches, workspace, flags (the merge reads these)
+  unsigned *sched;     // this launch's (next, done) counters
+  int hchunks;         // 16-head chunks per KV head (G / 16)
+  int units;           // B * KVH * hchunks
+  int check_append;    // new_slots given: check each slot against position n - 1
+};
+
+// Whether the phase with the given parity has completed (never waits).
+__device__ __forceinline__ bool wd_test_wait(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// A barrier of the 128 softmax threads on an mbarrier, with the bounded
+// wait (a thread that gave up elsewhere cannot leave the others waiting
+// forever).
+struct WdGroupSync {
+  uint64_t *bar;
+  int *phase;
+  __device__ __forceinline__ void operator()() const {
+    mbar_arrive(bar);
+    // a short wait: spin on the non-suspending test (bounded)
+    const uint32_t par = (uint32_t)(*phase) & 1u;
+    if (!wd_test_wait(bar, par)) {
+      const unsigned long long t0 = global_timer_ns();
+      while (!wd_test_wait(bar, par) && global_timer_ns() - t0 <= kWaitLimitNs) {
+      }
+    }
+    ++*phase;
+  }
+};
+
+__device__ __forceinline__ void wd_tma_4d(void *dst, const CUtensorMap *map, uint64_t *bar, int c0,
+                                          int c1, int c2, int c3, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%3, %4, %5, %6}], [%2], %7;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "r"(c3),
+      "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ void wd_tma_3d(void *dst, const CUtensorMap *map, uint64_t *bar, int c0,
+                                          int c1, int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+
+template <typename T>
+__device__ __forceinline__ unsigned short wd_bits(float x);
+template <>
+__device__ __forceinline__ unsigned short wd_bits<__nv_bfloat16>(float x) {
+  return __bfloat16_as_ushort(__float2bfloat16_rn(x));
+}
+template <>
+__device__ __forceinline__ unsigned short wd_bits<__half>(float x) {
+  return __half_as_ushort(__float2half_rn(x));
+}
+
+// Order of an item's loads through the ring: K0, K1, V0, K2, V1, K3, V2, ...,
+// V(n-1) -- keys a tile ahead of values, so the keys of tile j+2 are fetched
+// as soon as the values of tile j-1 are no longer read.
+__device__ __forceinline__ int wd_kidx(int j) { return j < 2 ? j : 2 * j - 1; }
+__device__ __forceinline__ int wd_vidx(int j, int n) { return j == n - 1 ? 2 * n - 1 : 2 * j + 2; }
+
+// The work items, numbered densely: unit u = (sequence, KV head, 16-head
+// chunk) contributes its partitions u's parts in order, units in order (an
+// empty context is one item that writes zero rows).  Consecutive claims go
+// to different CTAs, so a long context's partitions run side by side.
+__device__ __forceinline__ int wd_unit_len(const WdArgs &w, int u) {
+  const DecodeArgs &a = w.d;
+  int n = checked_len(a, u / (a.KVH * w.hchunks), false);
+  const long long reach = (long long)a.max_parts * a.P;
+  if ((long long)n > reach) n = (int)reach;  // flagged once by CTA 0
+  return n;
+}
+__device__ __forceinline__ int wd_unit_parts(const WdArgs &w, int u) {
+  if (u >= w.units) return 0;
+  const int n = wd_unit_len(w, u);
+  return n > 0 ? (n + w.d.P - 1) / w.d.P : 1;
+}
+
+__device__ __forceinline__ WdItem wd_make_item(const WdArgs &w, int u, int part) {
+  const DecodeArgs &a = w.d;
+  WdItem it;
+  memset(&it, 0, sizeof it);
+  it.b = u / (a.KVH * w.hchunks);
+  it.kvh = (u / w.hchunks) % a.KVH;
+  it.hc = u % w.hchunks;
+  it.part = part;
+  const int n = wd_unit_len(w, u);
+  it.n = n;
+  it.nparts = n > 0 ? (n + a.P - 1) / a.P : 1;
+  it.t0 = part * a.P;
+  it.t1 = min(n, it.t0 + a.P);
+  if (n == 0) {
+    it.kind = 2;  // empty context: zero output rows
+    return it;
+  }
+  it.kind = 1;
+  it.ntiles = (it.t1 - it.t0 + kWdTile - 1) / kWdTile;
+  return it;
+}
+
+// The end of one item, by the 128 softmax threads (thread ts, barrier
+// `sync`), given per head r: s_m[r] running max (log2 units), s_l[r] sum of
+// 2^(score - s_m[r]), s_o[r * D + d] the weighted V sum.  One partition:
+// the output rows s_o / s_l.  Otherwise the partials go to the workspace and
+// the partition that arrives last merges them:  M = max_p m_p,
+// L = sum_p l_p 2^(m_p - M),  out = sum_p o_p 2^(m_p - M) / L  -- the
+// weights first (into shared memory), then four output values per thread
+// and step with eight partitions' loads in flight.
+template <int D, typename T, typename Sync>
+__device__ void wd_finish(const DecodeArgs &a, int b, int head0, int part, int nparts,
+                          const float *s_m, const float *s_l, float *s_o, int *s_scratch,
+                          int *counter, int ts, Sync sync) {
+  T *out = reinterpret_cast<T *>(a.out);
+  const size_t row0 = (size_t)b * a.H + head0;
+  if (nparts == 1) {
+    for (int i = ts; i < kWdHeads * D; i += 128)
+      out[row0 * D + i] = from_f32<T>(s_o[i] / s_l[i / D]);
+    return;
+  }
+  if (ts < kWdHeads) {
+    a.ws_m[(row0 + ts) * a.max_parts + part] = s_m[ts];
+    a.ws_l[(row0 + ts) * a.max_parts + part] = s_l[ts];
+  }
+  for (int i = ts; i < kWdHeads * D / 4; i += 128) {
+    const int r = 4 * i / D, d = 4 * i - r * D;
+    *reinterpret_cast<float4 *>(a.ws_o + ((row0 + r) * a.max_parts + part) * D + d) =
+        *reinterpret_cast<const float4 *>(s_o + 4 * i);
+  }
+  // one thread publishes the item's partials (the barrier orders the
+  // group's writes before its fence), the atomic counts the partition
+  sync();
+  if (ts == 0) {
+    __threadfence();
+    const int last = atomicAdd(counter, 1) == nparts - 1;
+    if (last) __threadfence();
+    s_scratch[0] = last;
+  }
+  sync();
+  if (!s_scratch[0]) return;
+  const int warp = ts >> 5, lane = ts & 31;
+  const bool cached = kWdHeads * nparts <= kWdHeads * D;  // weights fit where s_o was
+  float *s_w = s_o;                                       // [16][nparts]
+  float *s_M = reinterpret_cast<float *>(s_scratch + 1), *s_invL = s_M + kWdHeads;
+  for (int r = warp; r < kWdHeads; r += 4) {
+    const float *pm = a.ws_m + (row0 + r) * a.max_parts, *pl = a.ws_l + (row0 + r) * a.max_parts;
+    float M = -INFINITY;
+    for (int p = lane; p < nparts; p += 32) M = fmaxf(M, __ldcg(pm + p));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    float L = 0.f;
+    for (int p = lane; p < nparts; p += 32) L += __ldcg(pl + p) * fast_exp2(__ldcg(pm + p) - M);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+    const float inv_l = 1.f / L;
+    if (cached)
+      for (int p = lane; p < nparts; p += 32) s_w[r * nparts + p] = fast_exp2(__ldcg(pm + p) - M) * inv_l;
+    if (lane == 0) {
+      s_M[r] = M;
+      s_invL[r] = inv_l;
+    }
+  }
+  sync();
+  for (int i = ts; i < kWdHeads * D / 4; i += 128) {
+    const int r = 4 * i / D, d = 4 * i - r * D;
+    const float4 *po = reinterpret_cast<const float4 *>(a.ws_o + (row0 + r) * a.max_parts * D + d);
+    const float *pm = a.ws_m + (row0 + r) * a.max_parts;
+    auto weight = [&](int p) {
+      return cached ? s_w[r * nparts + p] : fast_exp2(__ldcg(pm + p) - s_M[r]) * s_invL[r];
+    };
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    int p = 0;
+    for (; p + 8 <= nparts; p += 8) {
+      float4 v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) v[u] = __ldcg(po + (size_t)(p + u) * (D / 4));
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const float wt = weight(p + u);
+        acc.x += wt * v[u].x;
+        acc.y += wt * v[u].y;
+        acc.z += wt * v[u].z;
+        acc.w += wt * v[u].w;
+      }
+    }
+    for (; p < nparts; ++p) {
+      const float4 v = __ldcg(po + (size_t)p * (D / 4));
+      const float wt = weight(p);
+      acc.x += wt * v.x;
+      acc.y += wt * v.y;
+      acc.z += wt * v.z;
+      acc.w += wt * v.w;
+    }
+    T *o = out + (row0 + r) * D + d;
+    o[0] = from_f32<T>(acc.x);
+    o[1] = from_f32<T>(acc.y);
+    o[2] = from_f32<T>(acc.z);
+    o[3] = from_f32<T>(acc.w);
+  }
+  if (ts == 0) *counter = 0;  // every partition has arrived: ready for the next call
+}
+
+template <int D, typename T>
+__global__ void __launch_bounds__(kWdThreads, 1)
+    pkv_decode_wide_kernel(const __grid_constant__ CUtensorMap tmQ,
+                           const __grid_constant__ CUtensorMap tmK,
+                           const __grid_constant__ CUtensorMap tmV, const WdArgs w) {
+  using Sh = WdShape<D>;
+  const DecodeArgs &a = w.d;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *sm = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t *bars = reinterpret_cast<uint64_t *>(sm + Sh::kMiscOff);
+  uint64_t *slot_full = bars + 0;    // [kSlots]: a K or V tile landed
+  uint64_t *slot_empty = bars + 8;   // [kSlots]: the product that read it is done
+  uint64_t *prod_done = bars + 14;   // the producer is at an item's last tile
+  uint64_t *q_full = bars + 16;      // the item's query rows landed
+  uint64_t *q_empty = bars + 17;     // the item's last S^T is done
+  uint64_t *s_full = bars + 18;      // [2]: S^T in score buffer b
+  uint64_t *p_full = bars + 20;      // [2]: P^T written to buffer b
+  uint64_t *p_free = bars + 22;      // [2]: the O^T product that read P^T buffer b is done
+  uint64_t *o_done = bars + 24;      // the item's last O^T product is done
+  uint64_t *item_full = bars + 25;   // [2]: an item published
+  uint64_t *item_empty = bars + 27;  // [2]: every role has read it
+  uint64_t *mma_done = bars + 29;
+  uint64_t *grp_bar = bars + 30;     // the softmax warps' own barrier (128 arrivals a phase)
+  uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(bars + 31);
+  int *abort_flag = reinterpret_cast<int *>(tmem_holder + 1);
+  WdItem *items = reinterpret_cast<WdItem *>(bars + 32);            // [2] (96 bytes)
+  float *s_red = reinterpret_cast<float *>(bars + 44);              // [2][4 warps][16]
+  int *s_vote = reinterpret_cast<int *>(s_red + 2 * 4 * kWdHeads);  // [2][4]
+  float *s_m = reinterpret_cast<float *>(s_vote + 8);               // [16]
+  float *s_l = s_m + kWdHeads;                                      // [16]
+  int *s_scratch = reinterpret_cast<int *>(s_l + kWdHeads);         // [1 + 2 * 16]
+  float *s_o = reinterpret_cast<float *>(sm + Sh::kOOff);           // [16][D]
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+
+  if (tid == 0) {
+    for (int s = 0; s < Sh::kSlots; ++s) {
+      mbar_init(&slot_full[s], 1);
+      mbar_init(&slot_empty[s], 1);
+    }
+    mbar_init(q_full, 1);
+    mbar_init(q_empty, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s_full[i], 1);
+      mbar_init(&p_full[i], 128);
+      mbar_init(&p_free[i], 1);
+      mbar_init(&item_full[i], 1);
+      mbar_init(&item_empty[i], kWdReaders);
+    }
+    mbar_init(o_done, 1);
+    mbar_init(mma_done, 1);
+    mbar_init(grp_bar, 128);
+    mbar_init(prod_done, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0) tmem_alloc(tmem_holder, Sh::kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+  constexpr bool bf16 = std::is_same<T, __nv_bfloat16>::value;
+
+  auto abort_cta = [&]() {
+    raise_flag(a.err, PKV_FLAG_TIMEOUT);
+    *(volatile int *)abort_flag = 1;
+  };
+  auto aborted = [&]() { return *(volatile int *)abort_flag != 0; };
+
+  if (warp == kWdSchedWarp) {
+    // ------------------------------------------------------------ scheduler
+    if (blockIdx.x == 0) {
+      // the checks of the whole batch, once: lengths, the host's bound on
+      // them, and (fused step) each new token's slot against position n - 1
+      const long long reach = (long long)a.max_parts * a.P;
+      int over = 0;
+      for (int bb = lane; bb < a.B; bb += 32) {
+        const int n = checked_len(a, bb, true);
+        over |= (long long)n > reach;
+        if (w.check_append) {
+          const long long slot = __ldg(a.new_slots + bb);
+          if (slot >= 0) append_check(a, bb, 0, slot, n);
+        }
+      }
+      if (__any_sync(0xffffffffu, over) && lane == 0) raise_flag(a.err, PKV_FLAG_CONTEXT_OVER_HINT);
+    }
+    // The claim order: round r holds partition maxp - 1 - r of every unit
+    // that has it (the latest partitions, only long contexts have them,
+    // first); within a round the units whose partition is full come first,
+    // then those for which it is the last, partial one -- so the last items
+    // claimed are the smallest.  Items are numbered densely; per round its
+    // first item number, from a histogram of the units' partition counts (up
+    // to 64 rounds; beyond, units in order).  Up to 256 units keep their
+    // partition counts in the lanes' registers.
+    const int maxp = a.max_parts;
+    const bool by_round = maxp <= 64;
+    constexpr int kRegUnits = 8;                       // 8 x 32 units in registers
+    const bool in_regs = w.units <= 32 * kRegUnits;
+    int unit_np[kRegUnits];
+#pragma unroll
+    for (int r = 0; r < kRegUnits; ++r) unit_np[r] = in_regs ? wd_unit_parts(w, 32 * r + lane) : 0;
+    auto parts_of = [&](int base) -> int {             // the units base + lane (base a multiple of 32)
+      if (!in_regs) return wd_unit_parts(w, base + lane);
+      int v = 0;
+#pragma unroll
+      for (int r = 0; r < kRegUnits; ++r) v = (base == 32 * r) ? unit_np[r] : v;
+      return v;
+    };
+    int *s_hist = reinterpret_cast<int *>(sm + Sh::kMiscOff + 1168);  // [65], after s_scratch
+    int *s_cum = s_hist + 65;                                          // [65]
+    unsigned total = 0;
+    if (by_round) {
+      for (int i = lane; i < 65; i += 32) s_hist[i] = 0;
+      __syncwarp();
+      for (int base = 0; base < w.units; base += 32) {
+        const int np = parts_of(base);
+        if (np > 0) atomicAdd(&s_hist[np], 1);
+      }
+      __syncwarp();
+      if (lane == 0) {
+        unsigned cum = 0;
+        int with = 0;  // units with more than p partitions
+        for (int r = 0; r < maxp; ++r) {
+          const int p = maxp - 1 - r;
+          with += s_hist[p + 1];
+          s_cum[r] = (int)cum;
+          cum += (unsigned)with;
+        }
+        s_cum[maxp] = (int)cum;
+      }
+      __syncwarp();
+      total = (unsigned)s_cum[maxp];
+    } else {
+      for (int base = 0; base < w.units; base += 32) {
+        int np = parts_of(base);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) np += __shfl_xor_sync(0xffffffffu, np, o);
+        total += (unsigned)np;
+      }
+    }
+    // units in order: claims rise, so the search resumes where the last ended
+    int chunk_base = 0;
+    unsigned chunk_cum = 0;   // items of the units before chunk_base
+    unsigned k = blockIdx.x;
+    int it = 0, iq = 0;
+    bool ok = true;
+    while (true) {
+      WdItem item;
+      memset(&item, 0, sizeof item);
+      item.kind = -1;
+      if (k < total && by_round) {
+        // the round: the last whose first item number is <= k
+        const unsigned m0 = __ballot_sync(0xffffffffu, lane < maxp && (unsigned)s_cum[lane] <= k);
+        const unsigned m1 = __ballot_sync(0xffffffffu, lane + 32 < maxp && (unsigned)s_cum[lane + 32] <= k);
+        const int r = m1 ? 63 - __clz(m1) : 31 - __clz(m0);
+        const int p = maxp - 1 - r;
+        unsigned idx = k - (unsigned)s_cum[r];
+        // full partitions first (units with more than p + 1 partitions),
+        // then the units whose last partition is p
+        unsigned nfull = 0;
+        for (int base = 0; base < w.units; base += 32)
+          nfull += (unsigned)__popc(__ballot_sync(0xffffffffu, parts_of(base) > p + 1));
+        const bool want_full = idx < nfull;
+        if (!want_full) idx -= nfull;
+        for (int base = 0; base < w.units; base += 32) {
+          const int np = parts_of(base);
+          const unsigned m = __ballot_sync(0xffffffffu, want_full ? np > p + 1 : np == p + 1);
+          const unsigned c = (unsigned)__popc(m);
+          if (idx < c) {
+            item = wd_make_item(w, base + (int)__fns(m, 0, idx + 1), p);
+            break;
+          }
+          idx -= c;
+        }
+      } else if (k < total) {
+        while (true) {
+          const int np = parts_of(chunk_base);
+          int incl = np;
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+          }
+          const unsigned chunk_total = (unsigned)__shfl_sync(0xffffffffu, incl, 31);
+          if (k < chunk_cum + chunk_total) {
+            const unsigned hit = __ballot_sync(0xffffffffu, chunk_cum + (unsigned)incl > k);
+            const int src = __ffs(hit) - 1;
+            const int excl = __shfl_sync(0xffffffffu, incl - np, src);
+            item = wd_make_item(w, chunk_base + src, (int)(k - chunk_cum) - excl);
+            break;
+          }
+          chunk_cum += chunk_total;
+          chunk_base += 32;
+        }
+      }
+      const int slot = it & 1;
+      if (it >= 2) {
+        ok = __all_sync(0xffffffffu, mbar_wait_bounded(&item_empty[slot], ((it >> 1) - 1) & 1));
+        if (!ok) break;
+      }
+      if (lane == 0) {
+        items[slot] = item;
+        mbar_arrive(&item_full[slot]);
+      }
+      __syncwarp();
+      ++it;
+      if (item.kind < 0) break;
+      if (item.kind == 1) {
+        // the item's 16 query rows, once the last S^T of the previous is done
+        if (iq > 0) {
+          ok = __all_sync(0xffffffffu, mbar_wait_bounded(q_empty, (iq - 1) & 1)) && !aborted();
+          if (!ok) break;
+        }
+        if (lane == 0) mbar_arrive_expect_tx(q_full, (uint32_t)Sh::kQBytes);
+        __syncwarp();
+        const int head0 = item.kvh * a.G + item.hc * kWdHeads;
+        if (lane < Sh::kRegions)
+          wd_tma_3d(sm + Sh::kQOff + lane * Sh::kQRegion, &tmQ, q_full, 64 * lane, head0, item.b);
+        ++iq;
+      }
+      // the next item is claimed once the producer is at this one's last
+      // tile: a CTA holds one item ahead, not two, which keeps the last items
+      // for the CTAs that are free
+      ok = __all_sync(0xffffffffu, mbar_wait_bounded(prod_done, (it - 1) & 1)) && !aborted();
+      if (!ok) break;
+      unsigned nk = 0;
+      if (lane == 0) nk = atomicAdd(w.sched, 1u) + gridDim.x;
+      k = __shfl_sync(0xffffffffu, nk, 0);
+    }
+    if (!ok && lane == 0) abort_cta();
+    if (iq > 0) mbar_wait_bounded(q_full, (iq - 1) & 1);  // the last query rows land (bounded)
+  } else if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    // per tile: K into the next ring slot, then V into the one after; a slot
+    // is reused once the product that read it is done
+    const int per_tensor = kWdChunks * Sh::kRegions;     // boxes per tile (<= 32)
+    const int region = (lane % per_tensor) / kWdChunks, chunk = lane % kWdChunks;
+    const uint64_t policy = l2_evict_first_policy();
+    if (lane == 0) {
+      prefetch_tensormap(&tmK);
+      prefetch_tensormap(&tmV);
+    }
+    int it = 0, loads = 0;
+    bool ok = true;
+    while (ok) {
+      const int slot = it & 1;
+      ok = __all_sync(0xffffffffu, mbar_wait_bounded(&item_full[slot], (it >> 1) & 1));
+      if (!ok) break;
+      const WdItem item = items[slot];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&item_empty[slot]);
+      ++it;
+      if (item.kind < 0) break;
+      if (item.kind != 1) {
+        if (lane == 0) mbar_arrive(prod_done);
+        continue;
+      }
+      const int nt = item.ntiles;
+      for (int idx = 0; idx < 2 * nt && ok; ++idx) {
+        // which tile, K or V
+        int j, v;
+        if (idx == 2 * nt - 1) {
+          j = nt - 1;
+          v = 1;
+        } else if (idx < 2) {
+          j = idx;
+          v = 0;
+        } else if ((idx & 1) == 0) {
+          j = (idx - 2) >> 1;
+          v = 1;
+        } else {
+          j = (idx + 1) >> 1;
+          v = 0;
+        }
+        const int tok0 = item.t0 + j * kWdTile;
+        const int valid_chunks = min(kWdChunks, (item.t1 - tok0 + 15) >> 4);
+        const uint32_t bytes = (uint32_t)(valid_chunks * Sh::kRegions * 2048);
+        // the chunks' physical blocks (in flight during the slot wait)
+        int phys = 0;
+        if (lane < valid_chunks) phys = checked_block(a, item.b, (tok0 + 16 * lane) / a.bs);
+        phys = __shfl_sync(0xffffffffu, phys, chunk);
+        const int s = loads % Sh::kSlots, use = loads / Sh::kSlots;
+        if (use > 0) {
+          ok = __all_sync(0xffffffffu, mbar_wait_bounded(&slot_empty[s], (use - 1) & 1)) && !aborted();
+          if (!ok) break;
+        }
+        if (lane == 0) mbar_arrive_expect_tx(&slot_full[s], bytes);
+        __syncwarp();
+        if (lane < per_tensor && chunk < valid_chunks) {
+          const int t = tok0 + 16 * chunk;
+          const int lb = t / a.bs;
+          uint8_t *dst = sm + s * Sh::kTileBytes + region * Sh::kRegionBytes + chunk * 2048;
+          wd_tma_4d(dst, v ? &tmV : &tmK, &slot_full[s], region * 64, item.kvh, t - lb * a.bs, phys,
+                    policy);
+        }
+        ++loads;
+        // the scheduler may claim the next item once the last tile's loads
+        // are next (the claim's latency overlaps them)
+        if (idx == max(0, 2 * nt - 3) && lane == 0) mbar_arrive(prod_done);
+      }
+    }
+    if (!ok && lane == 0) abort_cta();
+    // the last fills land before the CTA can end (bounded)
+    for (int l = max(0, loads - Sh::kSlots); l < loads; ++l)
+      mbar_wait_bounded(&slot_full[l % Sh::kSlots], (l / Sh::kSlots) & 1);
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc_s = umma_idesc_f16(128, kWdHeads, bf16, false);       // K, Q: K-major
+      const uint32_t idesc_o = umma_idesc_f16_mn(128, kWdHeads, bf16, true, false);  // V MN-major
+      const uint32_t q_base = smem_u32(sm + Sh::kQOff), p_base = smem_u32(sm + Sh::kPOff);
+      int it = 0, loads = 0, st = 0, pt = 0, iq = 0;
+      bool ok = true;
+      while (ok) {
+        const int slot = it & 1;
+        ok = mbar_wait_bounded(&item_full[slot], (it >> 1) & 1);
+        if (!ok) break;
+        const WdItem item = items[slot];
+        mbar_arrive(&item_empty[slot]);
+        ++it;
+        if (item.kind < 0) break;
+        if (item.kind != 1) continue;
+        const int L0 = loads;   // the item's loads are L0 + wd_kidx(j) (K), L0 + wd_vidx(j, n) (V)
+        ok = mbar_wait_bounded(q_full, iq & 1) && !aborted();
+        ++iq;
+        if (!ok) break;
+        // S^T of tile j into the next score buffer
+        auto issue_s = [&](int j) -> bool {
+          const int l = L0 + wd_kidx(j), s = l % Sh::kSlots;
+          if (!mbar_wait_bounded(&slot_full[s], (l / Sh::kSlots) & 1)) return false;
+          tc_fence_after();
+          const int buf = st & 1;
+          const uint32_t kb = smem_u32(sm + s * Sh::kTileBytes);
+#pragma unroll
+          for (int k = 0; k < D / 16; ++k)
+            umma_f16(tmem + 16 * buf,
+                     umma_desc_sw128(kb + (k >> 2) * Sh::kRegionBytes + (k & 3) * 32, 16, 1024),
+                     umma_desc_sw128(q_base + (k >> 2) * Sh::kQRegion + (k & 3) * 32, 16, 1024),
+                     idesc_s, k > 0);
+          umma_commit(&s_full[buf]);
+          umma_commit(&slot_empty[s]);
+          ++st;
+          if (j == item.ntiles - 1) umma_commit(q_empty);  // the item's last S^T
+          return true;
+        };
+        ok = issue_s(0) && (item.ntiles < 2 || issue_s(1));
+        for (int j = 0; ok && j < item.ntiles; ++j) {
+          ok = mbar_wait_bounded(&p_full[pt & 1], (pt >> 1) & 1) && !aborted();
+          if (!ok) break;
+          const int l = L0 + wd_vidx(j, item.ntiles), s = l % Sh::kSlots;
+          ok = mbar_wait_bounded(&slot_full[s], (l / Sh::kSlots) & 1);
+          if (!ok) break;
+          tc_fence_after();
+          // O^T (+)= V^T . P^T, per block of 128 of the D values
+          const uint32_t vb = smem_u32(sm + s * Sh::kTileBytes), pb = p_base + (pt & 1) * Sh::kPBytes;
+#pragma unroll
+          for (int hh = 0; hh < D / 128; ++hh)
+#pragma unroll
+            for (int k = 0; k < kWdTile / 16; ++k)
+              umma_f16(tmem + 32 + 16 * hh,
+                       umma_desc_sw128(vb + 2 * hh * Sh::kRegionBytes + k * 2048, Sh::kRegionBytes, 1024),
+                       umma_desc_sw128(pb + (k >> 2) * Sh::kPRegion + (k & 3) * 32, 16, 1024),
+                       idesc_o, (j > 0 || k > 0));
+          umma_commit(&p_free[pt & 1]);
+          umma_commit(&slot_empty[s]);
+          ++pt;
+          if (j + 2 < item.ntiles) ok = issue_s(j + 2);
+          if (j == item.ntiles - 1) umma_commit(o_done);
+        }
+        loads = L0 + 2 * item.ntiles;
+      }
+      if (!ok) abort_cta();
+      umma_commit(mma_done);  // every product issued above has completed when this arrives
+      mbar_wait_bounded(mma_done, 0);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int q4 = warp & 3;                       // tensor-memory lane quarter
+    const int t = 32 * q4 + lane;                  // token lane of the tile; D lane of O^T
+    const int ts = (warp - 2) * 32 + lane;         // thread of the softmax group
+    const uint32_t lane_off = (uint32_t)(32 * q4) << 16;
+    const float sl2 = a.scale_log2;
+    T *out = reinterpret_cast<T *>(a.out);
+    int it = 0, loads = 0, tg = 0, io = 0;
+    int gphase = 0;   // phases of grp_bar this thread has passed
+    const WdGroupSync group_sync{grp_bar, &gphase};
+    bool ok = true;
+    while (true) {
+      const int slot = it & 1;
+      ok = __all_sync(0xffffffffu, mbar_wait_bounded(&item_full[slot], (it >> 1) & 1));
+      if (!ok) break;
+      const WdItem item = items[slot];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&item_empty[slot]);
+      ++it;
+      if (item.kind < 0) break;
+      const int head0 = item.kvh * a.G + item.hc * kWdHeads;
+      if (item.kind == 2) {  // empty context: zero output rows
+        for (int i = ts; i < kWdHeads * D; i += 128)
+          out[((size_t)item.b * a.H + head0) * D + i] = from_f32<T>(0.f);
+        continue;
+      }
+      if (item.kind != 1) continue;
+      const int L0 = loads;
+      float m_used[kWdHeads], l_part[kWdHeads];
+#pragma unroll
+      for (int h = 0; h < kWdHeads; ++h) {
+        m_used[h] = -INFINITY;
+        l_part[h] = 0.f;
+      }
+      for (int j = 0; j < item.ntiles; ++j, ++tg) {
+        const int buf = tg & 1;
+        ok = __all_sync(0xffffffffu, mbar_wait_bounded(&s_full[buf], (tg >> 1) & 1)) && !aborted();
+        if (!ok) break;
+        tc_fence_after();
+        float x[kWdHeads];
+        tmem_ld16(tmem + lane_off + 16 * buf, x);
+        const int tok = item.t0 + j * kWdTile + t;
+        const bool valid = tok < item.t1;
+        bool need = false;
+#pragma unroll
+        for (int h = 0; h < kWdHeads; ++h) {
+          x[h] = valid ? x[h] * sl2 : -INFINITY;
+          need |= x[h] > m_used[h] + 8.f;
+        }
+        // does any score of the tile pass its head's running max by 2^8?
+        const int par = tg & 1;
+        const int need_w = __any_sync(0xffffffffu, need);
+        if (lane == 0) s_vote[par * 4 + (warp - 2)] = need_w;
+        group_sync();
+        const bool any = s_vote[par * 4] | s_vote[par * 4 + 1] | s_vote[par * 4 + 2] | s_vote[par * 4 + 3];
+        if (any) {
+          // per-head max of the tile over the 128 token lanes
+#pragma unroll
+          for (int h = 0; h < kWdHeads; ++h) {
+            float v = x[h];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+            if (lane == 0) s_red[(par * 4 + (warp - 2)) * kWdHeads + h] = v;
+          }
+          group_sync();
+          bool moved = false;
+          float alpha[kWdHeads];
+#pragma unroll
+          for (int h = 0; h < kWdHeads; ++h) {
+            const float* r = s_red + par * 4 * kWdHeads + h;
+            const float tmax = fmaxf(fmaxf(r[0], r[kWdHeads]), fmaxf(r[2 * kWdHeads], r[3 * kWdHeads]));
+            const float m_new = tmax > m_used[h] + 8.f ? tmax : m_used[h];
+            alpha[h] = fast_exp2(m_used[h] - m_new);
+            moved |= m_new != m_used[h];
+            l_part[h] *= alpha[h];
+            m_used[h] = m_new;
+          }
+          if (moved && j > 0) {
+            // O^T holds tiles 0 .. j-1 once the product of tile j-1 is done
+            ok = __all_sync(0xffffffffu, mbar_wait_bounded(&p_free[(tg - 1) & 1], ((tg - 1) >> 1) & 1));
+            if (!ok) break;
+            tc_fence_after();
+#pragma unroll
+            for (int hh = 0; hh < D / 128; ++hh) {
+              float o[kWdHeads];
+              tmem_ld16(tmem + lane_off + 32 + 16 * hh, o);
+#pragma unroll
+              for (int h = 0; h < kWdHeads; ++h) o[h] *= alpha[h];
+              tmem_st16(tmem + lane_off + 32 + 16 * hh, o);
+            }
+          }
+        }
+        // P^T buffer: free once the product two tiles back is done
+        if (tg >= 2) {
+          ok = __all_sync(0xffffffffu, mbar_wait_bounded(&p_free[buf], ((tg - 2) >> 1) & 1));
+          if (!ok) break;
+        }
+        uint8_t *pb = sm + Sh::kPOff + buf * Sh::kPBytes + (t >> 6) * Sh::kPRegion + (t & 7) * 2;
+        const int c16 = (t & 63) >> 3;
+#pragma unroll
+        for (int h = 0; h < kWdHeads; ++h) {
+          const float p = fast_exp2(x[h] - m_used[h]);
+          l_part[h] += p;
+          *reinterpret_cast<unsigned short *>(pb + h * 128 + ((c16 ^ (h & 7)) << 4)) = wd_bits<T>(p);
+        }
+        // the tile's V rows past the partition are zeroed (they may hold
+        // anything, and 0 * NaN would poison the product)
+        const int vl = L0 + wd_vidx(j, item.ntiles);
+        if (item.t0 + (j + 1) * kWdTile > item.t1) {
+          const int vs = vl % Sh::kSlots;
+          ok = __all_sync(0xffffffffu, mbar_wait_bounded(&slot_full[vs], (vl / Sh::kSlots) & 1));
+          if (!ok) break;
+          if (!valid) {
+            uint8_t *vrow = sm + vs * Sh::kTileBytes + t * 128;
+#pragma unroll
+            for (int r = 0; r < Sh::kRegions; ++r)
+#pragma unroll
+              for (int c = 0; c < 8; ++c)
+                *reinterpret_cast<uint4 *>(vrow + r * Sh::kRegionBytes + c * 16) = make_uint4(0, 0, 0, 0);
+          }
+        }
+        fence_proxy_async_shared();  // P^T and zeroed rows before the product reads them
+        tc_fence_before();
+        mbar_arrive(&p_full[buf]);
+      }
+      if (!ok) break;
+      loads = L0 + 2 * item.ntiles;
+      // the item's end: per-head sums over the 128 lanes, O^T to shared
+      // memory, then the output rows or the partition's partials (merged by
+      // the sequence's last partition)
+      ok = __all_sync(0xffffffffu, mbar_wait_bounded(o_done, io & 1)) && !aborted();
+      ++io;
+      if (!ok) break;
+      tc_fence_after();
+#pragma unroll
+      for (int h = 0; h < kWdHeads; ++h) {
+        float v = l_part[h];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        if (lane == 0) s_red[(warp - 2) * kWdHeads + h] = v;
+      }
+#pragma unroll
+      for (int hh = 0; hh < D / 128; ++hh) {
+        float o[kWdHeads];
+        tmem_ld16(tmem + lane_off + 32 + 16 * hh, o);
+#pragma unroll
+        for (int h = 0; h < kWdHeads; ++h) s_o[h * D + 128 * hh + t] = o[h];
+      }
+      if (ts == 0) {
+#pragma unroll
+        for (int h = 0; h < kWdHeads; ++h) s_m[h] = m_used[h];
+      }
+      group_sync();
+      if (ts < kWdHeads)
+        s_l[ts] = (s_red[ts] + s_red[kWdHeads + ts]) + (s_red[2 * kWdHeads + ts] + s_red[3 * kWdHeads + ts]);
+      group_sync();
+      wd_finish<D, T>(a, item.b, head0, item.part, item.nparts, s_m, s_l, s_o, s_scratch,
+                      a.ws_cnt + (size_t)item.b * (a.KVH * w.hchunks) + item.kvh * w.hchunks + item.hc,
+                      ts, group_sync);
+      group_sync();  // shared memory free for the next item
+    }
+    if (!ok && lane == 0) abort_cta();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, Sh::kTmemCols);
+  if (tid == 0) {
+    // the last CTA of the launch puts the work counters back for the next
+    __threadfence();
+    if (atomicAdd(w.sched + 1, 1u) == gridDim.x - 1) {
+      atomicExch(w.sched, 0u);
+      atomicExch(w.sched + 1, 0u);
+    }
+  }
+}
+
+// ---------------------------------------------------------------- host side
+
+typedef CUresult (*WdEncodeFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                               const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                               const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                               CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static WdEncodeFn wd_encode_fn() {
+  static WdEncodeFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<WdEncodeFn>(p);
+  }
+  return fn;
+}
+
+// Tensor map of the [B, H, D] queries: box of 64 elements x 16 heads x 1
+// sequence, 128-byte swizzle.
+static bool encode_query_group_map(CUtensorMap *map, const void *q, pkv_dtype dt, int B, int H,
+                                   int D) {
+  WdEncodeFn fn = wd_encode_fn();
+  if (!fn) return false;
+  const cuuint64_t el = 2;
+  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)B};
+  cuuint64_t strides[2] = {D * el, (cuuint64_t)H * D * el};
+  cuuint32_t box[3] = {64, (cuuint32_t)kWdHeads, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map,
+            dt == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+            const_cast<void *>(q), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+static unsigned *wd_sched_counters() {
+  static unsigned *cached[64] = {nullptr};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
+  if (dev < 64 && cached[dev]) return cached[dev];
+  unsigned *p = nullptr;
+  if (cudaGetSymbolAddress(reinterpret_cast<void **>(&p), g_wd_sched) != cudaSuccess) return nullptr;
+  if (dev < 64) cached[dev] = p;
+  return p;
+}
+
+size_t wide_smem_bytes(int D) {
+  return D == 256 ? (size_t)WdShape<256>::kSmem : (size_t)WdShape<128>::kSmem;
+}
+
+template <int D, typename T>
+static pkv_status launch_wide_t(const WdArgs &w, const CUtensorMap &mq, const CUtensorMap &mk,
+                                const CUtensorMap &mv, int ctas, cudaStream_t stream) {
+  auto kern = pkv_decode_wide_kernel<D, T>;
+  static int configured[64] = {0};
+  if (!allow_smem(kern, WdShape<D>::kSmem, configured)) return PKV_ERR_CUDA;
+  kern<<<ctas, kWdThreads, WdShape<D>::kSmem, stream>>>(mq, mk, mv, w);
+  return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+pkv_status launch_decode_wide(const DecodeArgs &a, pkv_dtype dt, int num_sms, cudaStream_t stream) {
+  CUtensorMap mq, mk, mv;
+  if (!encode_query_group_map(&mq, a.q, dt, a.B, a.H, a.D) ||
+      !encode_cache_map(&mk, a.k_cache, dt, a.num_blocks, a.bs, a.KVH, a.D) ||
+      !encode_cache_map(&mv, a.v_cache, dt, a.num_blocks, a.bs, a.KVH, a.D))
+    return PKV_ERR_CUDA;
+  unsigned *sched = wd_sched_counters();
+  if (!sched) return PKV_ERR_CUDA;
+  // a counter slot per launch, taken in turn (launches in flight at once on
+  // one device must number fewer than kWdSchedSlots)
+  static std::atomic<unsigned> next_slot{0};
+  const unsigned slot = next_slot.fetch_add(1u) % kWdSchedSlots;
+  WdArgs w;
+  memset(&w, 0, sizeof w);
+  w.d = a;
+  w.sched = sched + 2 * slot;
+  w.hchunks = a.G / kWdHeads;
+  w.units = a.B * a.KVH * w.hchunks;
+  w.check_append = a.new_slots != nullptr;
+  // one persistent CTA per SM, never more than the items there can be
+  const long long items = (long long)w.units * a.max_parts;
+  const int ctas = (int)std::min<long long>(items, num_sms > 0 ? num_sms : 1);
+  const bool bf = dt == PKV_BF16;
+  if (a.D == 256) return bf ? launch_wide_t<256, __nv_bfloat16>(w, mq, mk, mv, ctas, stream)
+                            : launch_wide_t<256, __half>(w, mq, mk, mv, ctas, stream);
+  if (a.D == 128) return bf ? launch_wide_t<128, __nv_bfloat16>(w, mq, mk, mv, ctas, stream)
+                            : launch_wide_t<128, __half>(w, mq, mk, mv, ctas, stream);
+  return PKV_ERR_UNSUPPORTED;
+}
+
+}  // namespace pkv

@@ -13,7 +13,7 @@ namespace pkv {
 
 // Which decode kernel runs and how the context is partitioned.
 struct DecodePlan {
-  int kernel;          // 1: TMA + tensor-core kernel, 0: CUDA-core kernel
+  int kernel;          // 2: wide-group tcgen05 kernel, 1: TMA + tensor-core kernel, 0: CUDA-core kernel
   int P;               // partition size in tokens (multiple of 16)
   int max_parts;       // partitions per sequence the grid covers
   int heads_per_cta;   // query heads served by one CTA
@@ -35,7 +35,7 @@ bool tc_eligible(pkv_dtype dt, int D, int bs);
 // Fills *plan; returns false for sizes no kernel handles.
 bool make_plan(int B, int H, int KVH, int D, int bs, int max_blocks, int max_context_len,
                int partition_size, pkv_dtype dt, int num_sms, size_t smem_optin, bool aligned16,
-               DecodePlan *plan);
+               DecodePlan *plan, bool allow_wide = true);
 size_t workspace_bytes_for(int B, int H, int D, int max_parts);
 // Bytes at the start of the workspace that must be zero before a call (the
 // work queue and the per-(sequence, head group) counters).
@@ -90,5 +90,9 @@ pkv_status launch_decode_simt(const DecodeArgs &a, const DecodePlan &plan, pkv_d
                               cudaStream_t stream);
 pkv_status launch_decode_tc(const DecodeArgs &a, const DecodePlan &plan, pkv_dtype dt,
                             cudaStream_t stream);
+// Wide query groups (16 query heads per KV head, D of 128 or 256): the
+// persistent tensor-core decode with tokens as the product's M.
+size_t wide_smem_bytes(int D);
+pkv_status launch_decode_wide(const DecodeArgs &a, pkv_dtype dt, int num_sms, cudaStream_t stream);
 
 }  // namespace pkv

@@ -1,6 +1,7 @@
 // pkv_tcgen05.cuh -- wrappers for the 5th-generation tensor-core instructions
 // (tcgen05: TMEM allocation, MMA with shared-memory descriptors, commit to
-// an mbarrier, TMEM loads and stores) used by the prefill kernel.
+// an mbarrier, TMEM loads and stores) used by the prefill kernel and the
+// wide-group decode kernel.
 //
 // Operand layouts (bf16 / fp16, 128-byte swizzle, 1024-byte aligned tiles):
 //   K-major tile (A = queries or P, B = keys): rows of 64 elements (128 B),
@@ -9,12 +10,14 @@
 //     CU_TENSOR_MAP_SWIZZLE_128B.  Descriptor: stride between 8-row groups
 //     1024 B; one MMA's 16-element K step is the start address + 32 B
 //     within a region.
-//   MN-major tile (B = values: rows are tokens = K, 64 D-values per row):
-//     the same byte layout; descriptor: 1024 B between 8-row K groups
-//     (stride field) and the region size between 64-element N groups
-//     (leading field); one MMA's 16-token K step is + 2048 B.
+//   MN-major tile (values: rows are tokens = K, 64 D-values per row; as B
+//     with D as N, or as A with D as M): the same byte layout; descriptor:
+//     1024 B between 8-row K groups (stride field) and the region size
+//     between 64-element M / N groups (leading field); one MMA's 16-token K
+//     step is + 2048 B.
 // These encodings were checked on the GPU against a CPU product before any
-// kernel used them.
+// kernel used them (the MN-major A operand through the wide-group decode
+// kernel's parity tests against the oracle).
 #pragma once
 
 #include <stdint.h>
@@ -34,6 +37,12 @@ __device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t smem_addr, uint32_t
 __host__ __device__ constexpr uint32_t umma_idesc_f16(int M, int N, bool bf16, bool b_mn_major) {
   return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) |
          ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// The same with A MN-major as well (bit 15: A's M dimension contiguous).
+__host__ __device__ constexpr uint32_t umma_idesc_f16_mn(int M, int N, bool bf16, bool a_mn_major,
+                                                         bool b_mn_major) {
+  return umma_idesc_f16(M, N, bf16, b_mn_major) | ((a_mn_major ? 1u : 0u) << 15);
 }
 
 __device__ __forceinline__ void tmem_alloc(uint32_t *holder_smem, uint32_t ncols) {
@@ -83,6 +92,34 @@ __device__ __forceinline__ void umma_commit(uint64_t *bar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
           static_cast<uint32_t>(__cvta_generic_to_shared(bar)))
+      : "memory");
+}
+
+// 16 consecutive fp32 columns of this thread's TMEM lane (warp-collective;
+// the warp reads lanes 32 * (warp % 4) .. + 31), the wait for the load in
+// the same statement.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Store 16 consecutive fp32 columns of this thread's TMEM lane (warp-collective).
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};\n\t"
+      "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])), "r"(__float_as_uint(v[3])),
+      "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])), "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])),
+      "r"(__float_as_uint(v[8])), "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])), "r"(__float_as_uint(v[15]))
       : "memory");
 }
 

@@ -63,13 +63,16 @@ def test_configs_small(name, partition_size):
 @pytest.mark.parametrize("D", [64, 128, 192, 256])
 @pytest.mark.parametrize("H,KVH", [(4, 4), (8, 2), (16, 2), (32, 1), (48, 3)])
 def test_tensor_core_shapes(dtype, D, H, KVH):
-    """GQA groups of 1..32 heads (over 16: several CTAs per KV head)."""
+    """GQA groups of 1..32 heads (over 16: several CTAs per KV head; exactly 16
+    at D = 128 / 256: the wide-group kernel)."""
     lens = [1, 15, 16, 17, 33, 64, 100, 250]
     bs = 16 if D != 192 else 32
     case = random_paged_case(D + H * 7 + KVH, lens, H=H, KVH=KVH, D=D, bs=bs, dtype=dtype)
     P, _, kern = pkv.pkv_decode_plan(len(lens), H, KVH, D, bs, case["block_tables"].shape[1],
                                      dtype=dtype)
-    assert kern == 1  # TMA + tensor-core kernel
+    # groups of exactly 16 heads at D = 128 / 256 run on the wide-group
+    # kernel, the others on the TMA + mma.sync kernel
+    assert kern == (2 if H // KVH == 16 and D in (128, 256) else 1)
     args = (case["q"], case["k_cache"], case["v_cache"], case["block_tables"], case["context_lens"],
             1.0 / math.sqrt(D))
     for ps in (0, 32):
