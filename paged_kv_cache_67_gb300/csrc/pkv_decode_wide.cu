@@ -91,7 +91,7 @@ struct WdShape {
   // of 16 columns)
   static constexpr uint32_t kTmemCols = 64;
   static_assert(kSlots >= 3 && kSlots <= 6, "the ring has three to six slots");
-  static_assert(1168 + 2 * 65 * 4 <= kMiscBytes, "shared-memory misc area");
+  static_assert(1168 + 3 * 65 * 4 <= kMiscBytes, "shared-memory misc area");
   static_assert(kSmem <= 232448, "shared memory per block");
   static_assert(32 + 16 * (D / 128) <= (int)kTmemCols, "tensor memory");
 };
@@ -224,20 +224,19 @@ __device__ __forceinline__ WdItem wd_make_item(const WdArgs &w, int u, int part)
 // `sync`), given per head r: s_m[r] running max (log2 units), s_l[r] sum of
 // 2^(score - s_m[r]), s_o[r * D + d] the weighted V sum.  One partition:
 // the output rows s_o / s_l.  Otherwise the partials go to the workspace and
-// the partition that arrives last merges them:  M = max_p m_p,
-// L = sum_p l_p 2^(m_p - M),  out = sum_p o_p 2^(m_p - M) / L  -- the
-// weights first (into shared memory), then four output values per thread
-// and step with eight partitions' loads in flight.
+// thread 0 counts the partition with a release atomic whose result it reads
+// only later (wd_merge_if_last, at the next item's end): the atomic's round
+// trip is not waited for.  Returns whether a count is pending.
 template <int D, typename T, typename Sync>
-__device__ void wd_finish(const DecodeArgs &a, int b, int head0, int part, int nparts,
-                          const float *s_m, const float *s_l, float *s_o, int *s_scratch,
-                          int *counter, int ts, Sync sync) {
+__device__ bool wd_publish(const DecodeArgs &a, int b, int head0, int part, int nparts,
+                           const float *s_m, const float *s_l, const float *s_o, int *counter,
+                           int ts, Sync sync, unsigned *prev) {
   T *out = reinterpret_cast<T *>(a.out);
   const size_t row0 = (size_t)b * a.H + head0;
   if (nparts == 1) {
     for (int i = ts; i < kWdHeads * D; i += 128)
       out[row0 * D + i] = from_f32<T>(s_o[i] / s_l[i / D]);
-    return;
+    return false;
   }
   if (ts < kWdHeads) {
     a.ws_m[(row0 + ts) * a.max_parts + part] = s_m[ts];
@@ -248,20 +247,33 @@ __device__ void wd_finish(const DecodeArgs &a, int b, int head0, int part, int n
     *reinterpret_cast<float4 *>(a.ws_o + ((row0 + r) * a.max_parts + part) * D + d) =
         *reinterpret_cast<const float4 *>(s_o + 4 * i);
   }
-  // one thread publishes the item's partials (the barrier orders the
-  // group's writes before its fence), the atomic counts the partition
+  // the barrier orders the group's writes before thread 0's release
   sync();
   if (ts == 0) {
-    __threadfence();
-    const int last = atomicAdd(counter, 1) == nparts - 1;
-    if (last) __threadfence();
-    s_scratch[0] = last;
+    unsigned v;
+    asm volatile("atom.release.gpu.global.add.u32 %0, [%1], 1;"
+                 : "=r"(v)
+                 : "l"(reinterpret_cast<uint64_t>(counter))
+                 : "memory");
+    *prev = v;
   }
-  sync();
-  if (!s_scratch[0]) return;
+  return true;
+}
+
+// The merge of a (sequence, head chunk) whose partitions have all arrived,
+// by the group whose count was the last:  M = max_p m_p,
+// L = sum_p l_p 2^(m_p - M),  out = sum_p o_p 2^(m_p - M) / L -- the
+// weights first (into s_w, 16 x nparts floats when they fit in w_cap), then
+// four output values per thread and step with eight partitions' loads in
+// flight; the counter is put back to zero for the next call.
+template <int D, typename T, typename Sync>
+__device__ void wd_merge(const DecodeArgs &a, int b, int head0, int nparts, float *s_w, int w_cap,
+                         int *s_scratch, int *counter, int ts, Sync sync) {
+  T *out = reinterpret_cast<T *>(a.out);
+  const size_t row0 = (size_t)b * a.H + head0;
+  __threadfence();  // acquire: the other partitions' partials
   const int warp = ts >> 5, lane = ts & 31;
-  const bool cached = kWdHeads * nparts <= kWdHeads * D;  // weights fit where s_o was
-  float *s_w = s_o;                                       // [16][nparts]
+  const bool cached = kWdHeads * nparts <= w_cap;
   float *s_M = reinterpret_cast<float *>(s_scratch + 1), *s_invL = s_M + kWdHeads;
   for (int r = warp; r < kWdHeads; r += 4) {
     const float *pm = a.ws_m + (row0 + r) * a.max_parts, *pl = a.ws_l + (row0 + r) * a.max_parts;
@@ -335,6 +347,7 @@ __global__ void __launch_bounds__(kWdThreads, 1)
   uint64_t *slot_full = bars + 0;    // [kSlots]: a K or V tile landed
   uint64_t *slot_empty = bars + 8;   // [kSlots]: the product that read it is done
   uint64_t *prod_done = bars + 14;   // the producer is at an item's last tile
+  uint64_t *tmem_done = bars + 15;   // the softmax threads' last tensor-memory access is done
   uint64_t *q_full = bars + 16;      // the item's query rows landed
   uint64_t *q_empty = bars + 17;     // the item's last S^T is done
   uint64_t *s_full = bars + 18;      // [2]: S^T in score buffer b
@@ -375,6 +388,7 @@ __global__ void __launch_bounds__(kWdThreads, 1)
     mbar_init(mma_done, 1);
     mbar_init(grp_bar, 128);
     mbar_init(prod_done, 1);
+    mbar_init(tmem_done, 128);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -408,61 +422,86 @@ __global__ void __launch_bounds__(kWdThreads, 1)
       }
       if (__any_sync(0xffffffffu, over) && lane == 0) raise_flag(a.err, PKV_FLAG_CONTEXT_OVER_HINT);
     }
-    // The claim order: round r holds partition maxp - 1 - r of every unit
-    // that has it (the latest partitions, only long contexts have them,
-    // first); within a round the units whose partition is full come first,
-    // then those for which it is the last, partial one -- so the last items
-    // claimed are the smallest.  Items are numbered densely; per round its
-    // first item number, from a histogram of the units' partition counts (up
-    // to 64 rounds; beyond, units in order).  Up to 256 units keep their
-    // partition counts in the lanes' registers.
+    // The claim order, numbered densely: first every full partition (P
+    // tokens) -- round r holds partition maxp - 1 - r of the units long
+    // enough, so the latest partitions, only long contexts have them, go
+    // first -- then every unit's last, partial partition (or its empty
+    // context) by its tile count, most first: the last items claimed are the
+    // smallest.  The first item number of each round and of each tile
+    // count comes from histograms of the units' lengths in shared memory (up
+    // to 64 rounds and 63 tile counts; beyond, units in order).  Up to 256
+    // units keep their lengths in the lanes' registers.
     const int maxp = a.max_parts;
-    const bool by_round = maxp <= 64;
-    constexpr int kRegUnits = 8;                       // 8 x 32 units in registers
+    const int tmax = (a.P + kWdTile - 1) / kWdTile;     // tiles of a full partition
+    const bool sorted = maxp <= 64 && tmax <= 63;
+    constexpr int kRegUnits = 8;                        // 8 x 32 units in registers
     const bool in_regs = w.units <= 32 * kRegUnits;
-    int unit_np[kRegUnits];
+    int unit_n[kRegUnits];
 #pragma unroll
-    for (int r = 0; r < kRegUnits; ++r) unit_np[r] = in_regs ? wd_unit_parts(w, 32 * r + lane) : 0;
-    auto parts_of = [&](int base) -> int {             // the units base + lane (base a multiple of 32)
-      if (!in_regs) return wd_unit_parts(w, base + lane);
-      int v = 0;
+    for (int r = 0; r < kRegUnits; ++r) {
+      const int u = 32 * r + lane;
+      unit_n[r] = (in_regs && u < w.units) ? wd_unit_len(w, u) : -1;
+    }
+    auto len_of = [&](int base) -> int {              // unit base + lane's length, -1 past the end
+      if (!in_regs) return base + lane < w.units ? wd_unit_len(w, base + lane) : -1;
+      int v = -1;
 #pragma unroll
-      for (int r = 0; r < kRegUnits; ++r) v = (base == 32 * r) ? unit_np[r] : v;
+      for (int r = 0; r < kRegUnits; ++r) v = (base == 32 * r) ? unit_n[r] : v;
       return v;
     };
-    int *s_hist = reinterpret_cast<int *>(sm + Sh::kMiscOff + 1168);  // [65], after s_scratch
-    int *s_cum = s_hist + 65;                                          // [65]
-    unsigned total = 0;
-    if (by_round) {
-      for (int i = lane; i < 65; i += 32) s_hist[i] = 0;
+    auto full_parts = [&](int n) { return n > 0 ? n / a.P : 0; };
+    // the tile count of a unit's partial item: 1..tmax, 0 for an empty
+    // context, -1 for none (the context is whole partitions)
+    auto part_tiles = [&](int n) {
+      if (n < 0) return -1;
+      if (n == 0) return 0;
+      const int rem = n % a.P;
+      return rem == 0 ? -1 : (rem + kWdTile - 1) / kWdTile;
+    };
+    int *s_histA = reinterpret_cast<int *>(sm + Sh::kMiscOff + 1168);  // [65], after s_scratch
+    int *s_cumA = s_histA + 65;   // [65] first item number of each round
+    int *s_cumB = s_cumA + 65;    // [65] first item number of each tile count
+    unsigned total = 0, total_full = 0;
+    if (sorted) {
+      for (int i = lane; i < 3 * 65; i += 32) s_histA[i] = 0;
       __syncwarp();
       for (int base = 0; base < w.units; base += 32) {
-        const int np = parts_of(base);
-        if (np > 0) atomicAdd(&s_hist[np], 1);
+        const int n = len_of(base);
+        const int f = full_parts(n);
+        if (f > 0) atomicAdd(&s_histA[f], 1);   // units with f full partitions
+        const int t = part_tiles(n);
+        if (t >= 0) atomicAdd(&s_cumB[t], 1);   // partial items of t tiles (in place)
       }
       __syncwarp();
       if (lane == 0) {
         unsigned cum = 0;
-        int with = 0;  // units with more than p partitions
+        int with = 0;  // units with a full partition p
         for (int r = 0; r < maxp; ++r) {
-          const int p = maxp - 1 - r;
-          with += s_hist[p + 1];
-          s_cum[r] = (int)cum;
+          with += s_histA[maxp - r];
+          s_cumA[r] = (int)cum;
           cum += (unsigned)with;
         }
-        s_cum[maxp] = (int)cum;
+        s_cumA[maxp] = (int)cum;
+        for (int t = tmax; t >= 0; --t) {
+          const int h = s_cumB[t];
+          s_cumB[t] = (int)cum;
+          cum += (unsigned)h;
+        }
+        s_histA[0] = (int)cum;  // the total
       }
       __syncwarp();
-      total = (unsigned)s_cum[maxp];
+      total_full = (unsigned)s_cumA[maxp];
+      total = (unsigned)s_histA[0];
     } else {
       for (int base = 0; base < w.units; base += 32) {
-        int np = parts_of(base);
+        const int n = len_of(base);
+        int np = n < 0 ? 0 : (n > 0 ? (n + a.P - 1) / a.P : 1);
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) np += __shfl_xor_sync(0xffffffffu, np, o);
         total += (unsigned)np;
       }
     }
-    // units in order: claims rise, so the search resumes where the last ended
+    // units in order (no sort): claims rise, so the search resumes
     int chunk_base = 0;
     unsigned chunk_cum = 0;   // items of the units before chunk_base
     unsigned k = blockIdx.x;
@@ -472,33 +511,43 @@ __global__ void __launch_bounds__(kWdThreads, 1)
       WdItem item;
       memset(&item, 0, sizeof item);
       item.kind = -1;
-      if (k < total && by_round) {
-        // the round: the last whose first item number is <= k
-        const unsigned m0 = __ballot_sync(0xffffffffu, lane < maxp && (unsigned)s_cum[lane] <= k);
-        const unsigned m1 = __ballot_sync(0xffffffffu, lane + 32 < maxp && (unsigned)s_cum[lane + 32] <= k);
-        const int r = m1 ? 63 - __clz(m1) : 31 - __clz(m0);
-        const int p = maxp - 1 - r;
-        unsigned idx = k - (unsigned)s_cum[r];
-        // full partitions first (units with more than p + 1 partitions),
-        // then the units whose last partition is p
-        unsigned nfull = 0;
-        for (int base = 0; base < w.units; base += 32)
-          nfull += (unsigned)__popc(__ballot_sync(0xffffffffu, parts_of(base) > p + 1));
-        const bool want_full = idx < nfull;
-        if (!want_full) idx -= nfull;
-        for (int base = 0; base < w.units; base += 32) {
-          const int np = parts_of(base);
-          const unsigned m = __ballot_sync(0xffffffffu, want_full ? np > p + 1 : np == p + 1);
-          const unsigned c = (unsigned)__popc(m);
-          if (idx < c) {
-            item = wd_make_item(w, base + (int)__fns(m, 0, idx + 1), p);
-            break;
+      if (k < total && sorted) {
+        // the idx-th unit (in unit order) satisfying `pred`, made an item
+        auto pick = [&](unsigned idx, auto pred, auto part_of) {
+          for (int base = 0; base < w.units; base += 32) {
+            const int n = len_of(base);
+            const unsigned m = __ballot_sync(0xffffffffu, pred(n));
+            const unsigned c = (unsigned)__popc(m);
+            if (idx < c) {
+              const int src = (int)__fns(m, 0, idx + 1);
+              const int nn = __shfl_sync(0xffffffffu, n, src);
+              item = wd_make_item(w, base + src, part_of(nn));
+              return;
+            }
+            idx -= c;
           }
-          idx -= c;
+        };
+        if (k < total_full) {
+          // the round: the last whose first item number is <= k
+          const unsigned m0 = __ballot_sync(0xffffffffu, lane < maxp && (unsigned)s_cumA[lane] <= k);
+          const unsigned m1 = __ballot_sync(0xffffffffu, lane + 32 < maxp && (unsigned)s_cumA[lane + 32] <= k);
+          const int r = m1 ? 63 - __clz(m1) : 31 - __clz(m0);
+          const int p = maxp - 1 - r;
+          pick(k - (unsigned)s_cumA[r], [&](int n) { return full_parts(n) > p; }, [&](int) { return p; });
+        } else {
+          // the tile count: the last class whose first item number is <= k
+          // (class c holds tile count tmax - c; s_cumB is indexed by count)
+          const unsigned m0 = __ballot_sync(0xffffffffu, lane <= tmax && (unsigned)s_cumB[tmax - lane] <= k);
+          const unsigned m1 = __ballot_sync(0xffffffffu, lane + 32 <= tmax && (unsigned)s_cumB[tmax - lane - 32] <= k);
+          const int c = m1 ? 63 - __clz(m1) : 31 - __clz(m0);
+          const int t = tmax - c;
+          pick(k - (unsigned)s_cumB[t], [&](int n) { return part_tiles(n) == t; },
+               [&](int n) { return n > 0 ? n / a.P : 0; });
         }
       } else if (k < total) {
         while (true) {
-          const int np = parts_of(chunk_base);
+          const int n = len_of(chunk_base);
+          const int np = n < 0 ? 0 : (n > 0 ? (n + a.P - 1) / a.P : 1);
           int incl = np;
 #pragma unroll
           for (int o = 1; o < 32; o <<= 1) {
@@ -698,6 +747,11 @@ __global__ void __launch_bounds__(kWdThreads, 1)
       mbar_wait_bounded(mma_done, 0);
     }
     __syncwarp();
+    // the tensor memory is freed as soon as no product and no softmax thread
+    // uses it any more (the softmax threads' last merge and stores go on)
+    mbar_wait_bounded(tmem_done, 0);
+    tc_fence_after();
+    tmem_dealloc(tmem, Sh::kTmemCols);
   } else {
     // ------------------------------------------------------------ softmax
     const int q4 = warp & 3;                       // tensor-memory lane quarter
@@ -709,6 +763,23 @@ __global__ void __launch_bounds__(kWdThreads, 1)
     int it = 0, loads = 0, tg = 0, io = 0;
     int gphase = 0;   // phases of grp_bar this thread has passed
     const WdGroupSync group_sync{grp_bar, &gphase};
+    // a partition count still in flight (thread 0 holds the atomic's result)
+    bool pend = false;
+    int pend_b = 0, pend_head0 = 0, pend_nparts = 0;
+    int *pend_cnt = nullptr;
+    unsigned pend_prev = 0;
+    // the pending count's result: the last partition merges (the weights go
+    // to the P^T buffers, free between items)
+    auto settle = [&]() {
+      if (!pend) return;
+      if (ts == 0) s_scratch[0] = pend_prev == (unsigned)(pend_nparts - 1);
+      group_sync();
+      if (s_scratch[0])
+        wd_merge<D, T>(a, pend_b, pend_head0, pend_nparts, reinterpret_cast<float *>(sm + Sh::kPOff),
+                       2 * Sh::kPBytes / 4, s_scratch, pend_cnt, ts, group_sync);
+      group_sync();
+      pend = false;
+    };
     bool ok = true;
     while (true) {
       const int slot = it & 1;
@@ -855,17 +926,25 @@ __global__ void __launch_bounds__(kWdThreads, 1)
       if (ts < kWdHeads)
         s_l[ts] = (s_red[ts] + s_red[kWdHeads + ts]) + (s_red[2 * kWdHeads + ts] + s_red[3 * kWdHeads + ts]);
       group_sync();
-      wd_finish<D, T>(a, item.b, head0, item.part, item.nparts, s_m, s_l, s_o, s_scratch,
-                      a.ws_cnt + (size_t)item.b * (a.KVH * w.hchunks) + item.kvh * w.hchunks + item.hc,
-                      ts, group_sync);
+      settle();  // the previous item's merge, if it was the last partition
+      int *cnt = a.ws_cnt + (size_t)item.b * (a.KVH * w.hchunks) + item.kvh * w.hchunks + item.hc;
+      if (wd_publish<D, T>(a, item.b, head0, item.part, item.nparts, s_m, s_l, s_o, cnt, ts,
+                           group_sync, &pend_prev)) {
+        pend = true;
+        pend_b = item.b;
+        pend_head0 = head0;
+        pend_nparts = item.nparts;
+        pend_cnt = cnt;
+      }
       group_sync();  // shared memory free for the next item
     }
+    tc_fence_before();
+    mbar_arrive(tmem_done);  // no tensor-memory access after this
+    if (ok) settle();        // the last item's merge, if it was the last partition
     if (!ok && lane == 0) abort_cta();
   }
 
-  tc_fence_before();
   __syncthreads();
-  if (warp == 0) tmem_dealloc(tmem, Sh::kTmemCols);
   if (tid == 0) {
     // the last CTA of the launch puts the work counters back for the next
     __threadfence();
