@@ -96,7 +96,7 @@ struct PfShape {
   static constexpr int kQOff = 0;                               // [group]
   static constexpr int kKVOff = kQOff + kPfGroups * kQBytes;    // [stage][K, V]
   static constexpr int kBarOff = kKVOff + kPfStages * 2 * kKVBytes;
-  static constexpr int kSmem = kBarOff + 512 + 1024;            // + alignment slack
+  static constexpr int kSmem = kBarOff + 1024 + 1024;           // barriers, item ring, claim table; + alignment slack
   // tensor memory, 256 columns per group: S (128 fp32 columns; P, 128
   // tokens as 64 packed columns, is written over its first half once S is
   // read), O (D fp32 columns)
@@ -338,6 +338,92 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     if (__any_sync(0xffffffffu, bad) && lane == 0) raise_flag(a.err, PKV_FLAG_QUERY_LEN);
     if (__any_sync(0xffffffffu, over) && lane == 0) raise_flag(a.err, PKV_FLAG_QUERY_OVER_HINT);
     const unsigned total = (unsigned)pairs * (unsigned)a.H;
+    // The claim order: pairs (sequence, 256-query tile) by their KV tiles,
+    // most first (a chunk on a long cached prefix is heavy even at tile 0),
+    // then sequence and tile; each pair's heads one after another.  The
+    // first item number of each tile-count class comes from a histogram in
+    // shared memory (64 classes, 63 tiles and more together); batches with
+    // more than 4096 (sequence, tile) slots keep the order of pf_pair.
+    auto pair_tiles = [&](int ql, int n, int t) {
+      const int i0 = t * kCtaRows;
+      const int rows = min(kCtaRows, ql - i0);
+      const int p_first = n - ql + i0;
+      const int nt0 = (p_first + min(kPfRows, rows) - 1) / kPfTile + 1;
+      const int rows1 = rows - kPfRows;
+      const int nt1 = rows1 > 0 ? (p_first + kPfRows + rows1 - 1) / kPfTile + 1 : 0;
+      return max(nt0, nt1);
+    };
+    auto pair_class = [&](int bb, int ql, int t) {  // 0 heaviest .. 63 lightest or invalid
+      if (!pf_seq_ok(a, bb, ql)) return 63;
+      return 63 - min(63, pair_tiles(ql, __ldg(a.lens + bb), t));
+    };
+    const bool by_work = (long long)a.B * a.q_tiles <= 4096;
+    int *s_cls = reinterpret_cast<int *>(sm + Sh::kBarOff + 512);  // [65]
+    if (by_work) {
+      for (int i = lane; i < 65; i += 32) s_cls[i] = 0;
+      __syncwarp();
+      for (int bb = lane; bb < a.B; bb += 32) {
+        const int ql = __ldg(a.cu_q + bb + 1) - __ldg(a.cu_q + bb);
+        const int tl = ql > 0 ? min(a.q_tiles, (ql + kCtaRows - 1) / kCtaRows) : 0;
+        for (int t = 0; t < tl; ++t) atomicAdd(&s_cls[pair_class(bb, ql, t)], 1);
+      }
+      __syncwarp();
+      if (lane == 0) {
+        int cum = 0;
+        for (int c = 0; c < 64; ++c) {
+          const int hcount = s_cls[c];
+          s_cls[c] = cum;
+          cum += hcount;
+        }
+        s_cls[64] = cum;
+      }
+      __syncwarp();
+    }
+    // the pr-th pair of the claim order (warp-uniform)
+    auto pair_of = [&](int pr, int *b_out, int *qt_out) {
+      if (!by_work) {
+        pf_pair(a, pr, lane, b_out, qt_out);
+        return;
+      }
+      const unsigned m0 = __ballot_sync(0xffffffffu, s_cls[lane] <= pr);
+      const unsigned m1 = __ballot_sync(0xffffffffu, s_cls[lane + 32] <= pr);
+      const int c = m1 ? 63 - __clz(m1) : 31 - __clz(m0);
+      int idx = pr - s_cls[c];
+      *b_out = -1;
+      *qt_out = 0;
+      for (int base = 0; base < a.B; base += 32) {
+        const int bb = base + lane;
+        int cnt = 0, ql = 0, tl = 0;
+        if (bb < a.B) {
+          ql = __ldg(a.cu_q + bb + 1) - __ldg(a.cu_q + bb);
+          tl = ql > 0 ? min(a.q_tiles, (ql + kCtaRows - 1) / kCtaRows) : 0;
+          for (int t = 0; t < tl; ++t) cnt += pair_class(bb, ql, t) == c;
+        }
+        int incl = cnt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += y;
+        }
+        const int chunk = __shfl_sync(0xffffffffu, incl, 31);
+        if (idx < chunk) {
+          const int src = __ffs(__ballot_sync(0xffffffffu, incl > idx)) - 1;
+          int t_hit = 0;
+          if (lane == src) {
+            int k = idx - (incl - cnt);
+            for (int t = 0; t < tl; ++t)
+              if (pair_class(bb, ql, t) == c && k-- == 0) {
+                t_hit = t;
+                break;
+              }
+          }
+          *b_out = base + src;
+          *qt_out = __shfl_sync(0xffffffffu, t_hit, src);
+          return;
+        }
+        idx -= chunk;
+      }
+    };
     // claim items (CTA c starts with item c, then takes the next unclaimed
     // one), publish each to the CTA as soon as a ring slot is free, and load
     // its query tiles once the products that read the previous ones are done
@@ -348,7 +434,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       PfItem item = pf_item(a, -1, 0, -1, 0);
       if (w < total) {
         int bb, qq;
-        pf_pair(a, (int)(w / (unsigned)a.H), lane, &bb, &qq);
+        pair_of((int)(w / (unsigned)a.H), &bb, &qq);
         const int hh = (int)(w % (unsigned)a.H);
         if (bb < 0) {
           item = pf_item(a, 0, hh, bb, qq);
