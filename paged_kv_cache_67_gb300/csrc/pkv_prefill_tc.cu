@@ -16,8 +16,9 @@
 // "PagedAttention kernel: paged KV cache 与 block table", section 代码.
 //
 // Work decomposition.  A work item is (query head, sequence, 256 queries):
-// two 128-query tiles that share every K/V tile.  Items are numbered latest
-// (heaviest) query tiles first; the grid is persistent (at most one CTA per
+// two 128-query tiles that share every K/V tile.  Items are numbered by
+// their KV tile count, most first (a chunk on a long cached prefix is heavy
+// even at its first query tile); the grid is persistent (at most one CTA per
 // SM) and CTA c takes item c, then the next unclaimed one from a counter in
 // device memory, so the tensor memory stays allocated, the next item's
 // queries and first K/V tiles load while the current one finishes, and the
