@@ -224,9 +224,10 @@ __device__ __forceinline__ WdItem wd_make_item(const WdArgs &w, int u, int part)
 // `sync`), given per head r: s_m[r] running max (log2 units), s_l[r] sum of
 // 2^(score - s_m[r]), s_o[r * D + d] the weighted V sum.  One partition:
 // the output rows s_o / s_l.  Otherwise the partials go to the workspace and
-// thread 0 counts the partition with a release atomic whose result it reads
-// only later (wd_merge_if_last, at the next item's end): the atomic's round
-// trip is not waited for.  Returns whether a count is pending.
+// thread 0 counts the partition with an acquire-release atomic whose result
+// it reads only later (at the next item's end, where the last partition
+// merges): the atomic's round trip is not waited for.  Returns whether a
+// count is pending.
 template <int D, typename T, typename Sync>
 __device__ bool wd_publish(const DecodeArgs &a, int b, int head0, int part, int nparts,
                            const float *s_m, const float *s_l, const float *s_o, int *counter,
@@ -251,7 +252,7 @@ __device__ bool wd_publish(const DecodeArgs &a, int b, int head0, int part, int 
   sync();
   if (ts == 0) {
     unsigned v;
-    asm volatile("atom.release.gpu.global.add.u32 %0, [%1], 1;"
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;"
                  : "=r"(v)
                  : "l"(reinterpret_cast<uint64_t>(counter))
                  : "memory");
@@ -271,7 +272,9 @@ __device__ void wd_merge(const DecodeArgs &a, int b, int head0, int nparts, floa
                          int *s_scratch, int *counter, int ts, Sync sync) {
   T *out = reinterpret_cast<T *>(a.out);
   const size_t row0 = (size_t)b * a.H + head0;
-  __threadfence();  // acquire: the other partitions' partials
+  // the other partitions' partials: thread 0's count was an acquire-release
+  // atomic that saw theirs, the group barrier passes that on, and the loads
+  // below go to L2
   const int warp = ts >> 5, lane = ts & 31;
   const bool cached = kWdHeads * nparts <= w_cap;
   float *s_M = reinterpret_cast<float *>(s_scratch + 1), *s_invL = s_M + kWdHeads;
@@ -947,7 +950,9 @@ __global__ void __launch_bounds__(kWdThreads, 1)
   __syncthreads();
   if (tid == 0) {
     // the last CTA of the launch puts the work counters back for the next
-    __threadfence();
+    // (every claim of this CTA was an atomic whose value it used before the
+    // barrier, so it is performed already: no fence, which at the end of a
+    // launch can hold a thread for tens of microseconds)
     if (atomicAdd(w.sched + 1, 1u) == gridDim.x - 1) {
       atomicExch(w.sched, 0u);
       atomicExch(w.sched + 1, 0u);

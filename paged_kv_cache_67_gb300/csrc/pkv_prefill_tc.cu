@@ -868,7 +868,9 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   if (warp == 0) tmem_dealloc(tmem, Sh::kTmemCols);
   if (tid == 0) {
     // the last CTA of the launch puts the work counters back for the next
-    __threadfence();
+    // (every claim of this CTA was an atomic whose value it used before the
+    // barrier, so it is performed already: no fence, which at the end of a
+    // launch can hold a thread for tens of microseconds)
     if (atomicAdd(a.sched + 1, 1u) == gridDim.x - 1) {
       atomicExch(a.sched, 0u);
       atomicExch(a.sched + 1, 0u);
