@@ -321,16 +321,19 @@ __device__ void finish_partition(const DecodeArgs &a, int b, int head0, int nh, 
     a.ws_o[((row0 + r) * a.max_parts + part) * D + d] = s_o[r * ostride + d];
     if (clear_o) s_o[r * ostride + d] = 0.f;
   }
-  // One thread publishes the group's partials: the barrier orders the
-  // group's writes before its fence (release is cumulative), the atomic
-  // counts the partition, and the finisher's fence orders the reads after it.
+  // One thread publishes the group's partials and counts the partition with
+  // one acquire-release atomic: the barrier orders the group's writes before
+  // its release (cumulative), and for the last partition its acquire orders
+  // the merge's reads after the other partitions' writes (no separate fences,
+  // which can hold a thread for microseconds under load).
   sync();
   if (tid == 0) {
-    __threadfence();
-    const int prev = atomicAdd(counter, 1);
-    const int last = prev == nparts - 1;
-    if (last) __threadfence();
-    s_scratch[0] = last;
+    int prev;
+    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;"
+                 : "=r"(prev)
+                 : "l"(reinterpret_cast<uint64_t>(counter))
+                 : "memory");
+    s_scratch[0] = prev == nparts - 1;
   }
   sync();
   if (!s_scratch[0]) return;
