@@ -134,6 +134,31 @@ def test_persistent_many_items_per_cta():
     check(77, lens, qlens, 16, 4, 64, 16, torch.bfloat16, "many items")
 
 
+def test_claim_order_by_work_many_sequences():
+    """40 sequences (the claim search runs over two 32-lane chunks), chunks
+    on long cached prefixes mixed with whole prompts, so that items of one
+    tile-count class come from many sequences."""
+    g = torch.Generator().manual_seed(79)
+    lens = torch.randint(64, 900, (40,), generator=g).tolist()
+    qlens = [n if b % 2 else int(torch.randint(1, min(n, 300) + 1, (1,), generator=g)) for b, n in enumerate(lens)]
+    check(79, lens, qlens, 8, 2, 64, 16, torch.bfloat16, "claim order by work")
+
+
+def test_claim_order_fallback_for_large_batches():
+    """More (sequence, tile) slots than the work-ordered claims cover (here
+    300 sequences x 16 tiles of the host's bound): the plain order, exact."""
+    g = torch.Generator().manual_seed(80)
+    lens = torch.randint(1, 60, (300,), generator=g).tolist()
+    qlens = [max(1, n // 2) for n in lens]
+    case, q, cu = make_case(80, lens, qlens, 4, 2, 64, 16, torch.bfloat16)
+    scale = 0.125
+    out, err = gpu_prefill(q, case, cu, scale, max_q_len=4096)
+    assert err == 0
+    want = oracle.prefill(q, case["k_cache"], case["v_cache"], case["block_tables"], cu,
+                          case["context_lens"], scale)
+    assert_close(out, want, torch.bfloat16, "fallback order")
+
+
 def test_persistent_relaunch_and_graph_replay():
     """The work counters are taken back by each launch's last CTA: back-to-back
     launches and replays of one captured launch all give the oracle's result."""

@@ -78,6 +78,24 @@ def test_many_items_per_cta():
     assert_close(out, oracle_decode(*args), torch.bfloat16, "many items")
 
 
+def test_many_units_and_unsorted_claims():
+    """300 sequences (more units than the claim search keeps in registers),
+    and a partition size small enough that the claims fall back to unit
+    order (more than 64 partitions per sequence)."""
+    g = torch.Generator().manual_seed(25)
+    lens = torch.randint(1, 1200, (300,), generator=g).tolist()
+    lens[:3] = [1, 1199, 1024]
+    case, args = case_args(25, lens, 16, 1, 128, 16, torch.bfloat16)
+    want = oracle_decode(*args)
+    out, err = gpu_decode(*args)
+    assert err == 0
+    assert_close(out, want, torch.bfloat16, "300 units")
+    assert pkv.pkv_decode_plan(300, 16, 1, 128, 16, case["block_tables"].shape[1], 2048, 16)[1] > 64
+    out, err = gpu_decode(*args, partition_size=16, max_context_len=2048)
+    assert err == 0
+    assert_close(out, want, torch.bfloat16, "unit-order claims")
+
+
 def test_relaunch_and_graph_replay():
     case, args = case_args(24, [300, 17, 1000, 128], 16, 1, 256, 32, torch.bfloat16)
     want = oracle_decode(*args)
