@@ -25,24 +25,30 @@
 //
 // Work decomposition.  A work item is (sequence, KV head, 16-head chunk,
 // partition of P tokens); the grid is persistent (at most one CTA per SM)
-// and CTAs claim items from a counter in device memory, the latest
-// partitions first, so long contexts spread over SMs and short ones fill
-// the gaps.  7 warps:
-//   warp 6     scheduler: claims items, publishes each to the CTA through a
-//              two-slot ring, loads the item's 16 query rows (TMA, 128-byte
-//              swizzle) once the last S^T of the previous item is done;
-//   warp 0     producer: per 128-token tile the tiled TMA loads of K, then
-//              of V (16-token chunks of 64-column regions, 128-byte
-//              swizzle), each into the next slot of one ring of K-or-V slots;
+// and CTAs claim items from a counter in device memory: every full
+// partition first (the latest partitions, which only long contexts have,
+// first), then the partial ones by tile count, most first -- long contexts
+// spread over SMs early and the last claims are the smallest.  7 warps:
+//   warp 6     scheduler: claims items (the next once the producer reaches
+//              the current item's last tile), publishes each to the CTA
+//              through a two-slot ring, loads the item's 16 query rows (TMA,
+//              128-byte swizzle) once the last S^T of the previous item is
+//              done;
+//   warp 0     producer: the tiled TMA loads of K and V tiles (16-token
+//              chunks of 64-column regions, 128-byte swizzle) into one ring
+//              of K-or-V slots, in the order K0, K1, V0, K2, V1, ... so keys
+//              run a tile ahead of values;
 //   warp 1     MMA issuer (one thread): S^T of the item's first two tiles,
 //              then per tile, once its P^T is written: O^T += V^T . P^T and
-//              the S^T two tiles ahead into the freed score buffer;
+//              the S^T two tiles ahead into the freed score buffer; frees
+//              the tensor memory at the end;
 //   warps 2-5  softmax, thread = token lane: scores from tensor memory,
 //              running max and per-lane weight sums per head, P^T written to
 //              shared memory; after the item's last tile the per-head sums
 //              are reduced and the item is finished -- output rows, or the
-//              partition's partials and, by the last partition of the
-//              sequence, the log-sum-exp merge.
+//              partition's partials counted by an atomic read at the next
+//              item's end, where the last partition of the sequence merges
+//              (log-sum-exp).
 // Every wait on an mbarrier is bounded; on time-out the CTA raises
 // PKV_FLAG_TIMEOUT, lets its copies and products land (bounded) and exits.
 #include <string.h>
@@ -181,10 +187,10 @@ __device__ __forceinline__ unsigned short wd_bits<__half>(float x) {
 __device__ __forceinline__ int wd_kidx(int j) { return j < 2 ? j : 2 * j - 1; }
 __device__ __forceinline__ int wd_vidx(int j, int n) { return j == n - 1 ? 2 * n - 1 : 2 * j + 2; }
 
-// The work items, numbered densely: unit u = (sequence, KV head, 16-head
-// chunk) contributes its partitions u's parts in order, units in order (an
-// empty context is one item that writes zero rows).  Consecutive claims go
-// to different CTAs, so a long context's partitions run side by side.
+// Units u = (sequence, KV head, 16-head chunk): a unit's length (its
+// sequence's, checked, clamped to the partitions the launch covers) and its
+// work item for a partition (an empty context is one item that writes zero
+// rows).
 __device__ __forceinline__ int wd_unit_len(const WdArgs &w, int u) {
   const DecodeArgs &a = w.d;
   int n = checked_len(a, u / (a.KVH * w.hchunks), false);
@@ -192,12 +198,6 @@ __device__ __forceinline__ int wd_unit_len(const WdArgs &w, int u) {
   if ((long long)n > reach) n = (int)reach;  // flagged once by CTA 0
   return n;
 }
-__device__ __forceinline__ int wd_unit_parts(const WdArgs &w, int u) {
-  if (u >= w.units) return 0;
-  const int n = wd_unit_len(w, u);
-  return n > 0 ? (n + w.d.P - 1) / w.d.P : 1;
-}
-
 __device__ __forceinline__ WdItem wd_make_item(const WdArgs &w, int u, int part) {
   const DecodeArgs &a = w.d;
   WdItem it;
