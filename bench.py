@@ -503,7 +503,10 @@ def run_gpu(args, world, rank, local):
         dec_ms = statistics.mean(a.elapsed_time(b) for a, b in dec_ev)
     else:
         dec_ms = elapsed * 1e3 / args.steps  # back-to-back graph nodes: the per-step time
-    launches = args.steps * (1 if fused else 2)
+    # the fused entry is one launch, except on the wide-group kernel, where it
+    # runs pkv_write first (two launches, both inside the per-step events)
+    wide = kx is None and kernel_name(cfg, args.mode).startswith("pkv_decode_wide")
+    launches = args.steps * (1 if fused and not wide else 2)
     if int(err.item()) != 0:
         raise RuntimeError(f"device error flags {int(err.item()):#x} in the timed region")
     step_bytes = [steps[i % S]["dec"] + steps[i % S]["wr"] for i in range(args.steps)]
@@ -539,6 +542,7 @@ def run_gpu(args, world, rank, local):
                      "frac": round(achieved / peak, 4),
                      "traffic": decode_traffic(kname, args.workload),
                      "kernel": kname, "bytes_per_launch": round(kern_bytes),
+                     **({"timed_span": "pkv_write + " + kname} if fused and wide else {}),
                      "peak_source": ("measured (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
                                      else "fallback 6.8 TB/s"),
                      "kernel_us": round(dec_ms * 1e3, 2)},
