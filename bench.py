@@ -9,20 +9,23 @@ default a step is one pkv_write_decode_attention launch (`--mode
 two-launch`: pkv_write, then pkv_decode_attention).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
-                    [--workload NAME] [--mode fused|two-launch] [--graph]
+                    [--workload NAME] [--mode fused|two-launch] [--no-graph]
 
 Prints one JSON line.  `value` is the step's algorithmic bytes (K/V rows
 used, q, out, table prefix, lengths, plus the write's rows and slots) per
-second of device time over the K timed steps, all ranks together.  The
-`roofline` block is for the attention kernel (with the write, when fused):
-its algorithmic bytes over its mean launch time from CUDA events on its
-stream, against the measured HBM copy bandwidth.  `--impl reference` times
+second of device time over the K timed steps, all ranks together.  The K
+timed steps are captured once as a CUDA graph and replayed, so the host's
+launch rate stays out of the timed region (`--no-graph`: every step
+launched from the host).  The `roofline` block is for the attention kernel
+(with the write, when fused): its algorithmic bytes over its time per step
+(graph: the replay's CUDA-event span over K; `--no-graph`: the mean of the
+per-launch CUDA events on its stream), against the measured HBM copy
+bandwidth.  `--impl reference` times
 the oracle (plain fp64 C on the host cores) on bounded samples of the same
 workload instead.  Under torchrun (N > 1) every rank runs its own
 independent batch (weak scaling, no collective on the data path); time is
 the max over ranks.  `--workload` picks another of the five workloads (the
-per-step one cycles through its 32 steps); `--graph` replays the timed
-steps from one CUDA graph.
+per-step one cycles through its 32 steps).
 """
 from __future__ import annotations
 
@@ -710,8 +713,11 @@ def main():
     ap.add_argument("--mode", default="fused", choices=["fused", "two-launch"],
                     help="fused: one pkv_write_decode_attention launch per step; two-launch: "
                          "pkv_write then pkv_decode_attention")
-    ap.add_argument("--graph", action="store_true",
-                    help="replay the timed steps from one CUDA graph")
+    ap.add_argument("--graph", dest="graph", action="store_true", default=True,
+                    help="replay the timed steps from one CUDA graph (the default)")
+    ap.add_argument("--no-graph", dest="graph", action="store_false",
+                    help="launch every timed step from the host, each decode launch between "
+                         "its own CUDA events")
     ap.add_argument("--layout", default="token-major", choices=["token-major", "xpacked"],
                     help="xpacked: the layout experiment (caches in vLLM's packed layout, "
                          "write + decode in two launches; with --only-decode)")
