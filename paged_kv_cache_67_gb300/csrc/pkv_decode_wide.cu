@@ -220,6 +220,19 @@ __device__ __forceinline__ WdItem wd_make_item(const WdArgs &w, int u, int part)
   return it;
 }
 
+// Two fp32 values rounded to nearest even and packed as one pair of T (the
+// first in the low half, so at the lower address).
+template <typename T>
+__device__ __forceinline__ uint32_t wd_pack2(float lo, float hi) {
+  if constexpr (std::is_same<T, __nv_bfloat16>::value) {
+    const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t *>(&v);
+  } else {
+    const __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t *>(&v);
+  }
+}
+
 // The end of one item, by the 128 softmax threads (thread ts, barrier
 // `sync`), given per head r: s_m[r] running max (log2 units), s_l[r] sum of
 // 2^(score - s_m[r]), s_o[r * D + d] the weighted V sum.  One partition:
@@ -235,8 +248,18 @@ __device__ bool wd_publish(const DecodeArgs &a, int b, int head0, int part, int 
   T *out = reinterpret_cast<T *>(a.out);
   const size_t row0 = (size_t)b * a.H + head0;
   if (nparts == 1) {
-    for (int i = ts; i < kWdHeads * D; i += 128)
-      out[row0 * D + i] = from_f32<T>(s_o[i] / s_l[i / D]);
+    // eight outputs per thread and step: one 16-byte store
+    for (int i = ts; i < kWdHeads * D / 8; i += 128) {
+      const float4 x0 = *reinterpret_cast<const float4 *>(s_o + 8 * i);
+      const float4 x1 = *reinterpret_cast<const float4 *>(s_o + 8 * i + 4);
+      const float inv_l = 1.f / s_l[8 * i / D];
+      uint4 v;
+      v.x = wd_pack2<T>(x0.x * inv_l, x0.y * inv_l);
+      v.y = wd_pack2<T>(x0.z * inv_l, x0.w * inv_l);
+      v.z = wd_pack2<T>(x1.x * inv_l, x1.y * inv_l);
+      v.w = wd_pack2<T>(x1.z * inv_l, x1.w * inv_l);
+      *reinterpret_cast<uint4 *>(out + row0 * D + 8 * i) = v;
+    }
     return false;
   }
   if (ts < kWdHeads) {
@@ -263,10 +286,13 @@ __device__ bool wd_publish(const DecodeArgs &a, int b, int head0, int part, int 
 
 // The merge of a (sequence, head chunk) whose partitions have all arrived,
 // by the group whose count was the last:  M = max_p m_p,
-// L = sum_p l_p 2^(m_p - M),  out = sum_p o_p 2^(m_p - M) / L -- the
-// weights first (into s_w, 16 x nparts floats when they fit in w_cap), then
-// four output values per thread and step with eight partitions' loads in
-// flight; the counter is put back to zero for the next call.
+// L = sum_p l_p 2^(m_p - M),  out = sum_p o_p 2^(m_p - M) / L.  It sits at
+// the end of the work, so it is written for latency: warp w takes rows w,
+// w + 4, w + 8, w + 12 together (their m and l loads in one round trip when
+// nparts <= 32) and puts the weights in s_w (16 x nparts floats when they
+// fit in w_cap); then each thread takes four output vectors of four values at
+// a time with eight partitions' loads of each in flight.  The counter is put
+// back to zero for the next call.
 template <int D, typename T, typename Sync>
 __device__ void wd_merge(const DecodeArgs &a, int b, int head0, int nparts, float *s_w, int w_cap,
                          int *s_scratch, int *counter, int ts, Sync sync) {
@@ -276,62 +302,135 @@ __device__ void wd_merge(const DecodeArgs &a, int b, int head0, int nparts, floa
   // atomic that saw theirs, the group barrier passes that on, and the loads
   // below go to L2
   const int warp = ts >> 5, lane = ts & 31;
+  constexpr int kRows = kWdHeads / 4;
   const bool cached = kWdHeads * nparts <= w_cap;
   float *s_M = reinterpret_cast<float *>(s_scratch + 1), *s_invL = s_M + kWdHeads;
-  for (int r = warp; r < kWdHeads; r += 4) {
-    const float *pm = a.ws_m + (row0 + r) * a.max_parts, *pl = a.ws_l + (row0 + r) * a.max_parts;
-    float M = -INFINITY;
-    for (int p = lane; p < nparts; p += 32) M = fmaxf(M, __ldcg(pm + p));
+  const float *pm[kRows], *pl[kRows];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-    float L = 0.f;
-    for (int p = lane; p < nparts; p += 32) L += __ldcg(pl + p) * fast_exp2(__ldcg(pm + p) - M);
+  for (int j = 0; j < kRows; ++j) {
+    pm[j] = a.ws_m + (row0 + warp + 4 * j) * a.max_parts;
+    pl[j] = a.ws_l + (row0 + warp + 4 * j) * a.max_parts;
+  }
+  auto warp_max = [](float v) {
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
-    const float inv_l = 1.f / L;
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+  };
+  auto warp_sum = [](float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+  };
+  float M[kRows], inv_l[kRows];
+  if (nparts <= 32) {
+    const bool mine = lane < nparts;
+    const int pc = min(lane, nparts - 1);   // clamped: the loads are not predicated
+    float mv[kRows], lv[kRows];
+#pragma unroll
+    for (int j = 0; j < kRows; ++j) {
+      mv[j] = __ldcg(pm[j] + pc);
+      lv[j] = __ldcg(pl[j] + pc);
+    }
+#pragma unroll
+    for (int j = 0; j < kRows; ++j) mv[j] = mine ? mv[j] : -INFINITY;
+#pragma unroll
+    for (int j = 0; j < kRows; ++j) {
+      M[j] = warp_max(mv[j]);
+      const float e = mine ? fast_exp2(mv[j] - M[j]) : 0.f;
+      inv_l[j] = 1.f / warp_sum(mine ? lv[j] * e : 0.f);
+      if (cached && mine) s_w[(warp + 4 * j) * nparts + lane] = e * inv_l[j];
+    }
+  } else {
+    float L[kRows];
+#pragma unroll
+    for (int j = 0; j < kRows; ++j) {
+      M[j] = -INFINITY;
+      L[j] = 0.f;
+    }
+    for (int p = lane; p < nparts; p += 32) {
+#pragma unroll
+      for (int j = 0; j < kRows; ++j) M[j] = fmaxf(M[j], __ldcg(pm[j] + p));
+    }
+#pragma unroll
+    for (int j = 0; j < kRows; ++j) M[j] = warp_max(M[j]);
+    for (int p = lane; p < nparts; p += 32) {
+#pragma unroll
+      for (int j = 0; j < kRows; ++j) L[j] += __ldcg(pl[j] + p) * fast_exp2(__ldcg(pm[j] + p) - M[j]);
+    }
+#pragma unroll
+    for (int j = 0; j < kRows; ++j) inv_l[j] = 1.f / warp_sum(L[j]);
     if (cached)
-      for (int p = lane; p < nparts; p += 32) s_w[r * nparts + p] = fast_exp2(__ldcg(pm + p) - M) * inv_l;
-    if (lane == 0) {
-      s_M[r] = M;
-      s_invL[r] = inv_l;
+      for (int p = lane; p < nparts; p += 32) {
+#pragma unroll
+        for (int j = 0; j < kRows; ++j)
+          s_w[(warp + 4 * j) * nparts + p] = fast_exp2(__ldcg(pm[j] + p) - M[j]) * inv_l[j];
+      }
+  }
+  if (lane == 0) {
+#pragma unroll
+    for (int j = 0; j < kRows; ++j) {
+      s_M[warp + 4 * j] = M[j];
+      s_invL[warp + 4 * j] = inv_l[j];
     }
   }
   sync();
-  for (int i = ts; i < kWdHeads * D / 4; i += 128) {
-    const int r = 4 * i / D, d = 4 * i - r * D;
-    const float4 *po = reinterpret_cast<const float4 *>(a.ws_o + (row0 + r) * a.max_parts * D + d);
-    const float *pm = a.ws_m + (row0 + r) * a.max_parts;
-    auto weight = [&](int p) {
-      return cached ? s_w[r * nparts + p] : fast_exp2(__ldcg(pm + p) - s_M[r]) * s_invL[r];
-    };
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    int p = 0;
-    for (; p + 8 <= nparts; p += 8) {
-      float4 v[8];
+  constexpr int kVecs = kWdHeads * D / 4;   // output vectors of four values
+  constexpr int kU = 4;                     // vectors per thread and step
+  static_assert(kVecs % (128 * kU) == 0, "whole steps of the group");
+  for (int i0 = ts; i0 < kVecs; i0 += 128 * kU) {
+    int r[kU], d[kU];
+    const float4 *po[kU];
+    float4 acc[kU];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) v[u] = __ldcg(po + (size_t)(p + u) * (D / 4));
+    for (int u = 0; u < kU; ++u) {
+      const int i = i0 + 128 * u;
+      r[u] = 4 * i / D;
+      d[u] = 4 * i - r[u] * D;
+      po[u] = reinterpret_cast<const float4 *>(a.ws_o + (row0 + r[u]) * a.max_parts * D + d[u]);
+      acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    if (cached) {
+      // every load of a step issued before any is used: the partition index
+      // is clamped (a repeated load gets weight 0), so no load is predicated
+      for (int p0 = 0; p0 < nparts; p0 += 8) {
+        float4 v[kU][8];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const float wt = weight(p + u);
-        acc.x += wt * v[u].x;
-        acc.y += wt * v[u].y;
-        acc.z += wt * v[u].z;
-        acc.w += wt * v[u].w;
+        for (int u = 0; u < kU; ++u)
+#pragma unroll
+          for (int q = 0; q < 8; ++q) v[u][q] = __ldcg(po[u] + (size_t)min(p0 + q, nparts - 1) * (D / 4));
+#pragma unroll
+        for (int u = 0; u < kU; ++u)
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const float wt = p0 + q < nparts ? s_w[r[u] * nparts + p0 + q] : 0.f;
+            acc[u].x += wt * v[u][q].x;
+            acc[u].y += wt * v[u][q].y;
+            acc[u].z += wt * v[u][q].z;
+            acc[u].w += wt * v[u][q].w;
+          }
+      }
+    } else {
+      // more partitions than weights fit: each weight from its m
+      for (int p = 0; p < nparts; ++p) {
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+          const float wt = fast_exp2(__ldcg(a.ws_m + (row0 + r[u]) * a.max_parts + p) - s_M[r[u]]) *
+                           s_invL[r[u]];
+          const float4 v = __ldcg(po[u] + (size_t)p * (D / 4));
+          acc[u].x += wt * v.x;
+          acc[u].y += wt * v.y;
+          acc[u].z += wt * v.z;
+          acc[u].w += wt * v.w;
+        }
       }
     }
-    for (; p < nparts; ++p) {
-      const float4 v = __ldcg(po + (size_t)p * (D / 4));
-      const float wt = weight(p);
-      acc.x += wt * v.x;
-      acc.y += wt * v.y;
-      acc.z += wt * v.z;
-      acc.w += wt * v.w;
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      uint2 o;
+      o.x = wd_pack2<T>(acc[u].x, acc[u].y);
+      o.y = wd_pack2<T>(acc[u].z, acc[u].w);
+      *reinterpret_cast<uint2 *>(out + (row0 + r[u]) * D + d[u]) = o;
     }
-    T *o = out + (row0 + r) * D + d;
-    o[0] = from_f32<T>(acc.x);
-    o[1] = from_f32<T>(acc.y);
-    o[2] = from_f32<T>(acc.z);
-    o[3] = from_f32<T>(acc.w);
   }
   if (ts == 0) *counter = 0;  // every partition has arrived: ready for the next call
 }
