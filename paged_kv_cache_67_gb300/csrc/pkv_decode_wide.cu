@@ -63,7 +63,6 @@
 namespace pkv {
 
 constexpr int kWdTile = 128;             // tokens per KV tile (M of S^T)
-constexpr int kWdChunks = kWdTile / 16;  // 16-token chunks per tile
 constexpr int kWdHeads = 16;             // query heads per item (N)
 constexpr int kWdWarps = 7;
 constexpr int kWdThreads = 32 * kWdWarps;
@@ -117,6 +116,7 @@ struct WdArgs {
   int hchunks;         // 16-head chunks per KV head (G / 16)
   int units;           // B * KVH * hchunks
   int check_append;    // new_slots given: check each slot against position n - 1
+  int box_tok;         // tokens per K/V box: 16, 32, 64 or 128, dividing bs and P
 };
 
 // Whether the phase with the given parity has completed (never waits).
@@ -189,16 +189,21 @@ __device__ __forceinline__ int wd_vidx(int j, int n) { return j == n - 1 ? 2 * n
 
 // Units u = (sequence, KV head, 16-head chunk): a unit's length (its
 // sequence's, checked, clamped to the partitions the launch covers) and its
-// work item for a partition (an empty context is one item that writes zero
-// rows).
-__device__ __forceinline__ int wd_unit_len(const WdArgs &w, int u) {
+// work item for a partition, given the length (an empty context is one item
+// that writes zero rows).
+// A length as loaded, checked: negative counts as empty; beyond the block
+// table or the partitions the launch covers it is cut there (CTA 0 flags
+// both).
+__device__ __forceinline__ int wd_clamp_len(const WdArgs &w, int n) {
   const DecodeArgs &a = w.d;
-  int n = checked_len(a, u / (a.KVH * w.hchunks), false);
-  const long long reach = (long long)a.max_parts * a.P;
-  if ((long long)n > reach) n = (int)reach;  // flagged once by CTA 0
-  return n;
+  const long long cap = min((long long)a.max_blocks * a.bs, (long long)a.max_parts * a.P);
+  n = max(n, 0);
+  return (long long)n > cap ? (int)cap : n;
 }
-__device__ __forceinline__ WdItem wd_make_item(const WdArgs &w, int u, int part) {
+__device__ __forceinline__ int wd_unit_len(const WdArgs &w, int u) {
+  return wd_clamp_len(w, __ldg(w.d.lens + u / (w.d.KVH * w.hchunks)));
+}
+__device__ __forceinline__ WdItem wd_make_item(const WdArgs &w, int u, int part, int n) {
   const DecodeArgs &a = w.d;
   WdItem it;
   memset(&it, 0, sizeof it);
@@ -206,7 +211,6 @@ __device__ __forceinline__ WdItem wd_make_item(const WdArgs &w, int u, int part)
   it.kvh = (u / w.hchunks) % a.KVH;
   it.hc = u % w.hchunks;
   it.part = part;
-  const int n = wd_unit_len(w, u);
   it.n = n;
   it.nparts = n > 0 ? (n + a.P - 1) / a.P : 1;
   it.t0 = part * a.P;
@@ -495,6 +499,15 @@ __global__ void __launch_bounds__(kWdThreads, 1)
     fence_mbar_init();
   }
   if (warp == 0) tmem_alloc(tmem_holder, Sh::kTmemCols);
+  // the scheduler's unit lengths (up to 8 x 32 units), in flight across the
+  // set-up barrier: not predicated (the index is clamped), so all at once
+  constexpr int kRegUnits = 8;
+  int unit_raw[kRegUnits];
+  if (warp == kWdSchedWarp) {
+    const int last = max(w.units - 1, 0), per_seq = a.KVH * w.hchunks;
+#pragma unroll
+    for (int r = 0; r < kRegUnits; ++r) unit_raw[r] = __ldg(a.lens + min(32 * r + lane, last) / per_seq);
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -509,9 +522,10 @@ __global__ void __launch_bounds__(kWdThreads, 1)
 
   if (warp == kWdSchedWarp) {
     // ------------------------------------------------------------ scheduler
-    if (blockIdx.x == 0) {
-      // the checks of the whole batch, once: lengths, the host's bound on
-      // them, and (fused step) each new token's slot against position n - 1
+    // the checks of the whole batch, once, by CTA 0 after its first item is
+    // out: lengths, the host's bound on them, and (fused step) each new
+    // token's slot against position n - 1
+    auto batch_checks = [&]() {
       const long long reach = (long long)a.max_parts * a.P;
       int over = 0;
       for (int bb = lane; bb < a.B; bb += 32) {
@@ -523,7 +537,7 @@ __global__ void __launch_bounds__(kWdThreads, 1)
         }
       }
       if (__any_sync(0xffffffffu, over) && lane == 0) raise_flag(a.err, PKV_FLAG_CONTEXT_OVER_HINT);
-    }
+    };
     // The claim order, numbered densely: first every full partition (P
     // tokens) -- round r holds partition maxp - 1 - r of the units long
     // enough, so the latest partitions, only long contexts have them, go
@@ -536,13 +550,12 @@ __global__ void __launch_bounds__(kWdThreads, 1)
     const int maxp = a.max_parts;
     const int tmax = (a.P + kWdTile - 1) / kWdTile;     // tiles of a full partition
     const bool sorted = maxp <= 64 && tmax <= 63;
-    constexpr int kRegUnits = 8;                        // 8 x 32 units in registers
     const bool in_regs = w.units <= 32 * kRegUnits;
     int unit_n[kRegUnits];
 #pragma unroll
     for (int r = 0; r < kRegUnits; ++r) {
       const int u = 32 * r + lane;
-      unit_n[r] = (in_regs && u < w.units) ? wd_unit_len(w, u) : -1;
+      unit_n[r] = (in_regs && u < w.units) ? wd_clamp_len(w, unit_raw[r]) : -1;
     }
     auto len_of = [&](int base) -> int {              // unit base + lane's length, -1 past the end
       if (!in_regs) return base + lane < w.units ? wd_unit_len(w, base + lane) : -1;
@@ -623,7 +636,7 @@ __global__ void __launch_bounds__(kWdThreads, 1)
             if (idx < c) {
               const int src = (int)__fns(m, 0, idx + 1);
               const int nn = __shfl_sync(0xffffffffu, n, src);
-              item = wd_make_item(w, base + src, part_of(nn));
+              item = wd_make_item(w, base + src, part_of(nn), nn);
               return;
             }
             idx -= c;
@@ -661,7 +674,8 @@ __global__ void __launch_bounds__(kWdThreads, 1)
             const unsigned hit = __ballot_sync(0xffffffffu, chunk_cum + (unsigned)incl > k);
             const int src = __ffs(hit) - 1;
             const int excl = __shfl_sync(0xffffffffu, incl - np, src);
-            item = wd_make_item(w, chunk_base + src, (int)(k - chunk_cum) - excl);
+            const int nn = __shfl_sync(0xffffffffu, n, src);
+            item = wd_make_item(w, chunk_base + src, (int)(k - chunk_cum) - excl, nn);
             break;
           }
           chunk_cum += chunk_total;
@@ -679,6 +693,7 @@ __global__ void __launch_bounds__(kWdThreads, 1)
       }
       __syncwarp();
       ++it;
+      if (it == 1 && blockIdx.x == 0) batch_checks();
       if (item.kind < 0) break;
       if (item.kind == 1) {
         // the item's 16 query rows, once the last S^T of the previous is done
@@ -708,8 +723,11 @@ __global__ void __launch_bounds__(kWdThreads, 1)
     // ------------------------------------------------------------ producer
     // per tile: K into the next ring slot, then V into the one after; a slot
     // is reused once the product that read it is done
-    const int per_tensor = kWdChunks * Sh::kRegions;     // boxes per tile (<= 32)
-    const int region = (lane % per_tensor) / kWdChunks, chunk = lane % kWdChunks;
+    // a tile of one tensor is nch chunks of box_tok tokens (one box each,
+    // never across a cache block) times kRegions blocks of 64 values
+    const int bt = w.box_tok, nch = kWdTile / bt;
+    const int per_tensor = nch * Sh::kRegions;           // boxes per tile (<= 32)
+    const int region = (lane % per_tensor) / nch, chunk = lane % nch;
     const uint64_t policy = l2_evict_first_policy();
     if (lane == 0) {
       prefetch_tensormap(&tmK);
@@ -731,6 +749,16 @@ __global__ void __launch_bounds__(kWdThreads, 1)
         continue;
       }
       const int nt = item.ntiles;
+      // the physical blocks, read four tiles ahead of their use (a lookup
+      // per load would hold each load for a round trip): lane 8 * (j % 4) + c
+      // holds the table entry of tokens 16c .. 16c + 15 of tile j; tokens past
+      // the context read the last entry inside it; checked where used
+      const size_t trow = (size_t)item.b * a.max_blocks;
+      auto entry_of = [&](int j) {
+        const int t = min(item.t0 + j * kWdTile + 16 * (lane & 7), item.t1 - 1);
+        return __ldg(a.tables + trow + t / a.bs);
+      };
+      int ahead = (lane >> 3) < nt ? entry_of(lane >> 3) : 0;
       for (int idx = 0; idx < 2 * nt && ok; ++idx) {
         // which tile, K or V
         int j, v;
@@ -748,12 +776,13 @@ __global__ void __launch_bounds__(kWdThreads, 1)
           v = 0;
         }
         const int tok0 = item.t0 + j * kWdTile;
-        const int valid_chunks = min(kWdChunks, (item.t1 - tok0 + 15) >> 4);
-        const uint32_t bytes = (uint32_t)(valid_chunks * Sh::kRegions * 2048);
-        // the chunks' physical blocks (in flight during the slot wait)
-        int phys = 0;
-        if (lane < valid_chunks) phys = checked_block(a, item.b, (tok0 + 16 * lane) / a.bs);
-        phys = __shfl_sync(0xffffffffu, phys, chunk);
+        const int valid_chunks = min(nch, (item.t1 - tok0 + bt - 1) / bt);
+        const uint32_t bytes = (uint32_t)(valid_chunks * Sh::kRegions * bt * 128);
+        int phys = __shfl_sync(0xffffffffu, ahead, 8 * (j & 3) + (bt >> 4) * chunk);
+        if (phys < 0 || (long long)phys >= a.num_blocks) {  // outside the pool: flagged, block 0 read
+          if (lane < valid_chunks) raise_flag(a.err, PKV_FLAG_BLOCK_OUT_OF_RANGE);
+          phys = 0;
+        }
         const int s = loads % Sh::kSlots, use = loads / Sh::kSlots;
         if (use > 0) {
           ok = __all_sync(0xffffffffu, mbar_wait_bounded(&slot_empty[s], (use - 1) & 1)) && !aborted();
@@ -762,13 +791,16 @@ __global__ void __launch_bounds__(kWdThreads, 1)
         if (lane == 0) mbar_arrive_expect_tx(&slot_full[s], bytes);
         __syncwarp();
         if (lane < per_tensor && chunk < valid_chunks) {
-          const int t = tok0 + 16 * chunk;
+          const int t = tok0 + bt * chunk;
           const int lb = t / a.bs;
-          uint8_t *dst = sm + s * Sh::kTileBytes + region * Sh::kRegionBytes + chunk * 2048;
+          uint8_t *dst = sm + s * Sh::kTileBytes + region * Sh::kRegionBytes + chunk * bt * 128;
           wd_tma_4d(dst, v ? &tmV : &tmK, &slot_full[s], region * 64, item.kvh, t - lb * a.bs, phys,
                     policy);
         }
         ++loads;
+        // tile j's entries are done with once its values are on the way:
+        // the lanes of its group read those of tile j + 4
+        if (v && (lane >> 3) == (j & 3) && j + 4 < nt) ahead = entry_of(j + 4);
         // the scheduler may claim the next item once the last tile's loads
         // are next (the claim's latency overlaps them)
         if (idx == max(0, 2 * nt - 3) && lane == 0) mbar_arrive(prod_done);
@@ -1099,6 +1131,37 @@ static bool encode_query_group_map(CUtensorMap *map, const void *q, pkv_dtype dt
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Tensor map of a [num_blocks, bs, KVH, D] cache: box of 64 values x 1 head
+// x box_tok tokens x 1 block, 128-byte swizzle (a box lands as box_tok
+// consecutive 128-byte rows of one 64-value block of a tile).
+static bool encode_wide_cache_map(CUtensorMap *map, const void *cache, pkv_dtype dt,
+                                  long long num_blocks, int bs, int KVH, int D, int box_tok) {
+  WdEncodeFn fn = wd_encode_fn();
+  if (!fn) return false;
+  const cuuint64_t el = 2;
+  cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)KVH, (cuuint64_t)bs, (cuuint64_t)num_blocks};
+  cuuint64_t strides[3] = {D * el, (cuuint64_t)KVH * D * el, (cuuint64_t)bs * KVH * D * el};
+  cuuint32_t box[4] = {64, 1, (cuuint32_t)box_tok, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  return fn(map,
+            dt == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4,
+            const_cast<void *>(cache), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Tokens per K/V box: the largest of 128, 64, 32, 16 dividing both the block
+// size and the partition size, so that every box starts on a multiple of it
+// (tiles start at multiples of the partition size plus 128) and stays in one
+// block.  Fewer, larger boxes: with 16-token (2 KB) boxes the TMA unit's
+// per-box cost, not HBM, paced each CTA's loads (a 64 KB tile took ~1.4 us to
+// issue; ~0.9 us with 32-token boxes).
+static int wd_box_tokens(int bs, int P) {
+  for (int bt = kWdTile; bt > 16; bt >>= 1)
+    if (bs % bt == 0 && P % bt == 0) return bt;
+  return 16;
+}
+
 static unsigned *wd_sched_counters() {
   static unsigned *cached[64] = {nullptr};
   int dev = 0;
@@ -1126,9 +1189,10 @@ static pkv_status launch_wide_t(const WdArgs &w, const CUtensorMap &mq, const CU
 
 pkv_status launch_decode_wide(const DecodeArgs &a, pkv_dtype dt, int num_sms, cudaStream_t stream) {
   CUtensorMap mq, mk, mv;
+  const int box_tok = wd_box_tokens(a.bs, a.P);
   if (!encode_query_group_map(&mq, a.q, dt, a.B, a.H, a.D) ||
-      !encode_cache_map(&mk, a.k_cache, dt, a.num_blocks, a.bs, a.KVH, a.D) ||
-      !encode_cache_map(&mv, a.v_cache, dt, a.num_blocks, a.bs, a.KVH, a.D))
+      !encode_wide_cache_map(&mk, a.k_cache, dt, a.num_blocks, a.bs, a.KVH, a.D, box_tok) ||
+      !encode_wide_cache_map(&mv, a.v_cache, dt, a.num_blocks, a.bs, a.KVH, a.D, box_tok))
     return PKV_ERR_CUDA;
   unsigned *sched = wd_sched_counters();
   if (!sched) return PKV_ERR_CUDA;
@@ -1143,6 +1207,7 @@ pkv_status launch_decode_wide(const DecodeArgs &a, pkv_dtype dt, int num_sms, cu
   w.hchunks = a.G / kWdHeads;
   w.units = a.B * a.KVH * w.hchunks;
   w.check_append = a.new_slots != nullptr;
+  w.box_tok = box_tok;
   // one persistent CTA per SM, never more than the items there can be
   const long long items = (long long)w.units * a.max_parts;
   const int ctas = (int)std::min<long long>(items, num_sms > 0 ? num_sms : 1);
