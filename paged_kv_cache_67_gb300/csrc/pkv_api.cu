@@ -90,10 +90,11 @@ bool make_plan(int B, int H, int KVH, int D, int bs, int max_blocks, int max_con
   p.stages = p.kernel ? tc_stages(D) : 0;
   p.smem_bytes = p.kernel ? tc_smem_bytes(D, p.stages) : simt_smem_bytes(D, p.heads_per_cta);
   // Groups of exactly 16 query heads with D = 128 or 256 (MQA-like): the
-  // persistent kernel with tokens as the product's M; work items of 1024
-  // tokens (measured best on the log-uniform MQA batch: smaller items cost
-  // more per item than they gain in balance), never below the automatic
-  // floor that keeps them within the workspace.
+  // persistent kernel with tokens as the product's M.  The plan's partition
+  // is 1024 tokens (never below the automatic floor that keeps the
+  // partitions within the workspace); with it the kernel sizes its work
+  // items from the batch's lengths (about 1.2 CTA shares of tiles, never
+  // smaller than the plan's partition).
   if (allow_wide && p.kernel == 1 && G == 16 && (D == 128 || D == 256) &&
       wide_smem_bytes(D) <= (smem_optin > 0 ? smem_optin : kDefaultSmemOptin)) {
     p.kernel = 2;
@@ -307,7 +308,7 @@ static pkv_status decode_entry(void *out, const void *q, const void *k_cache, co
                                          num_kv_heads, head_dim, (int)el, err_flags, s);
       if (st != PKV_OK) return st;
     }
-    return launch_decode_wide(a, dt, sms, s);
+    return launch_decode_wide(a, dt, sms, partition_size == 0, s);
   }
   return plan.kernel ? launch_decode_tc(a, plan, dt, s) : launch_decode_simt(a, plan, dt, s);
 }

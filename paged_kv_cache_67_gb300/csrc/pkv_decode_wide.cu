@@ -117,6 +117,7 @@ struct WdArgs {
   int units;           // B * KVH * hchunks
   int check_append;    // new_slots given: check each slot against position n - 1
   int box_tok;         // tokens per K/V box: 16, 32, 64 or 128, dividing bs and P
+  int auto_items;      // the partition size is the plan's own: items may be larger
 };
 
 // Whether the phase with the given parity has completed (never waits).
@@ -203,7 +204,7 @@ __device__ __forceinline__ int wd_clamp_len(const WdArgs &w, int n) {
 __device__ __forceinline__ int wd_unit_len(const WdArgs &w, int u) {
   return wd_clamp_len(w, __ldg(w.d.lens + u / (w.d.KVH * w.hchunks)));
 }
-__device__ __forceinline__ WdItem wd_make_item(const WdArgs &w, int u, int part, int n) {
+__device__ __forceinline__ WdItem wd_make_item(const WdArgs &w, int u, int part, int n, int P) {
   const DecodeArgs &a = w.d;
   WdItem it;
   memset(&it, 0, sizeof it);
@@ -212,9 +213,9 @@ __device__ __forceinline__ WdItem wd_make_item(const WdArgs &w, int u, int part,
   it.hc = u % w.hchunks;
   it.part = part;
   it.n = n;
-  it.nparts = n > 0 ? (n + a.P - 1) / a.P : 1;
-  it.t0 = part * a.P;
-  it.t1 = min(n, it.t0 + a.P);
+  it.nparts = n > 0 ? (n + P - 1) / P : 1;
+  it.t0 = part * P;
+  it.t1 = min(n, it.t0 + P);
   if (n == 0) {
     it.kind = 2;  // empty context: zero output rows
     return it;
@@ -547,9 +548,6 @@ __global__ void __launch_bounds__(kWdThreads, 1)
     // count comes from histograms of the units' lengths in shared memory (up
     // to 64 rounds and 63 tile counts; beyond, units in order).  Up to 256
     // units keep their lengths in the lanes' registers.
-    const int maxp = a.max_parts;
-    const int tmax = (a.P + kWdTile - 1) / kWdTile;     // tiles of a full partition
-    const bool sorted = maxp <= 64 && tmax <= 63;
     const bool in_regs = w.units <= 32 * kRegUnits;
     int unit_n[kRegUnits];
 #pragma unroll
@@ -557,6 +555,28 @@ __global__ void __launch_bounds__(kWdThreads, 1)
       const int u = 32 * r + lane;
       unit_n[r] = (in_regs && u < w.units) ? wd_clamp_len(w, unit_raw[r]) : -1;
     }
+    // The item size P: the plan's partition size, or (the plan's own choice)
+    // about 1.2 times each CTA's share of the batch's 128-token tiles,
+    // rounded to whole tiles and never below the plan's, so a sequence
+    // never has more partitions than the workspace holds.  Measured on
+    // log-uniform MQA batches: the best item was 1.18 to 1.21 shares on
+    // three seeds; smaller items pay more item starts and merges than they
+    // gain in balance, larger ones leave the last CTAs alone.  Every CTA
+    // computes the same P from the same lengths.
+    int P = a.P;
+    if (w.auto_items && in_regs) {
+      int tiles = 0;
+#pragma unroll
+      for (int r = 0; r < kRegUnits; ++r) tiles += unit_n[r] > 0 ? (unit_n[r] + kWdTile - 1) / kWdTile : 0;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) tiles += __shfl_xor_sync(0xffffffffu, tiles, o);
+      const long long c = gridDim.x;
+      const long long want = (12LL * tiles + 5 * c) / (10 * c);
+      P = max(P, (int)(want < 63 ? want : 63) * kWdTile);
+    }
+    const int maxp = a.max_parts;
+    const int tmax = (P + kWdTile - 1) / kWdTile;       // tiles of a full partition
+    const bool sorted = maxp <= 64 && tmax <= 63;
     auto len_of = [&](int base) -> int {              // unit base + lane's length, -1 past the end
       if (!in_regs) return base + lane < w.units ? wd_unit_len(w, base + lane) : -1;
       int v = -1;
@@ -564,13 +584,13 @@ __global__ void __launch_bounds__(kWdThreads, 1)
       for (int r = 0; r < kRegUnits; ++r) v = (base == 32 * r) ? unit_n[r] : v;
       return v;
     };
-    auto full_parts = [&](int n) { return n > 0 ? n / a.P : 0; };
+    auto full_parts = [&](int n) { return n > 0 ? n / P : 0; };
     // the tile count of a unit's partial item: 1..tmax, 0 for an empty
     // context, -1 for none (the context is whole partitions)
     auto part_tiles = [&](int n) {
       if (n < 0) return -1;
       if (n == 0) return 0;
-      const int rem = n % a.P;
+      const int rem = n % P;
       return rem == 0 ? -1 : (rem + kWdTile - 1) / kWdTile;
     };
     int *s_histA = reinterpret_cast<int *>(sm + Sh::kMiscOff + 1168);  // [65], after s_scratch
@@ -610,7 +630,7 @@ __global__ void __launch_bounds__(kWdThreads, 1)
     } else {
       for (int base = 0; base < w.units; base += 32) {
         const int n = len_of(base);
-        int np = n < 0 ? 0 : (n > 0 ? (n + a.P - 1) / a.P : 1);
+        int np = n < 0 ? 0 : (n > 0 ? (n + P - 1) / P : 1);
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) np += __shfl_xor_sync(0xffffffffu, np, o);
         total += (unsigned)np;
@@ -636,7 +656,7 @@ __global__ void __launch_bounds__(kWdThreads, 1)
             if (idx < c) {
               const int src = (int)__fns(m, 0, idx + 1);
               const int nn = __shfl_sync(0xffffffffu, n, src);
-              item = wd_make_item(w, base + src, part_of(nn), nn);
+              item = wd_make_item(w, base + src, part_of(nn), nn, P);
               return;
             }
             idx -= c;
@@ -657,12 +677,12 @@ __global__ void __launch_bounds__(kWdThreads, 1)
           const int c = m1 ? 63 - __clz(m1) : 31 - __clz(m0);
           const int t = tmax - c;
           pick(k - (unsigned)s_cumB[t], [&](int n) { return part_tiles(n) == t; },
-               [&](int n) { return n > 0 ? n / a.P : 0; });
+               [&](int n) { return n > 0 ? n / P : 0; });
         }
       } else if (k < total) {
         while (true) {
           const int n = len_of(chunk_base);
-          const int np = n < 0 ? 0 : (n > 0 ? (n + a.P - 1) / a.P : 1);
+          const int np = n < 0 ? 0 : (n > 0 ? (n + P - 1) / P : 1);
           int incl = np;
 #pragma unroll
           for (int o = 1; o < 32; o <<= 1) {
@@ -675,7 +695,7 @@ __global__ void __launch_bounds__(kWdThreads, 1)
             const int src = __ffs(hit) - 1;
             const int excl = __shfl_sync(0xffffffffu, incl - np, src);
             const int nn = __shfl_sync(0xffffffffu, n, src);
-            item = wd_make_item(w, chunk_base + src, (int)(k - chunk_cum) - excl, nn);
+            item = wd_make_item(w, chunk_base + src, (int)(k - chunk_cum) - excl, nn, P);
             break;
           }
           chunk_cum += chunk_total;
@@ -1187,7 +1207,8 @@ static pkv_status launch_wide_t(const WdArgs &w, const CUtensorMap &mq, const CU
   return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
-pkv_status launch_decode_wide(const DecodeArgs &a, pkv_dtype dt, int num_sms, cudaStream_t stream) {
+pkv_status launch_decode_wide(const DecodeArgs &a, pkv_dtype dt, int num_sms, bool auto_items,
+                              cudaStream_t stream) {
   CUtensorMap mq, mk, mv;
   const int box_tok = wd_box_tokens(a.bs, a.P);
   if (!encode_query_group_map(&mq, a.q, dt, a.B, a.H, a.D) ||
@@ -1208,6 +1229,7 @@ pkv_status launch_decode_wide(const DecodeArgs &a, pkv_dtype dt, int num_sms, cu
   w.units = a.B * a.KVH * w.hchunks;
   w.check_append = a.new_slots != nullptr;
   w.box_tok = box_tok;
+  w.auto_items = auto_items;
   // one persistent CTA per SM, never more than the items there can be
   const long long items = (long long)w.units * a.max_parts;
   const int ctas = (int)std::min<long long>(items, num_sms > 0 ? num_sms : 1);

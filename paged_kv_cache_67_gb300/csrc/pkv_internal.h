@@ -93,6 +93,7 @@ pkv_status launch_decode_tc(const DecodeArgs &a, const DecodePlan &plan, pkv_dty
 // Wide query groups (16 query heads per KV head, D of 128 or 256): the
 // persistent tensor-core decode with tokens as the product's M.
 size_t wide_smem_bytes(int D);
-pkv_status launch_decode_wide(const DecodeArgs &a, pkv_dtype dt, int num_sms, cudaStream_t stream);
+pkv_status launch_decode_wide(const DecodeArgs &a, pkv_dtype dt, int num_sms, bool auto_items,
+                              cudaStream_t stream);
 
 }  // namespace pkv
