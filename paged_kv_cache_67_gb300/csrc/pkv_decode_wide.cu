@@ -570,9 +570,8 @@ __global__ void __launch_bounds__(kWdThreads, 1)
       for (int r = 0; r < kRegUnits; ++r) tiles += unit_n[r] > 0 ? (unit_n[r] + kWdTile - 1) / kWdTile : 0;
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) tiles += __shfl_xor_sync(0xffffffffu, tiles, o);
-      const long long c = gridDim.x;
-      const long long want = (12LL * tiles + 5 * c) / (10 * c);
-      P = max(P, (int)(want < 63 ? want : 63) * kWdTile);
+      const int c = (int)gridDim.x;   // tiles <= 256 units x 64: 32-bit arithmetic
+      P = max(P, min((12 * tiles + 5 * c) / (10 * c), 63) * kWdTile);
     }
     const int maxp = a.max_parts;
     const int tmax = (P + kWdTile - 1) / kWdTile;       // tiles of a full partition
@@ -603,30 +602,63 @@ __global__ void __launch_bounds__(kWdThreads, 1)
       for (int base = 0; base < w.units; base += 32) {
         const int n = len_of(base);
         const int f = full_parts(n);
-        if (f > 0) atomicAdd(&s_histA[f], 1);   // units with f full partitions
+        if (f > 0) atomicAdd(&s_histA[f - 1], 1);   // units with f full partitions (at f - 1)
         const int t = part_tiles(n);
-        if (t >= 0) atomicAdd(&s_cumB[t], 1);   // partial items of t tiles (in place)
+        if (t >= 0) atomicAdd(&s_cumB[t], 1);       // partial items of t tiles (in place)
       }
       __syncwarp();
-      if (lane == 0) {
-        unsigned cum = 0;
-        int with = 0;  // units with a full partition p
-        for (int r = 0; r < maxp; ++r) {
-          with += s_histA[maxp - r];
-          s_cumA[r] = (int)cum;
-          cum += (unsigned)with;
+      // Prefix sums as warp scans, lane l holding entries l and l + 32 (a
+      // serial loop in one lane cost about a microsecond before the first
+      // claim).  Inclusive suffix sums first: su(i) = sum over j >= i.
+      auto suffix64 = [&](int &x0, int &x1) {
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y0 = __shfl_down_sync(0xffffffffu, x0, o), y1 = __shfl_down_sync(0xffffffffu, x1, o);
+          if (lane + o < 32) {
+            x0 += y0;
+            x1 += y1;
+          }
         }
-        s_cumA[maxp] = (int)cum;
-        for (int t = tmax; t >= 0; --t) {
-          const int h = s_cumB[t];
-          s_cumB[t] = (int)cum;
-          cum += (unsigned)h;
+        x0 += __shfl_sync(0xffffffffu, x1, 0);
+      };
+      auto at64 = [&](int x0, int x1, int i) {   // entry i (0..63) of a lane-distributed pair
+        const int a0 = __shfl_sync(0xffffffffu, x0, i & 31), a1 = __shfl_sync(0xffffffffu, x1, i & 31);
+        return i < 32 ? a0 : a1;
+      };
+      // round r (r < maxp) holds the units with at least maxp - r full
+      // partitions: su(maxp - r - 1) of the histogram over f - 1
+      int u0 = s_histA[lane], u1 = s_histA[lane + 32];
+      suffix64(u0, u1);
+      const int w0 = at64(u0, u1, max(maxp - lane - 1, 0)), w1 = at64(u0, u1, max(maxp - lane - 33, 0));
+      int c0 = lane < maxp ? w0 : 0, c1 = lane + 32 < maxp ? w1 : 0;
+      // first item number of each round: the exclusive prefix of the counts
+      int e0 = c0, e1 = c1;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y0 = __shfl_up_sync(0xffffffffu, e0, o), y1 = __shfl_up_sync(0xffffffffu, e1, o);
+        if (lane >= o) {
+          e0 += y0;
+          e1 += y1;
         }
-        s_histA[0] = (int)cum;  // the total
       }
+      const int half = __shfl_sync(0xffffffffu, e0, 31);
+      e1 += half;
+      total_full = (unsigned)__shfl_sync(0xffffffffu, e1, 31);
+      // classes by tile count, most first: first item number of count t =
+      // total_full + the partial items with more tiles
+      int b0 = s_cumB[lane], b1 = s_cumB[lane + 32];
+      int v0 = b0, v1 = b1;
+      suffix64(v0, v1);
+      total = total_full + (unsigned)__shfl_sync(0xffffffffu, v0, 0);
       __syncwarp();
-      total_full = (unsigned)s_cumA[maxp];
-      total = (unsigned)s_histA[0];
+      s_cumA[lane] = e0 - c0;
+      s_cumA[lane + 32] = e1 - c1;
+      if (lane == 0) s_cumA[64] = (int)total_full;
+      s_cumB[lane] = (int)total_full + v0 - b0;
+      s_cumB[lane + 32] = (int)total_full + v1 - b1;
+      __syncwarp();
+      if (lane == 0 && maxp < 64) s_cumA[maxp] = (int)total_full;
+      __syncwarp();
     } else {
       for (int base = 0; base < w.units; base += 32) {
         const int n = len_of(base);
