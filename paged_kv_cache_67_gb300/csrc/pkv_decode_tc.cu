@@ -246,8 +246,9 @@ __global__ void __launch_bounds__(32 * kTcWarps, 1)
     return __shfl_sync(0xffffffffu, my_phys, i & 31);
   };
   // Fetch chunk i of this warp into `slot` (warp-collective).  Lane 0 posts
-  // the byte count; lanes 0 .. 2*kBoxes-1 issue one box each (one thread
-  // issues TMA operations one after another, so they are spread over lanes).
+  // the byte count; lane 0 issues K's box, lane 1 V's: one box per tensor
+  // covers the chunk's 16 rows and all D / 64 blocks of 64 values (the TMA
+  // unit's cost is per box: a box per 64 values was the larger part of it).
   const int bs_mask = (a.bs & (a.bs - 1)) == 0 ? a.bs - 1 : -1;
   auto issue = [&](int i, int slot) {
     const int phys = phys_of(i);
@@ -257,13 +258,9 @@ __global__ void __launch_bounds__(32 * kTcWarps, 1)
     uint64_t *bar = &bars[w * S + slot];
     if (lane == 0) mbar_arrive_expect_tx(bar, Sh::kStageBytes);
     __syncwarp();
-    if (lane < 2 * Sh::kBoxes) {
-      if (lane < Sh::kBoxes)
-        tma_load_4d(st + lane * kBoxBytes, &tmK, bar, lane * kBoxElems, kvh, row0, phys, policy);
-      else
-        tma_load_4d(st + lane * kBoxBytes, &tmV, bar, (lane - Sh::kBoxes) * kBoxElems, kvh, row0,
-                    phys, policy);
-    }
+    if (lane < 2)
+      tma_load_5d(st + lane * Sh::kBoxes * kBoxBytes, lane ? &tmV : &tmK, bar, 0, row0, 0, kvh, phys,
+                  policy);
   };
   // The patching warp loads the new rows (and checks the slot) before
   // anything else, so that these loads overlap the first fetches and the
@@ -475,6 +472,28 @@ bool encode_cache_map(CUtensorMap *map, const void *cache, pkv_dtype dt, long lo
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Tensor map of a [num_blocks, bs, KVH, D] cache seen as 5-D, innermost first:
+// 64 values (stride 1), row in the block, block of 64 values (stride 128
+// bytes), head, block; box of 64 values x 16 rows x D / 64 blocks x 1 head x
+// 1 block, 128-byte swizzle.  A box lands as D / 64 tiles of 16 rows x 128
+// bytes, one after another: the layout of one 4-D box per 64 values, in one
+// copy.
+static bool encode_chunk_map(CUtensorMap *map, const void *cache, pkv_dtype dt,
+                             long long num_blocks, int bs, int KVH, int D) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t el = 2;
+  cuuint64_t dims[5] = {(cuuint64_t)kBoxElems, (cuuint64_t)bs, (cuuint64_t)(D / kBoxElems),
+                        (cuuint64_t)KVH, (cuuint64_t)num_blocks};
+  cuuint64_t strides[4] = {(cuuint64_t)KVH * D * el, kBoxElems * el, D * el,
+                           (cuuint64_t)bs * KVH * D * el};
+  cuuint32_t box[5] = {kBoxElems, kChunk, (cuuint32_t)(D / kBoxElems), 1, 1};
+  cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  return fn(map, map_type(dt), 5, const_cast<void *>(cache), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Tensor map of a [rows, H, D] 16-bit tensor (one row of H heads per token):
 // box of 64 elements x 1 head x box_rows rows, 128-byte swizzle; rows past
 // the end read as zero.
@@ -525,8 +544,8 @@ static pkv_status launch_tc_dt(const DecodeArgs &a, const DecodePlan &plan, cons
 pkv_status launch_decode_tc(const DecodeArgs &a, const DecodePlan &plan, pkv_dtype dt,
                             cudaStream_t stream) {
   CUtensorMap mk, mv;
-  if (!encode_cache_map(&mk, a.k_cache, dt, a.num_blocks, a.bs, a.KVH, a.D) ||
-      !encode_cache_map(&mv, a.v_cache, dt, a.num_blocks, a.bs, a.KVH, a.D))
+  if (!encode_chunk_map(&mk, a.k_cache, dt, a.num_blocks, a.bs, a.KVH, a.D) ||
+      !encode_chunk_map(&mv, a.v_cache, dt, a.num_blocks, a.bs, a.KVH, a.D))
     return PKV_ERR_CUDA;
   if (dt == PKV_BF16) return launch_tc_dt<__nv_bfloat16>(a, plan, mk, mv, stream);
   if (dt == PKV_F16) return launch_tc_dt<__half>(a, plan, mk, mv, stream);
