@@ -186,7 +186,12 @@ __global__ void __launch_bounds__(32 * kTcWarps, 1)
   int *s_scratch = reinterpret_cast<int *>(s_l + kTcHeads);
 
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
-  const int b = blockIdx.z, hc = blockIdx.y, part = blockIdx.x;
+  // grid (max_parts, head chunks, B), or with part_major (head chunks, B,
+  // max_parts): every unit's first partitions launch first and the short or
+  // empty last ones at the end of the launch
+  const int hc = a.part_major ? blockIdx.x : blockIdx.y;
+  const int b = a.part_major ? blockIdx.y : blockIdx.z;
+  const int part = a.part_major ? blockIdx.z : blockIdx.x;
   const int kvh = hc / a.gchunks, gc = hc - kvh * a.gchunks;
   const int head0 = kvh * a.G + gc * kTcHeads;
   const int nh = min(kTcHeads, a.G - gc * kTcHeads);
@@ -196,9 +201,9 @@ __global__ void __launch_bounds__(32 * kTcWarps, 1)
   const long long s_new = kAppend ? append_slot(a, b) : -1LL;
   const int n = checked_len(a, b, part == 0 && hc == 0 && tid == 0);
   int nparts = (n + a.P - 1) / a.P;
-  if (nparts > (int)gridDim.x) {
-    if (part == (int)gridDim.x - 1 && hc == 0 && tid == 0) raise_flag(a.err, PKV_FLAG_CONTEXT_OVER_HINT);
-    nparts = gridDim.x;
+  if (nparts > a.max_parts) {
+    if (part == a.max_parts - 1 && hc == 0 && tid == 0) raise_flag(a.err, PKV_FLAG_CONTEXT_OVER_HINT);
+    nparts = a.max_parts;
   }
   if (n == 0) {
     if (part == 0) {
@@ -426,7 +431,7 @@ __global__ void __launch_bounds__(32 * kTcWarps, 1)
   }
   __syncthreads();
   finish_partition<T>(a, b, head0, nh, part, nparts, s_m, s_l, sO, Sh::kOStride, s_scratch,
-                      a.ws_cnt + (size_t)b * gridDim.y + blockIdx.y, tid, blockDim.x, CtaSync(),
+                      a.ws_cnt + (size_t)b * (a.KVH * a.gchunks) + hc, tid, blockDim.x, CtaSync(),
                       false);
 }
 
@@ -517,7 +522,9 @@ static pkv_status launch_tc_k(const DecodeArgs &a, const DecodePlan &plan, const
   auto kern = pkv_decode_tc_kernel<D, T, kAppend>;
   static int configured[64] = {0};
   if (!allow_smem(kern, plan.smem_bytes, configured)) return PKV_ERR_CUDA;
-  dim3 grid(plan.max_parts, a.KVH * plan.gchunks, a.B);
+  if (a.part_major && plan.max_parts > 65535) return PKV_ERR_UNSUPPORTED;  // the grid's z extent
+  const dim3 grid = a.part_major ? dim3(a.KVH * plan.gchunks, a.B, plan.max_parts)
+                                 : dim3(plan.max_parts, a.KVH * plan.gchunks, a.B);
   kern<<<grid, 32 * kTcWarps, plan.smem_bytes, stream>>>(mk, mv, a);
   return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }

@@ -37,8 +37,9 @@ struct DecodeArgs {
   int heads_per_cta;     // query heads one CTA serves (<= its kernel's maximum)
   int gchunks;           // ceil(G / heads_per_cta)
   int P;                 // partition size in tokens (multiple of 16)
-  int max_parts;         // partitions the grid covers per sequence (gridDim.x); workspace stride
+  int max_parts;         // partitions the grid covers per sequence; workspace stride
   int stages;            // pipeline depth per warp (TMA kernel)
+  int part_major;        // TMA kernel: grid (head chunks, B, max_parts), else (max_parts, head chunks, B)
   float scale_log2;      // scale * log2(e): scores are kept in log2 units
   // Fused append (pkv_write_decode_attention); new_slots == nullptr otherwise.
   const int64_t *new_slots;   // [B] slot of sequence b's new token, negative: none

@@ -21,6 +21,7 @@ struct DecodePlan {
   int stages;          // TMA pipeline depth per warp
   int threads;         // threads per CTA
   size_t smem_bytes;   // dynamic shared memory per CTA
+  int part_major;      // tensor-core kernel: the partition is the grid's slowest index
 };
 
 // Heads one tensor-core CTA serves (the M = 16 rows of one mma tile).
