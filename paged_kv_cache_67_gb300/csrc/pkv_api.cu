@@ -320,7 +320,7 @@ static pkv_status decode_entry(void *out, const void *q, const void *k_cache, co
                                          num_kv_heads, head_dim, (int)el, err_flags, s);
       if (st != PKV_OK) return st;
     }
-    return launch_decode_wide(a, dt, sms, partition_size == 0, s);
+    return launch_decode_wide(a, dt, sms, partition_size == 0, app != nullptr, s);
   }
   return plan.kernel ? launch_decode_tc(a, plan, dt, s) : launch_decode_simt(a, plan, dt, s);
 }

@@ -118,6 +118,7 @@ struct WdArgs {
   int check_append;    // new_slots given: check each slot against position n - 1
   int box_tok;         // tokens per K/V box: 16, 32, 64 or 128, dividing bs and P
   int auto_items;      // the partition size is the plan's own: items may be larger
+  int after_write;     // launched as the programmatic dependent of the step's pkv_write
 };
 
 // Whether the phase with the given parity has completed (never waits).
@@ -787,6 +788,10 @@ __global__ void __launch_bounds__(kWdThreads, 1)
     }
     int it = 0, loads = 0;
     bool ok = true;
+    // in the fused step this launch may start while the write kernel still
+    // runs (everything up to here, and the scheduler's claims, read only
+    // lengths, tables and queries): the cache rows are read after it is done
+    if (w.after_write) asm volatile("griddepcontrol.wait;" ::: "memory");
     while (ok) {
       const int slot = it & 1;
       ok = __all_sync(0xffffffffu, mbar_wait_bounded(&item_full[slot], (it >> 1) & 1));
@@ -1235,12 +1240,23 @@ static pkv_status launch_wide_t(const WdArgs &w, const CUtensorMap &mq, const CU
   auto kern = pkv_decode_wide_kernel<D, T>;
   static int configured[64] = {0};
   if (!allow_smem(kern, WdShape<D>::kSmem, configured)) return PKV_ERR_CUDA;
-  kern<<<ctas, kWdThreads, WdShape<D>::kSmem, stream>>>(mq, mk, mv, w);
+  cudaLaunchConfig_t cfg;
+  memset(&cfg, 0, sizeof cfg);
+  cfg.gridDim = dim3(ctas);
+  cfg.blockDim = dim3(kWdThreads);
+  cfg.dynamicSmemBytes = WdShape<D>::kSmem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = w.after_write ? 1 : 0;
+  if (cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, w) != cudaSuccess) return PKV_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
 pkv_status launch_decode_wide(const DecodeArgs &a, pkv_dtype dt, int num_sms, bool auto_items,
-                              cudaStream_t stream) {
+                              bool after_write, cudaStream_t stream) {
   CUtensorMap mq, mk, mv;
   const int box_tok = wd_box_tokens(a.bs, a.P);
   if (!encode_query_group_map(&mq, a.q, dt, a.B, a.H, a.D) ||
@@ -1262,6 +1278,7 @@ pkv_status launch_decode_wide(const DecodeArgs &a, pkv_dtype dt, int num_sms, bo
   w.check_append = a.new_slots != nullptr;
   w.box_tok = box_tok;
   w.auto_items = auto_items;
+  w.after_write = after_write;
   // one persistent CTA per SM, never more than the items there can be
   const long long items = (long long)w.units * a.max_parts;
   const int ctas = (int)std::min<long long>(items, num_sms > 0 ? num_sms : 1);

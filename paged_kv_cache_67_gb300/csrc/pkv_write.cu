@@ -44,6 +44,10 @@ constexpr int kWriteWarps = 4;
 template <int VEC>
 __global__ void __launch_bounds__(32 * kWriteWarps) pkv_write_kernel(const WriteArgs a) {
   using V = typename VecType<VEC>::type;
+  // a kernel launched after this one as its programmatic dependent may start
+  // now; it waits for this grid's rows before it reads them (no effect on a
+  // plain launch after)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int lane = threadIdx.x & 31;
   const int64_t t = (int64_t)blockIdx.x * kWriteWarps + (threadIdx.x >> 5);
   if (t >= a.T) return;
