@@ -253,7 +253,9 @@ PKV_API pkv_status pkv_decode_attention_static(void *out, const void *q, const v
  * directly, so it does not wait for its own cache write; one CTA per
  * (sequence, KV head) writes the cache row.  (Shapes that run the
  * wide-group kernel -- see pkv_decode_attention -- make this two launches:
- * pkv_write's kernel, then that decode kernel, which checks the slots.)  The
+ * pkv_write's kernel, then that decode kernel, which checks the slots; the
+ * decode is launched as the write's programmatic dependent, so its set-up
+ * overlaps the write and only its cache reads wait for it.)  The
  * cache ends bit-identical to pkv_write's; the output is bit-identical to
  * pkv_write + pkv_decode_attention with the same partition size.
  * Additional requirements: k, v, k_cache, v_cache 16-byte aligned;
