@@ -251,12 +251,17 @@ def test_full_size_llama8b_step_sampled():
         assert_close(out[b], want[b], cfg.dtype, f"sequence {b}")
 
 
-def test_step_loop_fused_in_cuda_graph():
+@pytest.mark.parametrize("name", ["step", "mqa"])
+def test_step_loop_fused_in_cuda_graph(name):
     """The per-step loop with the fused launch: every step's launch captured
     in one CUDA graph (each step its own slice of device-resident step
     inputs), replayed once; caches and every step's output against the
-    oracle's write-then-decode sequence."""
-    cfg = wl.small_variant(wl.CONFIGS["step_bf16"], B=16, len_hi=300, steps=6)
+    oracle's write-then-decode sequence.  "mqa" runs the wide-group kernel,
+    whose decode is the write kernel's programmatic dependent and reads the
+    new rows from the cache: each step must see its own write (contexts up
+    to 2500 tokens, so some are split and merged)."""
+    cfg = (wl.small_variant(wl.CONFIGS["step_bf16"], B=16, len_hi=300, steps=6) if name == "step" else
+           wl.small_variant(wl.CONFIGS["mqa_bf16"], B=12, len_hi=2500, steps=5))
     inp = wl.make_decode_inputs(cfg, seed=97)
     st = wl.make_steps(inp, seed=98)
     B, H, D = cfg.B, cfg.H, cfg.D
@@ -267,6 +272,8 @@ def test_step_loop_fused_in_cuda_graph():
     err = torch.zeros(1, dtype=torch.int32, device=DEV)
     cap = cfg.table_width * cfg.bs
     ws = pkv.DecodeWorkspace(B, H, cfg.KVH, D, cfg.bs, cfg.table_width, cap, 0, device=DEV)
+    kern = pkv.pkv_decode_plan(B, H, cfg.KVH, D, cfg.bs, cfg.table_width, cap, dtype=cfg.dtype)[2]
+    assert kern == (2 if name == "mqa" else 1)
 
     def step(s):
         pkv.pkv_write_decode_attention(outs[s], d_q[s], d_k[s], d_v[s], d_slots[s], kc, vc,
