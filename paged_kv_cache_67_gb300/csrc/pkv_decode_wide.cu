@@ -24,8 +24,10 @@
 // only when some score exceeds the running max by more than 2^8.
 //
 // Work decomposition.  A work item is (sequence, KV head, 16-head chunk,
-// partition of P tokens); the grid is persistent (at most one CTA per SM)
-// and CTAs claim items from a counter in device memory: every full
+// partition of P tokens: the plan's partition size, or, when the plan chose
+// it, about 1.2 CTA shares of the batch's 128-token tiles, worked out by
+// every CTA from the lengths); the grid is persistent (at most one CTA per
+// SM) and CTAs claim items from a counter in device memory: every full
 // partition first (the latest partitions, which only long contexts have,
 // first), then the partial ones by tile count, most first -- long contexts
 // spread over SMs early and the last claims are the smallest.  7 warps:
@@ -34,10 +36,13 @@
 //              through a two-slot ring, loads the item's 16 query rows (TMA,
 //              128-byte swizzle) once the last S^T of the previous item is
 //              done;
-//   warp 0     producer: the tiled TMA loads of K and V tiles (16-token
-//              chunks of 64-column regions, 128-byte swizzle) into one ring
-//              of K-or-V slots, in the order K0, K1, V0, K2, V1, ... so keys
-//              run a tile ahead of values;
+//   warp 0     producer: the tiled TMA loads of K and V tiles (boxes of up
+//              to 128 tokens of one cache block x 64 columns, 128-byte
+//              swizzle; block-table entries read four tiles ahead) into one
+//              ring of K-or-V slots, in the order K0, K1, V0, K2, V1, ... so
+//              keys run a tile ahead of values; in the fused step it waits
+//              for the write kernel (this launch's programmatic primary)
+//              before its first cache read;
 //   warp 1     MMA issuer (one thread): S^T of the item's first two tiles,
 //              then per tile, once its P^T is written: O^T += V^T . P^T and
 //              the S^T two tiles ahead into the freed score buffer; frees
