@@ -102,21 +102,31 @@ def decode_traffic(kernel, workload):
         return None
 
 
+def code_only(text):
+    """C/C++/CUDA source without its comments and with whitespace runs
+    collapsed: what the compiler sees, so that a comment edit does not read
+    as a kernel change."""
+    import re
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def sources_sha256():
     """Digest of what the decode kernels' launches are built from: the
     tensor-core kernel's file, the shared device header and the plan
-    (partition choice) in the API file."""
+    (partition choice) in the API file, comments left out."""
     import hashlib
     import re
     csrc = os.path.join(ROOT, "paged_kv_cache_67_gb300", "csrc")
     h = hashlib.sha256()
     for f in ("pkv_decode_tc.cu", "pkv_device.cuh"):
-        with open(os.path.join(csrc, f), "rb") as fh:
-            h.update(fh.read())
-    with open(os.path.join(csrc, "pkv_api.cu")) as fh:
+        with open(os.path.join(csrc, f), encoding="utf-8") as fh:
+            h.update(code_only(fh.read()).encode())
+    with open(os.path.join(csrc, "pkv_api.cu"), encoding="utf-8") as fh:
         api = fh.read()
     m = re.search(r"\nbool make_plan\(.*?\n}\n", api, re.S)
-    h.update((m.group(0) if m else api).encode())
+    h.update(code_only(m.group(0) if m else api).encode())
     return h.hexdigest()
 
 

@@ -14,14 +14,16 @@
 // partitioned (v2) variant, section 深入原理, is the split into work items.
 //
 // Work decomposition.  CTA = (partition of the context, KV head x chunk of
-// <= 16 query heads, sequence); 4 warps.  A partition is split into 16-token
-// chunks (block_size is a multiple of 16, so a chunk never spans two
-// physical blocks); warp w takes chunks w, w+4, w+8, ...  Each warp has its
-// own ring of `stages` shared-memory slots; lanes 0..2*D/64-1 fetch a chunk's
-// K and V rows of this KV head with one tiled 4-D TMA load each (box 64
-// elements x 1 head x 16 rows x 1 block, 128-byte swizzle, L2 evict-first)
-// completing on the slot's mbarrier; the table entries come from one
-// coalesced load per 32 chunks, broadcast by shuffle.
+// <= 16 query heads, sequence); 4 warps; with fewer such units than resident
+// CTA slots the partition is the grid's slowest index (first partitions
+// launch first).  A partition is split into 16-token chunks (block_size is a
+// multiple of 16, so a chunk never spans two physical blocks); warp w takes
+// chunks w, w+4, w+8, ...  Each warp has its own ring of `stages`
+// shared-memory slots; lanes 0 and 1 fetch a chunk's K and V rows of this KV
+// head with one tiled 5-D TMA load each (box 64 elements x 16 rows x D/64
+// blocks of 64 elements x 1 head x 1 block, 128-byte swizzle, L2
+// evict-first) completing on the slot's mbarrier; the table entries come
+// from one coalesced load per 32 chunks, broadcast by shuffle.
 //
 // Per chunk, per warp (the query group padded to the 16 rows of one tile):
 //   S[16 x 16]  = Qgroup[16 x D] . K^T        D/16 mma, K via ldmatrix
