@@ -180,8 +180,13 @@ PKV_API size_t pkv_decode_workspace_size(int B, int H, int num_kv_heads, int hea
  * head_dim 128 or 256 (MQA-like) the wide-group kernel (persistent, one CTA
  * per SM claiming (sequence, KV head, partition) items from a device
  * counter; 5th-generation tensor cores with the KV tile's tokens as the
- * product's M), the others the TMA + mma.sync kernel; every other supported
- * shape runs the CUDA-core kernel.
+ * product's M; with partition_size 0 its items may be larger than the
+ * plan's partition -- about 1.2 CTA shares of the batch's 128-token tiles,
+ * worked out on the device from context_lens -- never smaller, so the
+ * workspace the plan sizes always holds them), the others the TMA +
+ * mma.sync kernel; every other supported shape runs the CUDA-core kernel.
+ * An explicit partition_size is used as given.  The output does not depend
+ * on the partitioning beyond fp32 rounding order.
  * Errors: PKV_ERR_INVALID_ARG, PKV_ERR_UNSUPPORTED, PKV_ERR_WORKSPACE,
  * PKV_ERR_CUDA.  B == 0 enqueues nothing.
  */
@@ -345,7 +350,9 @@ PKV_API pkv_status pkv_decode_attention_xpacked(
 /*
  * pkv_decode_plan -- the partition size and the partitions per sequence that
  * pkv_decode_attention would use for these arguments on a GPU with
- * num_sms SMs (host only, no CUDA call; for tests and tuning).  Returns the
+ * num_sms SMs (host only, no CUDA call; for tests and tuning; on the
+ * wide-group kernel with partition_size 0, the floor of its item size and
+ * the most partitions a sequence can have).  Returns the
  * partition size in tokens (>= 16), or 0 for invalid sizes; *kernel is set to
  * 2 for the wide-group tensor-core kernel, 1 for the TMA + mma.sync
  * tensor-core kernel, 0 for the CUDA-core kernel.
