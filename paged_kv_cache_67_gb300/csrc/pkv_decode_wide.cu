@@ -571,12 +571,15 @@ __global__ void __launch_bounds__(kWdThreads, 1)
     // computes the same P from the same lengths.
     int P = a.P;
     if (w.auto_items && in_regs) {
-      int tiles = 0;
+      int tiles = 0;   // this lane's units (<= 8 x 2^24 tiles)
 #pragma unroll
       for (int r = 0; r < kRegUnits; ++r) tiles += unit_n[r] > 0 ? (unit_n[r] + kWdTile - 1) / kWdTile : 0;
+      // saturated before the sum, which then stays far inside 32 bits: a lane
+      // past 2^20 tiles already puts the item size at its 63-tile cap
+      tiles = min(tiles, 1 << 20);
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) tiles += __shfl_xor_sync(0xffffffffu, tiles, o);
-      const int c = (int)gridDim.x;   // tiles <= 256 units x 64: 32-bit arithmetic
+      const int c = (int)gridDim.x;
       P = max(P, min((12 * tiles + 5 * c) / (10 * c), 63) * kWdTile);
     }
     const int maxp = a.max_parts;
