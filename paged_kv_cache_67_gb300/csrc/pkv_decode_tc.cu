@@ -524,10 +524,11 @@ static pkv_status launch_tc_k(const DecodeArgs &a, const DecodePlan &plan, const
   auto kern = pkv_decode_tc_kernel<D, T, kAppend>;
   static int configured[64] = {0};
   if (!allow_smem(kern, plan.smem_bytes, configured)) return PKV_ERR_CUDA;
-  if (a.part_major && plan.max_parts > 65535) return PKV_ERR_UNSUPPORTED;  // the grid's z extent
-  const dim3 grid = a.part_major ? dim3(a.KVH * plan.gchunks, a.B, plan.max_parts)
-                                 : dim3(plan.max_parts, a.KVH * plan.gchunks, a.B);
-  kern<<<grid, 32 * kTcWarps, plan.smem_bytes, stream>>>(mk, mv, a);
+  DecodeArgs args = a;
+  if (plan.max_parts > 65535) args.part_major = 0;  // past the grid's z extent: unit-major
+  const dim3 grid = args.part_major ? dim3(a.KVH * plan.gchunks, a.B, plan.max_parts)
+                                    : dim3(plan.max_parts, a.KVH * plan.gchunks, a.B);
+  kern<<<grid, 32 * kTcWarps, plan.smem_bytes, stream>>>(mk, mv, args);
   return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
