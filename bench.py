@@ -140,34 +140,46 @@ def hbm_peak():
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle samples while the timed region runs."""
+    """nvidia-smi clock and throttle samples, each stamped with the host's
+    monotonic clock, from before the first warm-up to the end of the run.
+    A timed region reports the samples inside it plus the nearest one on
+    each side of it, so a region shorter than the sampling period (20 steps
+    of ~0.1 ms) still has two.  Read-only queries: no GPU setting changes."""
 
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
+    def __init__(self, gpu_index: int, period_ms: int = 50):
         self.gpu = gpu_index
+        self.period_ms = period_ms
         self.proc = None
-        self.lines = []
+        self.thread = None
+        self.samples = []     # (monotonic seconds, csv line)
+        self.lock = threading.Lock()
 
-    def __enter__(self):
+    def start(self, wait_s: float = 5.0):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "50"],
+                 "--format=csv,noheader,nounits", "-lms", str(self.period_ms)],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
         except Exception:
             self.proc = None
+            return self
+        t_end = time.monotonic() + wait_s
+        while time.monotonic() < t_end and not self.samples and self.proc.poll() is None:
+            time.sleep(0.01)
         return self
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            with self.lock:
+                self.samples.append((time.monotonic(), line.strip()))
 
-    def __exit__(self, *exc):
+    def stop(self):
         if self.proc is not None:
             self.proc.terminate()
             try:
@@ -175,11 +187,38 @@ class ClockSampler:
             except Exception:
                 self.proc.kill()
             self.thread.join(timeout=5)
+            self.proc = None
 
-    def summary(self):
+    def __enter__(self):
+        return self.start()
+
+    def __exit__(self, *exc):
+        self.stop()
+
+    def window(self, t0: float, t1: float, wait_s: float = 2.0):
+        """Summary of the samples taken between t0 and t1 (monotonic), with
+        the last one before t0 and the first one after t1 (waited for)."""
+        if self.proc is not None:
+            t_end = time.monotonic() + wait_s
+            while time.monotonic() < t_end and self.proc.poll() is None:
+                with self.lock:
+                    if self.samples and self.samples[-1][0] > t1:
+                        break
+                time.sleep(0.005)
+        with self.lock:
+            samples = list(self.samples)
+        inside = [ln for ts, ln in samples if t0 <= ts <= t1]
+        before = [ln for ts, ln in samples if ts < t0][-1:]
+        after = [ln for ts, ln in samples if ts > t1][:1]
+        out = self.summarize(before + inside + after)
+        out["inside_region"] = len(inside)
+        return out
+
+    @staticmethod
+    def summarize(lines):
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in self.lines:
+        for line in lines:
             parts = [p.strip() for p in line.split(",")]
             if len(parts) < 8:
                 continue
@@ -322,8 +361,7 @@ def run_reference(args, world, rank):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(dt / max(args.steps, 1) * 1e3, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": dict(config_block(args.workload, args.mode),
-                       sample=f"{threads} (sequence, KV head) units per step"),
+        "config": config_block(args.workload, args.mode),
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads,
                          "kind": "oracle",
                          "sample": f"{threads} (sequence, KV head) units per step, rotating"},
@@ -334,6 +372,10 @@ def run_reference(args, world, rank):
 
 
 # -------------------------------------------------------------- GPU (lib)
+
+DECODE_CONFIG_ORDER = ("long_bf16", "mqa_bf16", "step_bf16", "tiny_fp32")
+KERNEL_CHOICES = {"auto": -1, "cuda-core": 0, "tc": 1, "wide": 2}
+
 
 def make_step_inputs(cfg, inp, rank, dev, elem):
     """Device inputs of each distinct step (one for a single-step workload:
@@ -359,15 +401,248 @@ def make_step_inputs(cfg, inp, rank, dev, elem):
     return steps
 
 
-def kernel_name(cfg, mode):
+def max_context(cfg):
+    """The host-side bound on the context lengths the bench passes as
+    max_context_len: the longest first-step context, plus the appended
+    tokens of a multi-step workload."""
+    return cfg.len_hi + (cfg.steps if cfg.steps > 1 else 0)
+
+
+def kernel_name(cfg, mode, kernel=-1):
     import paged_kv_cache_67_gb300 as pkv
     P, _, kern = pkv.pkv_decode_plan(cfg.B, cfg.H, cfg.KVH, cfg.D, cfg.bs, cfg.table_width,
-                                     dtype=cfg.dtype)
+                                     max_context(cfg), dtype=cfg.dtype)
+    if kernel >= 0:
+        kern = kernel
     t = {torch.bfloat16: "bf16", torch.float16: "fp16", torch.float32: "fp32"}[cfg.dtype]
     if kern == 2:  # the fused step on this kernel is pkv_write followed by it
         return f"pkv_decode_wide_kernel<{cfg.D}, {t}>"
     base = f"pkv_decode_tc_kernel<{cfg.D}, {t}" if kern == 1 else f"pkv_decode_simt_kernel<{t}"
     return base + (", append>" if mode == "fused" else ">")
+
+
+def l2_bytes(dev):
+    try:
+        return int(torch.cuda.get_device_properties(dev).L2_cache_size)
+    except Exception:
+        return 126 * 2**20
+
+
+class DecodeRun:
+    """One decode workload on the GPU, as the bench times it: `copies`
+    independent input sets (each with its cache pool, tables, queries and
+    the step inputs) cycled step by step, one output buffer, one workspace.
+    A step is pkv_write_decode_attention (mode "fused") or pkv_write then
+    pkv_decode_attention (mode "two-launch", where `kernel` >= 0 names the
+    decode kernel); layout "xpacked" runs the packed-layout pair."""
+
+    def __init__(self, pkv, name, dev, rank, mode="fused", kernel=-1, copies=1,
+                 layout="token-major"):
+        self.pkv, self.name, self.dev = pkv, name, dev
+        self.cfg = cfg = wl.CONFIGS[name]
+        self.elem = torch.empty((), dtype=cfg.dtype).element_size()
+        self.mode, self.kernel, self.layout = mode, kernel, layout
+        self.fused = mode == "fused" and layout == "token-major"
+        self.sets = []
+        for c in range(copies):
+            seed = 1234 + rank + 7919 * c
+            inp = wl.make_decode_inputs(cfg, seed=seed, device=dev)
+            steps = make_step_inputs(cfg, inp, rank + 7919 * c, dev, self.elem)
+            kx = vx = None
+            if layout == "xpacked":
+                nb = inp.k_cache.shape[0]
+                kx = inp.k_cache.view(nb, cfg.bs, cfg.KVH, cfg.D // 8, 8).permute(0, 2, 3, 1, 4).contiguous()
+                vx = inp.v_cache.permute(0, 2, 3, 1).contiguous()
+            self.sets.append(dict(inp=inp, steps=steps, kx=kx, vx=vx))
+        self.order = [(c, s) for s in range(len(self.sets[0]["steps"])) for c in range(copies)]
+        self.inp = self.sets[0]["inp"]
+        self.out = torch.empty_like(self.inp.q)
+        self.err = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.max_ctx = max_context(cfg)
+        self.ws = pkv.DecodeWorkspace(cfg.B, cfg.H, cfg.KVH, cfg.D, cfg.bs, cfg.table_width,
+                                      self.max_ctx, 0, device=dev)
+        self.kname = (kernel_name(cfg, mode, kernel) if layout == "token-major" else
+                      f"pkv_decode_xpacked_kernel<{cfg.D}, bf16>")
+        wide = layout == "token-major" and self.kname.startswith("pkv_decode_wide")
+        # launches per step: the fused entry is one, except on the wide-group
+        # kernel (pkv_write, then the decode as its programmatic dependent)
+        self.launches_per_step = 1 if self.fused and not wide else 2
+        self.wide_fused = self.fused and wide
+
+    def entry(self, i):
+        c, s = self.order[i % len(self.order)]
+        return self.sets[c], self.sets[c]["steps"][s]
+
+    def step_bytes(self, i):
+        _, st = self.entry(i)
+        return st["dec"] + st["wr"]
+
+    def kernel_bytes(self, i):
+        """Algorithmic bytes of the timed decode launch (the write's too when
+        the step is fused)."""
+        _, st = self.entry(i)
+        return st["dec"] + (st["wr"] if self.fused else 0)
+
+    def write(self, i, stream):
+        set_, st = self.entry(i)
+        inp = set_["inp"]
+        if set_["kx"] is not None:
+            self.pkv.pkv_write_xpacked(set_["kx"], set_["vx"], st["k"], st["v"], st["slots"],
+                                       err_flags=self.err, stream=stream)
+        else:
+            self.pkv.pkv_write(inp.k_cache, inp.v_cache, st["k"], st["v"], st["slots"],
+                               err_flags=self.err, stream=stream)
+
+    def decode(self, i, stream):
+        pkv = self.pkv
+        set_, st = self.entry(i)
+        inp = set_["inp"]
+        kw = dict(max_context_len=self.max_ctx, workspace=self.ws, err_flags=self.err, stream=stream)
+        if set_["kx"] is not None:
+            pkv.pkv_decode_attention_xpacked(self.out, st["q"], set_["kx"], set_["vx"], st["tables"],
+                                             st["lens"], inp.scale, **kw)
+        elif self.fused:
+            pkv.pkv_write_decode_attention(self.out, st["q"], st["k"], st["v"], st["slots"],
+                                           inp.k_cache, inp.v_cache, st["tables"], st["lens"],
+                                           inp.scale, **kw)
+        elif self.kernel >= 0:
+            pkv.pkv_decode_attention_with_kernel(self.out, st["q"], inp.k_cache, inp.v_cache,
+                                                 st["tables"], st["lens"], inp.scale, self.kernel, **kw)
+        else:
+            pkv.pkv_decode_attention(self.out, st["q"], inp.k_cache, inp.v_cache, st["tables"],
+                                     st["lens"], inp.scale, **kw)
+
+    def step(self, i, stream, ev=None):
+        if not self.fused:
+            self.write(i, stream)
+        if ev is not None:
+            ev[0].record(stream)
+        self.decode(i, stream)
+        if ev is not None:
+            ev[1].record(stream)
+
+    def check_flags(self, when):
+        if int(self.err.item()) != 0:
+            raise RuntimeError(f"{self.name}: device error flags {int(self.err.item()):#x} {when}")
+
+    def warmup(self, n, stream):
+        for i in range(max(n, len(self.order))):
+            self.step(i, stream)
+        torch.cuda.synchronize()
+        self.check_flags("during warm-up")
+
+    def time_graph(self, steps, stream, world, sampler):
+        """The timed steps captured once as a CUDA graph and replayed between
+        CUDA events on the launching stream: (elapsed s, clocks)."""
+        cap = torch.cuda.Stream(self.dev)
+        cap.wait_stream(stream)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(cap):
+            with torch.cuda.graph(graph, stream=cap):
+                for i in range(steps):
+                    self.step(i, cap)
+        torch.cuda.synchronize()
+        t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier(world)
+        torch.cuda.synchronize()
+        h0 = time.monotonic()
+        t_start.record(stream)
+        graph.replay()
+        t_end.record(stream)
+        torch.cuda.synchronize()
+        h1 = time.monotonic()
+        barrier(world)
+        self.check_flags("in the timed region")
+        del graph
+        return t_start.elapsed_time(t_end) * 1e-3, sampler.window(h0, h1)
+
+    def time_launches(self, steps, stream, world, sampler, flush=None):
+        """Every timed step launched from the host, the decode launch between
+        its own CUDA events on its stream; with `flush` (a buffer larger than
+        L2) the buffer is rewritten before every step, outside the events.
+        Returns (elapsed s, mean decode ms, median decode ms, clocks)."""
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(steps)]
+        t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier(world)
+        torch.cuda.synchronize()
+        h0 = time.monotonic()
+        t_start.record(stream)
+        for i in range(steps):
+            if flush is not None:
+                flush.add_(1)
+            self.step(i, stream, evs[i])
+        t_end.record(stream)
+        torch.cuda.synchronize()
+        h1 = time.monotonic()
+        barrier(world)
+        self.check_flags("in the timed region")
+        ms = [a.elapsed_time(b) for a, b in evs]
+        return (t_start.elapsed_time(t_end) * 1e-3, statistics.mean(ms), statistics.median(ms),
+                sampler.window(h0, h1))
+
+
+def config_entry(run, args, stream, world, sampler, peak, flush):
+    """One workload of the `configs` block: its decode kernel timed at the
+    run's K and W, against the HBM peak.  Without `flush` the timed steps
+    are replayed from one CUDA graph (the run's input sets, cycled, are
+    larger than L2); with it every step is launched from the host after the
+    L2 is flushed."""
+    run.warmup(args.warmup, stream)
+    cycle_bytes = sum(run.step_bytes(i) for i in range(len(run.order)))
+    if not flush:
+        elapsed, clocks = run.time_graph(args.steps, stream, world, sampler)
+        kern_ms = elapsed * 1e3 / args.steps
+        timing = (f"{args.steps} steps replayed from one CUDA graph; "
+                  + (f"{len(run.sets)} independent input sets cycled, " if len(run.sets) > 1 else "")
+                  + f"inputs larger than L2 ({cycle_bytes / len(run.order) / 1e6:.0f} MB per step"
+                  + (f", {cycle_bytes / 1e6:.0f} MB per cycle" if len(run.sets) > 1 else "")
+                  + "), no flush")
+    else:
+        buf = torch.zeros(2 * l2_bytes(run.dev) // 4 + 1, dtype=torch.float32, device=run.dev)
+        elapsed, _, kern_ms, clocks = run.time_launches(args.steps, stream, world, sampler, buf)
+        timing = (f"{args.steps} host-launched steps, a {buf.numel() * 4 / 1e6:.0f} MB buffer "
+                  f"rewritten before each (L2 flush), CUDA events around each decode launch "
+                  f"(median)")
+        del buf
+    kb = statistics.mean(run.kernel_bytes(i) for i in range(args.steps))
+    achieved = kb / (kern_ms * 1e-3) / 1e9
+    return {
+        "workload": f"{run.name}: {WORKLOAD_TEXT[run.name]}",
+        "step": ("pkv_write_decode_attention" if run.fused else "pkv_write + pkv_decode_attention")
+                + (" (on this kernel: pkv_write, then the decode as its programmatic dependent; "
+                   "both in the timed span)" if run.wide_fused else ""),
+        "kernel": run.kname, "kernel_us": round(kern_ms * 1e3, 2),
+        "bytes_per_launch": round(kb), "achieved": round(achieved, 1), "unit": "GB/s",
+        "peak": peak, "frac": round(achieved / peak, 4), "bound": "hbm",
+        "traffic": decode_traffic(run.kname, run.name),
+        "ms_per_step": round(elapsed * 1e3 / args.steps, 4), "timing": timing,
+        "gpu_launches": args.steps * run.launches_per_step, "clocks": clocks,
+    }
+
+
+def measure_copy(pkv, dev, stream):
+    """In-run copy bandwidth of 1 GiB buffers: the library's own copy kernel
+    (pkv_hbm_copy), and torch's copy_ for context; read + write bytes."""
+    src = torch.empty(1 << 30, dtype=torch.uint8, device=dev)
+    dst = torch.empty_like(src)
+    res = {}
+    for name, fn in (("pkv_hbm_copy", lambda: pkv.pkv_hbm_copy(dst, src, stream=stream)),
+                     ("torch_copy", lambda: dst.copy_(src))):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(10)]
+        for a, b in evs:
+            a.record(stream)
+            fn()
+            b.record(stream)
+        torch.cuda.synchronize()
+        ms = min(a.elapsed_time(b) for a, b in evs)
+        res[name] = round(2 * src.numel() / (ms * 1e-3) / 1e9, 1)
+    del src, dst
+    return res
 
 
 def run_gpu(args, world, rank, local):
@@ -377,67 +652,28 @@ def run_gpu(args, world, rank, local):
     libbuild.build()
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    cfg = wl.CONFIGS[args.workload]
-    elem = torch.empty((), dtype=cfg.dtype).element_size()
-    inp = wl.make_decode_inputs(cfg, seed=1234 + rank, device=dev)
-    steps = make_step_inputs(cfg, inp, rank, dev, elem)
-    S = len(steps)
-    out = torch.empty_like(inp.q)
-    err = torch.zeros(1, dtype=torch.int32, device=dev)
-    max_ctx = cfg.len_hi + (cfg.steps if cfg.steps > 1 else 0)
-    ws = pkv.DecodeWorkspace(cfg.B, cfg.H, cfg.KVH, cfg.D, cfg.bs, cfg.table_width, max_ctx, 0,
-                             device=dev)
     stream = torch.cuda.current_stream(dev)
-    fused = args.mode == "fused" and args.layout == "token-major"
     peak, peak_kind = hbm_peak()
-    kx = vx = None
-    if args.layout == "xpacked":
-        # the layout experiment: the same values in vLLM's packed layout
-        nb = inp.k_cache.shape[0]
-        kx = inp.k_cache.view(nb, cfg.bs, cfg.KVH, cfg.D // 8, 8).permute(0, 2, 3, 1, 4).contiguous()
-        vx = inp.v_cache.permute(0, 2, 3, 1).contiguous()
+    sampler = ClockSampler(local).start()
+    try:
+        return _run_gpu(args, world, rank, dev, stream, peak, peak_kind, sampler, pkv)
+    finally:
+        sampler.stop()
 
-    def write(st):
-        if kx is not None:
-            pkv.pkv_write_xpacked(kx, vx, st["k"], st["v"], st["slots"], err_flags=err, stream=stream)
-            return
-        pkv.pkv_write(inp.k_cache, inp.v_cache, st["k"], st["v"], st["slots"], err_flags=err,
-                      stream=stream)
 
-    def decode(st):
-        if kx is not None:
-            pkv.pkv_decode_attention_xpacked(out, st["q"], kx, vx, st["tables"], st["lens"], inp.scale,
-                                             max_context_len=max_ctx, workspace=ws, err_flags=err,
-                                             stream=stream)
-        elif fused:
-            pkv.pkv_write_decode_attention(out, st["q"], st["k"], st["v"], st["slots"],
-                                           inp.k_cache, inp.v_cache, st["tables"], st["lens"],
-                                           inp.scale, max_context_len=max_ctx, workspace=ws,
-                                           err_flags=err, stream=stream)
-        else:
-            pkv.pkv_decode_attention(out, st["q"], inp.k_cache, inp.v_cache, st["tables"],
-                                     st["lens"], inp.scale, max_context_len=max_ctx,
-                                     workspace=ws, err_flags=err, stream=stream)
-
-    def step(i, ev=None):
-        st = steps[i % S]
-        if not fused:
-            write(st)
-        if ev is not None:
-            ev[0].record(stream)
-        decode(st)
-        if ev is not None:
-            ev[1].record(stream)
-
+def _run_gpu(args, world, rank, dev, stream, peak, peak_kind, sampler, pkv):
+    run = DecodeRun(pkv, args.workload, dev, rank, mode=args.mode,
+                    kernel=KERNEL_CHOICES[args.kernel], layout=args.layout)
+    cfg, inp = run.cfg, run.inp
     extra = {}
     if not args.only_decode:
         # write_kv on a bulk fill (every context token of the batch): GB/s
         bulk = wl.make_bulk_fill(inp, seed=99 + rank, device=dev)
-        bulk_bytes = wl.write_bytes(bulk.slot_mapping, cfg.KVH, cfg.D, elem)
+        bulk_bytes = wl.write_bytes(bulk.slot_mapping, cfg.KVH, cfg.D, run.elem)
 
         def bulk_write():
             pkv.pkv_write(inp.k_cache, inp.v_cache, bulk.k, bulk.v, bulk.slot_mapping,
-                          err_flags=err, stream=stream)
+                          err_flags=run.err, stream=stream)
 
         for _ in range(3):
             bulk_write()
@@ -456,134 +692,115 @@ def run_gpu(args, world, rank, local):
                              "bytes": bulk_bytes, "us": round(bulk_ms * 1e3, 2),
                              "what": "bulk fill: every context token of the workload, random order"}
         del bulk  # the pool now holds the bulk-fill values; the decode reads those
+        copy = measure_copy(pkv, dev, stream)
+        extra["hbm_copy_gbs_in_run"] = copy["pkv_hbm_copy"]
+        extra["hbm_copy_in_run"] = {"pkv_hbm_copy_gbs": copy["pkv_hbm_copy"],
+                                    "torch_copy_gbs": copy["torch_copy"],
+                                    "what": "1 GiB buffers, read + write bytes, best of 10, "
+                                            "pkv_hbm_copy is the library's own copy kernel"}
 
-        # in-run copy bandwidth of a 1 GiB buffer (context for the measured peak)
-        src = torch.empty(1 << 29, dtype=torch.bfloat16, device=dev)
-        dst = torch.empty_like(src)
-        for _ in range(3):
-            dst.copy_(src)
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(10):
-            dst.copy_(src)
-        e1.record(stream)
-        torch.cuda.synchronize()
-        extra["hbm_copy_gbs_in_run"] = round(10 * 2 * src.numel() * 2 / (e0.elapsed_time(e1) * 1e-3) / 1e9, 1)
-        del src, dst
-
-    # warm-up (every distinct step at least once)
-    for i in range(max(args.warmup, S)):
-        step(i)
-    torch.cuda.synchronize()
-    if int(err.item()) != 0:
-        raise RuntimeError(f"device error flags {int(err.item()):#x} during warm-up")
-
-    graph = None
+    run.warmup(args.warmup, stream)
     if args.graph:
-        # the K timed steps as one CUDA graph (captured on a side stream)
-        cap = torch.cuda.Stream(dev)
-        cap.wait_stream(stream)
-        graph = torch.cuda.CUDAGraph()
-        outer = stream
-        with torch.cuda.stream(cap):
-            stream = cap
-            with torch.cuda.graph(graph, stream=cap):
-                for i in range(args.steps):
-                    step(i)
-            stream = outer
-        torch.cuda.synchronize()
-
-    # timed region: K steps; each decode launch bracketed by events on its stream
-    dec_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(args.steps)]
-    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier(world)
-    torch.cuda.synchronize()
-    torch.cuda.nvtx.range_push("timed")
-    with ClockSampler(local) as clocks:
-        t_start.record(stream)
-        if graph is not None:
-            graph.replay()
-        else:
-            for i in range(args.steps):
-                step(i, dec_ev[i])
-        t_end.record(stream)
-        torch.cuda.synchronize()
-    torch.cuda.nvtx.range_pop()
-    barrier(world)
-    elapsed = t_start.elapsed_time(t_end) * 1e-3
-    if graph is None:
-        dec_ms = statistics.mean(a.elapsed_time(b) for a, b in dec_ev)
-    else:
+        elapsed, clocks = run.time_graph(args.steps, stream, world, sampler)
         dec_ms = elapsed * 1e3 / args.steps  # back-to-back graph nodes: the per-step time
-    # the fused entry is one launch, except on the wide-group kernel, where it
-    # runs pkv_write first (two launches, both inside the per-step events)
-    wide = kx is None and kernel_name(cfg, args.mode).startswith("pkv_decode_wide")
-    launches = args.steps * (1 if fused and not wide else 2)
-    if int(err.item()) != 0:
-        raise RuntimeError(f"device error flags {int(err.item()):#x} in the timed region")
-    step_bytes = [steps[i % S]["dec"] + steps[i % S]["wr"] for i in range(args.steps)]
+    else:
+        elapsed, dec_ms, _, clocks = run.time_launches(args.steps, stream, world, sampler)
+    step_bytes = [run.step_bytes(i) for i in range(args.steps)]
     value, tmax, _ = aggregate(elapsed, sum(step_bytes) / 1e9, world, dev)
-    # the timed kernel's algorithmic bytes: the fused launch does the write too
-    kern_bytes = statistics.mean(steps[i % S]["dec"] + (steps[i % S]["wr"] if fused else 0)
-                                 for i in range(args.steps))
-    dec_bytes = statistics.mean(st["dec"] for st in steps)
-    wr_bytes = statistics.mean(st["wr"] for st in steps)
+    kern_bytes = statistics.mean(run.kernel_bytes(i) for i in range(args.steps))
+    dec_bytes = statistics.mean(st["dec"] for st in run.sets[0]["steps"])
+    wr_bytes = statistics.mean(st["wr"] for st in run.sets[0]["steps"])
 
     e2e = None
     if not args.only_decode:
-        e2e = run_e2e(args, world, dev, pkv, inp, steps, out, ws, err, stream, max_ctx, fused,
-                      sum(step_bytes))
+        e2e = run_e2e(args, world, dev, pkv, run, stream, sum(step_bytes))
 
     achieved = kern_bytes / (dec_ms * 1e-3) / 1e9
+    configs = None
+    if args.configs == "all" and not args.only_decode and args.layout == "token-major":
+        configs = run_configs(args, world, rank, dev, stream, peak, sampler, pkv, exclude=args.workload)
     if rank != 0:
         return None
     cpu = None
     if world == 1 and not args.only_decode and not args.no_cpu_baseline:
-        cpu = cpu_baseline(inp, elem)
-    kname = (kernel_name(cfg, args.mode) if kx is None else
-             f"pkv_decode_xpacked_kernel<{cfg.D}, bf16>")
+        cpu = cpu_baseline(inp, run.elem)
     dt = {torch.bfloat16: "bf16", torch.float16: "fp16", torch.float32: "fp32"}[cfg.dtype]
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(tmax / args.steps * 1e3, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": dt, "data": "synthetic",
-        "config": config_block(args.workload, args.mode, round(dec_bytes), round(wr_bytes), world,
+        "config": config_block(args.workload, run.mode, round(dec_bytes), round(wr_bytes), world,
                                args.graph),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4),
-                     "traffic": decode_traffic(kname, args.workload),
-                     "kernel": kname, "bytes_per_launch": round(kern_bytes),
-                     **({"timed_span": "pkv_write + " + kname} if fused and wide else {}),
+                     "traffic": decode_traffic(run.kname, args.workload),
+                     "kernel": run.kname, "bytes_per_launch": round(kern_bytes),
+                     **({"timed_span": "pkv_write + " + run.kname} if run.wide_fused else {}),
                      "peak_source": ("measured (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
                                      else "fallback 6.8 TB/s"),
                      "kernel_us": round(dec_ms * 1e3, 2)},
         **extra,
         "e2e": e2e,
-        "gpu_launches": launches,
-        "clocks": clocks.summary(),
+        "gpu_launches": args.steps * run.launches_per_step,
+        "clocks": clocks,
         "cpu_baseline": cpu,
     }
+    if configs is not None:
+        line["configs"] = configs
     print(json.dumps(line), flush=True)
     return line
 
 
-def run_prefill(args, world, rank, local):
-    """Causal varlen prefill attention over the paged cache: TFLOP/s of the
-    tensor-core kernel against the measured bf16 matmul peak."""
-    from paged_kv_cache_67_gb300 import build as libbuild
-    import paged_kv_cache_67_gb300 as pkv
+def input_sets(cfg, rank, dev):
+    """(input sets, flush) for timing a workload without a warm L2: one set
+    when a step's bytes exceed twice L2; else enough independent sets (up to
+    four) that one cycle of them does; else one set and an L2 flush before
+    every step."""
+    elem = torch.empty((), dtype=cfg.dtype).element_size()
+    lens = wl.draw_lengths(cfg, 1234 + rank)
+    per_set = wl.decode_bytes(lens, cfg.B, cfg.H, cfg.KVH, cfg.D, cfg.bs, elem)
+    need = 2 * l2_bytes(dev)
+    if per_set > need:
+        return 1, False
+    copies = -(-need // max(per_set, 1)) + 1
+    return (copies, False) if copies <= 4 else (1, True)
 
-    libbuild.build()
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    cfg = wl.PREFILL_CONFIGS[args.workload]
+
+def run_configs(args, world, rank, dev, stream, peak, sampler, pkv, exclude):
+    """The other workloads at the same K and W: one entry each."""
+    out = {}
+    for name in DECODE_CONFIG_ORDER:
+        if name == exclude:
+            continue
+        copies, flush = input_sets(wl.CONFIGS[name], rank, dev)
+        run = DecodeRun(pkv, name, dev, rank, mode="fused", copies=copies)
+        out[name] = config_entry(run, args, stream, world, sampler, peak, flush)
+        del run
+        torch.cuda.empty_cache()
+    for name in sorted(wl.PREFILL_CONFIGS):
+        out[name] = prefill_entry(args, world, rank, dev, stream, sampler, pkv, name)
+        torch.cuda.empty_cache()
+    return out
+
+
+def prefill_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            pk = json.load(f)
+        return float(pk["bf16_tflops"]), float(pk["bf16_tflops_sustained"]), "measured"
+    except Exception:
+        return 1900.0, 1700.0, "fallback"
+
+
+def prefill_timed(args, world, rank, dev, stream, sampler, pkv, name):
+    """Causal varlen prefill over the paged cache, each launch between CUDA
+    events: (cfg, inputs, flops per launch, elapsed s, mean ms, clocks)."""
+    cfg = wl.PREFILL_CONFIGS[name]
     inp = wl.make_prefill_inputs(cfg, seed=1234 + rank, device=dev)
     tables, cu, lens = inp.block_tables.to(dev), inp.cu_seqlens_q.to(dev), inp.context_lens.to(dev)
     out = torch.empty_like(inp.q)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
-    stream = torch.cuda.current_stream(dev)
     flops = wl.prefill_flops(inp.context_lens, inp.cu_seqlens_q, cfg.H, cfg.D)
 
     def step():
@@ -598,60 +815,97 @@ def run_prefill(args, world, rank, local):
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
     torch.cuda.synchronize()
-    with ClockSampler(local) as clocks:
-        t_start.record(stream)
-        for a, b in evs:
-            a.record(stream)
-            step()
-            b.record(stream)
-        t_end.record(stream)
-        torch.cuda.synchronize()
+    h0 = time.monotonic()
+    t_start.record(stream)
+    for a, b in evs:
+        a.record(stream)
+        step()
+        b.record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    h1 = time.monotonic()
     barrier(world)
     if int(err.item()) != 0:
-        raise RuntimeError(f"device error flags {int(err.item()):#x}")
+        raise RuntimeError(f"{name}: device error flags {int(err.item()):#x}")
     elapsed = t_start.elapsed_time(t_end) * 1e-3
     k_ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    return cfg, inp, flops, elapsed, k_ms, sampler.window(h0, h1)
+
+
+def prefill_text(name, cfg, inp):
+    return (f"{name}: B={cfg.B} H={cfg.H} KVH={cfg.KVH} D={cfg.D} block_size={cfg.bs}, "
+            f"context_lens U[{cfg.len_lo},{cfg.len_hi}], even sequences prefill the whole prompt, "
+            f"odd ones a chunk of U[{cfg.chunk_lo},{cfg.chunk_hi}] queries on a cached prefix; "
+            f"{int(inp.cu_seqlens_q[-1])} queries")
+
+
+def prefill_entry(args, world, rank, dev, stream, sampler, pkv, name):
+    cfg, inp, flops, elapsed, k_ms, clocks = prefill_timed(args, world, rank, dev, stream, sampler,
+                                                           pkv, name)
+    peak, peak_s, src = prefill_peaks()
+    achieved = flops / (k_ms * 1e-3) / 1e12
+    return {"workload": prefill_text(name, cfg, inp), "step": "pkv_prefill_attention",
+            "kernel": f"pkv_prefill_tc_kernel<{cfg.D}, bf16>", "kernel_us": round(k_ms * 1e3, 2),
+            "flops_per_launch": flops, "achieved": round(achieved, 1), "unit": "TFLOP/s",
+            "peak": peak, "frac": round(achieved / peak, 4),
+            "frac_of_sustained": round(achieved / peak_s, 4), "bound": "tensor",
+            "peak_source": f"{src} (MEASURED_PEAKS.json bf16_tflops)", "traffic": None,
+            "ms_per_step": round(elapsed * 1e3 / args.steps, 4),
+            "timing": (f"{args.steps} host-launched launches, CUDA events around each (mean); "
+                       "q, out and K/V larger than L2, no flush"),
+            "gpu_launches": args.steps, "clocks": clocks}
+
+
+def run_prefill(args, world, rank, local):
+    """Causal varlen prefill attention over the paged cache: TFLOP/s of the
+    tensor-core kernel against the measured bf16 matmul peak."""
+    from paged_kv_cache_67_gb300 import build as libbuild
+    import paged_kv_cache_67_gb300 as pkv
+
+    libbuild.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream(dev)
+    sampler = ClockSampler(local).start()
+    try:
+        cfg, inp, flops, elapsed, k_ms, clocks = prefill_timed(args, world, rank, dev, stream,
+                                                               sampler, pkv, args.workload)
+    finally:
+        sampler.stop()
     value, tmax, _ = aggregate(elapsed, flops * args.steps / 1e12, world, dev)
     if rank != 0:
         return None
-    try:
-        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
-            pk = json.load(f)
-        peak, peak_s, src = float(pk["bf16_tflops"]), float(pk["bf16_tflops_sustained"]), "measured"
-    except Exception:
-        peak, peak_s, src = 1900.0, 1700.0, "fallback"
+    peak, peak_s, src = prefill_peaks()
     achieved = flops / (k_ms * 1e-3) / 1e12
     line = {
         "metric": "paged causal prefill attn achieved TFLOP/s", "value": round(value, 1),
         "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(tmax / args.steps * 1e3, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": (f"{args.workload}: B={cfg.B} H={cfg.H} KVH={cfg.KVH} D={cfg.D} "
-                                f"block_size={cfg.bs}, context_lens U[{cfg.len_lo},{cfg.len_hi}], even "
-                                f"sequences prefill the whole prompt, odd ones a chunk of "
-                                f"U[{cfg.chunk_lo},{cfg.chunk_hi}] queries on a cached prefix; "
-                                f"{int(inp.cu_seqlens_q[-1])} queries"),
+        "config": {"workload": prefill_text(args.workload, cfg, inp),
                    "flops_per_step": flops,
                    "l2": "q, out and K/V larger than L2, no flush"},
         "roofline": {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak,
                      "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
                      "frac_of_sustained": round(achieved / peak_s, 4), "traffic": None,
-                     "kernel": "pkv_prefill_tc_kernel<128, bf16>",
+                     "kernel": f"pkv_prefill_tc_kernel<{cfg.D}, bf16>",
                      "peak_source": f"{src} (MEASURED_PEAKS.json bf16_tflops)",
                      "kernel_us": round(k_ms * 1e3, 2)},
-        "e2e": None, "gpu_launches": args.steps, "clocks": clocks.summary(), "cpu_baseline": None,
+        "e2e": None, "gpu_launches": args.steps, "clocks": clocks, "cpu_baseline": None,
     }
     print(json.dumps(line), flush=True)
     return line
 
 
-def run_e2e(args, world, dev, pkv, inp, steps, out, ws, err, stream, max_ctx, fused, total_bytes):
+def run_e2e(args, world, dev, pkv, run, stream, total_bytes):
     """The same steps end to end through the public API: each step's inputs
     copied in from pinned host memory, the output read back and waited for.
 
     A step's inputs sit in one pinned host buffer (each tensor at a 256-byte
     aligned offset) and go over in one copy into a device buffer that the
     kernels read through views, the way a serving loop stages a batch."""
+    steps = run.sets[0]["steps"]
+    inp, out, ws, err, max_ctx = run.inp, run.out, run.ws, run.err, run.max_ctx
     S = len(steps)
     keys = ("q", "k", "v", "slots", "tables", "lens")
     offs, off = {}, 0
@@ -678,7 +932,7 @@ def run_e2e(args, world, dev, pkv, inp, steps, out, ws, err, stream, max_ctx, fu
 
     def e2e_step(i):
         dblob.copy_(host[i % S], non_blocking=True)
-        if fused:
+        if run.fused:
             pkv.pkv_write_decode_attention(out, dbuf["q"], dbuf["k"], dbuf["v"], dbuf["slots"],
                                            inp.k_cache, inp.v_cache, dbuf["tables"], dbuf["lens"],
                                            inp.scale, max_context_len=max_ctx, workspace=ws,
@@ -716,13 +970,20 @@ def main():
     ap.add_argument("--impl", default="lib", choices=["lib", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only-decode", action="store_true",
-                    help="warm-up + timed steps only (no bulk fill, e2e or CPU baseline): for profiling")
+                    help="warm-up + timed steps only (no bulk fill, e2e, CPU baseline or other "
+                         "workloads): for profiling")
     ap.add_argument("--workload", default=WORKLOAD,
                     choices=sorted(wl.CONFIGS) + sorted(wl.PREFILL_CONFIGS),
                     help="the batch the steps run on (default: the Llama-3-8B-shaped decode)")
+    ap.add_argument("--configs", default="all", choices=["all", "none"],
+                    help="all (default): also time every other workload at the same steps and "
+                         "warm-up, one entry each under `configs`")
     ap.add_argument("--mode", default="fused", choices=["fused", "two-launch"],
                     help="fused: one pkv_write_decode_attention launch per step; two-launch: "
                          "pkv_write then pkv_decode_attention")
+    ap.add_argument("--kernel", default="auto", choices=sorted(KERNEL_CHOICES),
+                    help="with --mode two-launch: the decode kernel to run instead of the plan's "
+                         "(pkv_decode_attention_with_kernel), to compare kernels on one batch")
     ap.add_argument("--graph", dest="graph", action="store_true", default=True,
                     help="replay the timed steps from one CUDA graph (the default)")
     ap.add_argument("--no-graph", dest="graph", action="store_false",
@@ -736,6 +997,10 @@ def main():
         ap.error("--warmup must be >= 3")
     if args.layout == "xpacked" and not args.only_decode:
         ap.error("--layout xpacked goes with --only-decode")
+    if args.layout == "xpacked":
+        args.mode = "two-launch"
+    if args.kernel != "auto" and args.mode != "two-launch":
+        ap.error("--kernel goes with --mode two-launch")
     world, rank, local = dist_setup()
     try:
         if args.impl == "reference":

@@ -85,7 +85,9 @@ typedef enum pkv_dtype {
                                             hint sized the grid too small); output of that
                                             sequence unspecified */
 #define PKV_FLAG_TIMEOUT 0x20            /* a bounded wait for an asynchronous copy ran out
-                                            (should never happen); outputs unspecified */
+                                            (should never happen); outputs unspecified, and a
+                                            decode workspace used by that call must be
+                                            zero-filled again before its next use */
 #define PKV_FLAG_QUERY_LEN 0x80          /* prefill: a sequence with qlen < 0, qlen > context_lens[b]
                                             or a context longer than the table; skipped, its
                                             output rows unspecified */
@@ -133,9 +135,12 @@ PKV_API pkv_status pkv_write(void *k_cache, void *v_cache, const void *k, const 
  *
  * The workspace holds per-partition partial results and one counter per
  * (sequence, head group).  Before its FIRST use it must be zero-filled
- * (e.g. cudaMemset); every call leaves the counters at zero again, so the
- * same workspace can be reused by later calls on the same stream without
- * clearing.  Calls that run concurrently need separate workspaces.
+ * (e.g. cudaMemset); every call that completes without PKV_FLAG_TIMEOUT
+ * leaves the counters at zero again, so the same workspace can be reused by
+ * later calls on the same stream without clearing.  A call that raised
+ * PKV_FLAG_TIMEOUT may have left a partition uncounted: zero-fill the
+ * workspace again before reusing it.  Calls that run concurrently need
+ * separate workspaces.
  */
 PKV_API size_t pkv_decode_workspace_size(int B, int H, int num_kv_heads, int head_dim,
                                          int block_size, int max_blocks, int max_context_len,
@@ -161,9 +166,10 @@ PKV_API size_t pkv_decode_workspace_size(int B, int H, int num_kv_heads, int hea
  *   max_context_len  host-side upper bound on context_lens (sizes the grid;
  *                 0 = max_blocks * block_size).  A longer context sets
  *                 PKV_FLAG_CONTEXT_OVER_HINT.
- *   partition_size   tokens per partition of the split-KV path, a positive
- *                 multiple of 16 (or of block_size when that is not a multiple
- *                 of 16); 0 = choose from the sizes and the SM count.  A
+ *   partition_size   tokens per partition of the split-KV path: 0 = choose
+ *                 from the sizes and the SM count, else a positive multiple
+ *                 of 16 (any other value is PKV_ERR_INVALID_ARG), whatever
+ *                 the block size (a partition may end inside a block).  A
  *                 context longer than one partition is processed by several
  *                 CTAs whose (max, sum, weighted-V) partials are merged in the
  *                 workspace with a log-sum-exp rescale.
@@ -214,10 +220,13 @@ PKV_API pkv_status pkv_decode_attention(void *out, const void *q, const void *k_
  *   - Sizes whose split-KV scratch would exceed PKV_STATIC_SCRATCH_BYTES are
  *     rejected with PKV_ERR_WORKSPACE before anything is enqueued (pass a
  *     larger partition_size, or use pkv_decode_attention with a workspace).
+ *   - Every argument check of pkv_decode_attention, and the size check, is
+ *     made before anything is enqueued: a rejected call enqueues nothing.
  *   - No cudaMalloc, cudaFree or other allocating call is made.  The first
  *     call on each device looks up the array's device address
- *     (cudaGetSymbolAddress) with that device current; make that first call
- *     before any stream capture.
+ *     (cudaGetSymbolAddress) with that device current, and keeps it for that
+ *     device's context (after cudaDeviceReset it is looked up again); make
+ *     that first call before any stream capture.
  *   - Each call clears the array's merge counters on `stream` before the
  *     kernel runs.  All calls share the one array: calls whose work overlaps
  *     on the GPU (different streams, or concurrent host threads) race and
@@ -232,6 +241,26 @@ PKV_API pkv_status pkv_decode_attention_static(void *out, const void *q, const v
                                                pkv_dtype dt, int max_context_len,
                                                int partition_size, int *err_flags,
                                                pkv_stream_t stream);
+
+/*
+ * pkv_decode_attention_with_kernel -- pkv_decode_attention with the kernel
+ * named by the caller instead of chosen by the plan, for tests and tuning
+ * (the pages have no counterpart: it exists to measure one kernel against
+ * another on the same batch).  kernel: -1 = the plan's choice (exactly
+ * pkv_decode_attention), 0 = the CUDA-core kernel (any supported shape),
+ * 1 = the TMA + mma.sync tensor-core kernel, 2 = the wide-group tcgen05
+ * kernel.  A kernel that cannot run the given shape returns
+ * PKV_ERR_UNSUPPORTED before anything is enqueued; any other kernel value is
+ * PKV_ERR_INVALID_ARG.  Arguments, workspace (sized by
+ * pkv_decode_workspace_size, which covers every kernel), results and errors
+ * otherwise as in pkv_decode_attention.
+ */
+PKV_API pkv_status pkv_decode_attention_with_kernel(
+    void *out, const void *q, const void *k_cache, const void *v_cache,
+    const int32_t *block_tables, const int32_t *context_lens, int B, int H, int num_kv_heads,
+    int head_dim, int block_size, int max_blocks, int64_t num_blocks, float scale, pkv_dtype dt,
+    int max_context_len, int partition_size, void *workspace, size_t workspace_bytes,
+    int *err_flags, int kernel, pkv_stream_t stream);
 
 /*
  * pkv_write_decode_attention -- one decode step in one launch: pkv_write of
@@ -360,6 +389,17 @@ PKV_API pkv_status pkv_decode_attention_xpacked(
 PKV_API int pkv_decode_plan(int B, int H, int num_kv_heads, int head_dim, int block_size,
                             int max_blocks, int max_context_len, int partition_size,
                             pkv_dtype dt, int num_sms, int *max_partitions, int *kernel);
+
+/*
+ * pkv_hbm_copy -- a plain streaming copy of `bytes` bytes from src to dst
+ * (device pointers, 16-byte aligned, bytes a multiple of 16, the ranges
+ * not overlapping), enqueued on `stream`.  It is the yardstick the other
+ * kernels are measured against: the HBM bandwidth a copy reaches on this
+ * GPU (2 * bytes of traffic per call), taken in the same run.  The pages
+ * have no counterpart.  Errors: PKV_ERR_INVALID_ARG (alignment, size,
+ * overlap, NULL), PKV_ERR_CUDA.  bytes == 0 enqueues nothing.
+ */
+PKV_API pkv_status pkv_hbm_copy(void *dst, const void *src, size_t bytes, pkv_stream_t stream);
 
 /* A static, human-readable name for a status code. */
 PKV_API const char *pkv_status_string(pkv_status status);

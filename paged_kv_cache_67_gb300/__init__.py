@@ -25,10 +25,16 @@ from ._binding import (  # noqa: F401
     exported_symbols,
     library_path,
     load_library,
+    KERNEL_AUTO,
+    KERNEL_CUDA_CORE,
+    KERNEL_TC,
+    KERNEL_WIDE,
     pkv_decode_attention,
+    pkv_decode_attention_with_kernel,
     pkv_decode_attention_xpacked,
     pkv_decode_plan,
     pkv_decode_workspace_size,
+    pkv_hbm_copy,
     pkv_prefill_attention,
     pkv_status_string,
     pkv_version,

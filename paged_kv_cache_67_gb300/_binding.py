@@ -70,6 +70,11 @@ def load_library():
                                              c_int, c_int, i64, ctypes.c_float, c_int, c_int,
                                              c_int, vp, c_size, vp, vp]
         lib.pkv_decode_attention.restype = c_int
+        lib.pkv_decode_attention_with_kernel.argtypes = [vp, vp, vp, vp, vp, vp, c_int, c_int, c_int,
+                                                         c_int, c_int, c_int, i64, ctypes.c_float,
+                                                         c_int, c_int, c_int, vp, c_size, vp, c_int,
+                                                         vp]
+        lib.pkv_decode_attention_with_kernel.restype = c_int
         lib.pkv_write_decode_attention.argtypes = [vp, vp, vp, vp, i64, i64, vp, vp, vp, vp, vp,
                                                    c_int, c_int, c_int, c_int, c_int, c_int, i64,
                                                    ctypes.c_float, c_int, c_int, c_int, vp, c_size,
@@ -103,6 +108,8 @@ def load_library():
         lib.pkv_bm_stats.restype = None
         lib.pkv_bm_block_refcount.argtypes = [vp, i64]
         lib.pkv_bm_block_refcount.restype = c_int
+        lib.pkv_hbm_copy.argtypes = [vp, vp, c_size, vp]
+        lib.pkv_hbm_copy.restype = c_int
         lib.pkv_status_string.argtypes = [c_int]
         lib.pkv_status_string.restype = ctypes.c_char_p
         lib.pkv_version.argtypes = []
@@ -294,25 +301,10 @@ def pkv_decode_attention(out, q, k_cache, v_cache, block_tables, context_lens, s
                          err_flags=None, stream=None):
     """Paged decode attention into ``out`` [B, H, D] (returned)."""
     lib = load_library()
-    _require(q.dim() == 3 and out.shape == q.shape, "q and out must be [B, H, D]")
+    dev = _decode_checks(out, q, k_cache, v_cache, block_tables, context_lens)
     B, H, D = q.shape
-    _require(k_cache.dim() == 4 and v_cache.shape == k_cache.shape and k_cache.shape[3] == D,
-             "caches must be [nb, bs, KVH, D]")
     nb, bs, kvh, _ = k_cache.shape
-    for t in (out, q, k_cache, v_cache, block_tables, context_lens):
-        _require(t.is_contiguous(), "tensors must be contiguous")
-    _require(q.dtype == out.dtype == k_cache.dtype == v_cache.dtype and q.dtype in _DT, "dtype mismatch")
-    _require(block_tables.dtype == torch.int32 and block_tables.dim() == 2 and block_tables.shape[0] == B,
-             "block_tables must be int32 [B, max_blocks]")
-    _require(context_lens.dtype == torch.int32 and context_lens.shape == (B,), "context_lens must be int32 [B]")
-    dev = q.device
-    _require(dev.type == "cuda" and all(t.device == dev for t in (out, k_cache, v_cache, block_tables,
-                                                                   context_lens)),
-             "all tensors must be on the same CUDA device")
-    ws_ptr, ws_bytes = None, 0
-    if workspace is not None:
-        buf = workspace.buffer if isinstance(workspace, DecodeWorkspace) else workspace
-        ws_ptr, ws_bytes = _ptr(buf), buf.numel() * buf.element_size()
+    ws_ptr, ws_bytes = _workspace_arg(workspace)
     _check(lib.pkv_decode_attention(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache),
                                     _ptr(block_tables), _ptr(context_lens), B, H, kvh, D, bs,
                                     block_tables.shape[1], nb, float(scale), _DT[q.dtype],
@@ -320,6 +312,44 @@ def pkv_decode_attention(out, q, k_cache, v_cache, block_tables, context_lens, s
                                     _ptr(err_flags), _stream_handle(stream, dev)),
            "pkv_decode_attention")
     return out
+
+
+KERNEL_AUTO, KERNEL_CUDA_CORE, KERNEL_TC, KERNEL_WIDE = -1, 0, 1, 2
+
+
+def pkv_decode_attention_with_kernel(out, q, k_cache, v_cache, block_tables, context_lens,
+                                     scale: float, kernel: int, max_context_len: int = 0,
+                                     partition_size: int = 0, workspace=None, err_flags=None,
+                                     stream=None):
+    """pkv_decode_attention on the kernel named by ``kernel`` (-1 the plan's
+    choice, 0 CUDA-core, 1 TMA + mma.sync, 2 wide-group tcgen05): for tests
+    and tuning.  A kernel that cannot run the shape raises PkvError
+    (status PKV_ERR_UNSUPPORTED)."""
+    lib = load_library()
+    dev = _decode_checks(out, q, k_cache, v_cache, block_tables, context_lens)
+    B, H, D = q.shape
+    nb, bs, kvh, _ = k_cache.shape
+    ws_ptr, ws_bytes = _workspace_arg(workspace)
+    _check(lib.pkv_decode_attention_with_kernel(
+        _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(context_lens),
+        B, H, kvh, D, bs, block_tables.shape[1], nb, float(scale), _DT[q.dtype],
+        int(max_context_len), int(partition_size), ws_ptr, ws_bytes, _ptr(err_flags), int(kernel),
+        _stream_handle(stream, dev)), "pkv_decode_attention_with_kernel")
+    return out
+
+
+def pkv_hbm_copy(dst, src, stream=None) -> None:
+    """Streaming device-to-device copy of src's bytes into dst (the same
+    byte size, contiguous, 16-byte aligned, not overlapping): the library's
+    yardstick for HBM bandwidth."""
+    lib = load_library()
+    nbytes = src.numel() * src.element_size()
+    _require(dst.numel() * dst.element_size() == nbytes, "dst and src differ in size")
+    _require(src.is_contiguous() and dst.is_contiguous(), "tensors must be contiguous")
+    _require(src.device.type == "cuda" and dst.device == src.device,
+             "both tensors must be on the same CUDA device")
+    _check(lib.pkv_hbm_copy(_ptr(dst), _ptr(src), nbytes, _stream_handle(stream, src.device)),
+           "pkv_hbm_copy")
 
 
 PKV_ERR_OUT_OF_BLOCKS = 5
@@ -410,20 +440,35 @@ class BlockManager:
 
 # ------------------------------------------------------- layout experiment
 
+def _xpacked_cache_checks(k_cache_x, v_cache_x):
+    _require(k_cache_x.dim() == 5 and k_cache_x.shape[3] == 16 and k_cache_x.shape[4] == 8,
+             "k_cache_x must be [nb, KVH, D/8, 16, 8]")
+    nb, kvh, dg, bs, _ = k_cache_x.shape
+    _require(v_cache_x.shape == (nb, kvh, dg * 8, bs), "v_cache_x must be [nb, KVH, D, 16]")
+    _require(k_cache_x.is_contiguous() and v_cache_x.is_contiguous(), "caches must be contiguous")
+    # (fp32 passes: the library answers PKV_ERR_UNSUPPORTED for it)
+    _require(k_cache_x.dtype == v_cache_x.dtype and k_cache_x.dtype in _DT,
+             "packed caches must have one dtype of float32, bfloat16, float16")
+    _require(k_cache_x.device.type == "cuda" and v_cache_x.device == k_cache_x.device,
+             "caches must be on one CUDA device")
+
+
 def pkv_write_xpacked(k_cache_x, v_cache_x, k, v, slot_mapping, err_flags=None, stream=None) -> None:
     """write_kv into the packed layout: k_cache_x [nb, KVH, D/8, 16, 8],
     v_cache_x [nb, KVH, D, 16]; k, v [T, KVH, D]; slot_mapping [T] int64."""
     lib = load_library()
-    _require(k_cache_x.dim() == 5 and k_cache_x.shape[3] == 16 and k_cache_x.shape[4] == 8,
-             "k_cache_x must be [nb, KVH, D/8, 16, 8]")
+    _xpacked_cache_checks(k_cache_x, v_cache_x)
     nb, kvh, dg, bs, _ = k_cache_x.shape
     d = dg * 8
-    _require(v_cache_x.shape == (nb, kvh, d, bs), "v_cache_x must be [nb, KVH, D, 16]")
     _require(k.dim() == 3 and v.shape == k.shape and k.shape[1:] == (kvh, d), "k, v must be [T, KVH, D]")
     _require(k.stride(2) == 1 and k.stride(1) == d and v.stride(2) == 1 and v.stride(1) == d,
              "each token's [KVH, D] row must be contiguous")
-    _require(slot_mapping.dtype == torch.int64 and slot_mapping.numel() == k.shape[0], "slot_mapping int64 [T]")
-    dev = k.device
+    _require(k.dtype == v.dtype == k_cache_x.dtype and k.dtype in _DT, "dtype mismatch")
+    _require(slot_mapping.dtype == torch.int64 and slot_mapping.is_contiguous()
+             and slot_mapping.numel() == k.shape[0], "slot_mapping must be contiguous int64 [T]")
+    dev = k_cache_x.device
+    _require(all(t.device == dev for t in (k, v, slot_mapping)),
+             "all tensors must be on the same CUDA device")
     T = k.shape[0]
     _check(lib.pkv_write_xpacked(_ptr(k_cache_x), _ptr(v_cache_x), _ptr(k), _ptr(v), _ptr(slot_mapping), T,
                                  k.stride(0) if T > 0 else kvh * d, v.stride(0) if T > 0 else kvh * d,
@@ -438,8 +483,19 @@ def pkv_decode_attention_xpacked(out, q, k_cache_x, v_cache_x, block_tables, con
     lib = load_library()
     _require(q.dim() == 3 and out.shape == q.shape, "q and out must be [B, H, D]")
     B, H, D = q.shape
+    _xpacked_cache_checks(k_cache_x, v_cache_x)
     nb, kvh, dg, bs, _ = k_cache_x.shape
-    _require(dg * 8 == D and v_cache_x.shape == (nb, kvh, D, bs), "packed caches do not match q")
+    _require(dg * 8 == D, "packed caches do not match q")
+    for t in (out, q, block_tables, context_lens):
+        _require(t.is_contiguous(), "tensors must be contiguous")
+    _require(q.dtype == out.dtype == k_cache_x.dtype and q.dtype in _DT, "dtype mismatch")
+    _require(block_tables.dtype == torch.int32 and block_tables.dim() == 2 and block_tables.shape[0] == B,
+             "block_tables must be int32 [B, max_blocks]")
+    _require(context_lens.dtype == torch.int32 and context_lens.shape == (B,), "context_lens must be int32 [B]")
+    dev = q.device
+    _require(dev.type == "cuda" and all(t.device == dev for t in (out, k_cache_x, v_cache_x, block_tables,
+                                                                   context_lens)),
+             "all tensors must be on the same CUDA device")
     ws_ptr, ws_bytes = _workspace_arg(workspace)
     _check(lib.pkv_decode_attention_xpacked(_ptr(out), _ptr(q), _ptr(k_cache_x), _ptr(v_cache_x),
                                             _ptr(block_tables), _ptr(context_lens), B, H, kvh, D, bs,

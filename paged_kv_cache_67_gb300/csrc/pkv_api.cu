@@ -51,7 +51,7 @@ static int tc_stages(int D) { return D <= 64 ? 6 : (D <= 128 ? 3 : (D <= 192 ? 2
 
 bool make_plan(int B, int H, int KVH, int D, int bs, int max_blocks, int max_context_len,
                int partition_size, pkv_dtype dt, int num_sms, size_t smem_optin, bool aligned16,
-               DecodePlan *plan, bool allow_wide) {
+               DecodePlan *plan, bool allow_wide, int force_kernel) {
   if (B < 0 || H <= 0 || KVH <= 0 || H % KVH != 0 || D <= 0 || D > 512 || bs <= 0 ||
       max_blocks < 0 || partition_size < 0 || partition_size % 16 != 0 || max_context_len < 0)
     return false;
@@ -59,7 +59,7 @@ bool make_plan(int B, int H, int KVH, int D, int bs, int max_blocks, int max_con
   const int G = H / KVH;
   DecodePlan p;
   memset(&p, 0, sizeof p);
-  p.kernel = (tc_eligible(dt, D, bs) && aligned16) ? 1 : 0;
+  p.kernel = (tc_eligible(dt, D, bs) && aligned16 && force_kernel != 0) ? 1 : 0;
   p.heads_per_cta = p.kernel ? kTcHeads : (D <= 256 ? 4 : 2);
   p.gchunks = (G + p.heads_per_cta - 1) / p.heads_per_cta;
   p.threads = 128;
@@ -106,7 +106,7 @@ bool make_plan(int B, int H, int KVH, int D, int bs, int max_blocks, int max_con
   // partitions within the workspace); with it the kernel sizes its work
   // items from the batch's lengths (about 1.2 CTA shares of tiles, never
   // smaller than the plan's partition).
-  if (allow_wide && p.kernel == 1 && G == 16 && (D == 128 || D == 256) &&
+  if (allow_wide && force_kernel != 1 && p.kernel == 1 && G == 16 && (D == 128 || D == 256) &&
       wide_smem_bytes(D) <= (smem_optin > 0 ? smem_optin : kDefaultSmemOptin)) {
     p.kernel = 2;
     p.heads_per_cta = 16;
@@ -122,6 +122,9 @@ bool make_plan(int B, int H, int KVH, int D, int bs, int max_blocks, int max_con
     p.stages = 0;
     p.smem_bytes = wide_smem_bytes(D);
   }
+  // a kernel named by the caller (tests and tuning) that cannot run these
+  // sizes: no plan
+  if (force_kernel >= 0 && p.kernel != force_kernel) return false;
   *plan = p;
   return true;
 }
@@ -219,23 +222,29 @@ struct AppendIn {
   const int64_t *slots;
 };
 
-// pkv_decode_attention, and with `app` the fused append of one new token per
-// sequence.
-static pkv_status decode_entry(void *out, const void *q, const void *k_cache, const void *v_cache,
-                               const int32_t *block_tables, const int32_t *context_lens, int B,
-                               int H, int num_kv_heads, int head_dim, int block_size,
-                               int max_blocks, int64_t num_blocks, float scale, pkv_dtype dt,
-                               int max_context_len, int partition_size, void *workspace,
-                               size_t workspace_bytes, int *err_flags, pkv_stream_t stream,
-                               const AppendIn *app, bool xpacked = false) {
+// Every host-side check of a decode call that needs no workspace, and the
+// plan.  *empty is set when B == 0 (nothing to enqueue).  Used by the
+// workspace entry points and by pkv_decode_attention_static, so that a call
+// rejected here has enqueued nothing.
+pkv_status decode_check_and_plan(const void *out, const void *q, const void *k_cache,
+                                 const void *v_cache, const int32_t *block_tables,
+                                 const int32_t *context_lens, int B, int H, int num_kv_heads,
+                                 int head_dim, int block_size, int max_blocks, int64_t num_blocks,
+                                 pkv_dtype dt, int max_context_len, int partition_size,
+                                 bool xpacked, int force_kernel, DecodePlan *plan, int *num_sms,
+                                 bool *empty) {
+  *empty = false;
   if (B < 0 || B > 65535 || H <= 0 || H > 65535 || num_kv_heads <= 0 || H % num_kv_heads != 0 ||
       head_dim <= 0 || block_size <= 0 || max_blocks < 0 || num_blocks < 0 ||
       num_blocks > 0x7fffffffLL || max_context_len < 0 || partition_size < 0 ||
-      partition_size % 16 != 0)
+      partition_size % 16 != 0 || force_kernel < -1 || force_kernel > 2)
     return PKV_ERR_INVALID_ARG;
   if (dt != PKV_F32 && dt != PKV_BF16 && dt != PKV_F16) return PKV_ERR_INVALID_ARG;
   if (head_dim > 512) return PKV_ERR_UNSUPPORTED;
-  if (B == 0) return PKV_OK;
+  if (B == 0) {
+    *empty = true;
+    return PKV_OK;
+  }
   if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens)
     return PKV_ERR_INVALID_ARG;
   const uintptr_t el = (uintptr_t)elem_size(dt);
@@ -251,13 +260,41 @@ static pkv_status decode_entry(void *out, const void *q, const void *k_cache, co
   int sms = 0;
   size_t smem_optin = 0;
   if (!device_caps(&sms, &smem_optin)) return PKV_ERR_CUDA;
-  DecodePlan plan;
   if (!make_plan(B, H, num_kv_heads, head_dim, block_size, max_blocks, max_context_len,
-                 partition_size, dt, sms, smem_optin, aligned16, &plan, !xpacked))
+                 partition_size, dt, sms, smem_optin, aligned16, plan, !xpacked, force_kernel)) {
+    // valid sizes that the named kernel does not handle
+    DecodePlan any;
+    if (force_kernel >= 0 && make_plan(B, H, num_kv_heads, head_dim, block_size, max_blocks,
+                                       max_context_len, partition_size, dt, sms, smem_optin,
+                                       aligned16, &any, !xpacked))
+      return PKV_ERR_UNSUPPORTED;
     return PKV_ERR_INVALID_ARG;
-  if ((long long)num_kv_heads * plan.gchunks > 65535) return PKV_ERR_UNSUPPORTED;
-  if (xpacked && (plan.kernel != 1 || block_size != 16 || head_dim == 192))
+  }
+  if ((long long)num_kv_heads * plan->gchunks > 65535) return PKV_ERR_UNSUPPORTED;
+  if (xpacked && (plan->kernel != 1 || block_size != 16 || head_dim == 192))
     return PKV_ERR_UNSUPPORTED;
+  *num_sms = sms;
+  return PKV_OK;
+}
+
+// pkv_decode_attention, and with `app` the fused append of one new token per
+// sequence.
+static pkv_status decode_entry(void *out, const void *q, const void *k_cache, const void *v_cache,
+                               const int32_t *block_tables, const int32_t *context_lens, int B,
+                               int H, int num_kv_heads, int head_dim, int block_size,
+                               int max_blocks, int64_t num_blocks, float scale, pkv_dtype dt,
+                               int max_context_len, int partition_size, void *workspace,
+                               size_t workspace_bytes, int *err_flags, pkv_stream_t stream,
+                               const AppendIn *app, bool xpacked = false, int force_kernel = -1) {
+  DecodePlan plan;
+  int sms = 0;
+  bool empty = false;
+  const pkv_status chk = decode_check_and_plan(
+      out, q, k_cache, v_cache, block_tables, context_lens, B, H, num_kv_heads, head_dim,
+      block_size, max_blocks, num_blocks, dt, max_context_len, partition_size, xpacked,
+      force_kernel, &plan, &sms, &empty);
+  if (chk != PKV_OK || empty) return chk;
+  const uintptr_t el = (uintptr_t)elem_size(dt);
 
   DecodeArgs a;
   memset(&a, 0, sizeof a);
@@ -340,6 +377,18 @@ PKV_API pkv_status pkv_decode_attention(void *out, const void *q, const void *k_
   return decode_entry(out, q, k_cache, v_cache, block_tables, context_lens, B, H, num_kv_heads,
                       head_dim, block_size, max_blocks, num_blocks, scale, dt, max_context_len,
                       partition_size, workspace, workspace_bytes, err_flags, stream, nullptr);
+}
+
+PKV_API pkv_status pkv_decode_attention_with_kernel(
+    void *out, const void *q, const void *k_cache, const void *v_cache,
+    const int32_t *block_tables, const int32_t *context_lens, int B, int H, int num_kv_heads,
+    int head_dim, int block_size, int max_blocks, int64_t num_blocks, float scale, pkv_dtype dt,
+    int max_context_len, int partition_size, void *workspace, size_t workspace_bytes,
+    int *err_flags, int kernel, pkv_stream_t stream) {
+  return decode_entry(out, q, k_cache, v_cache, block_tables, context_lens, B, H, num_kv_heads,
+                      head_dim, block_size, max_blocks, num_blocks, scale, dt, max_context_len,
+                      partition_size, workspace, workspace_bytes, err_flags, stream, nullptr, false,
+                      kernel);
 }
 
 PKV_API pkv_status pkv_write_decode_attention(

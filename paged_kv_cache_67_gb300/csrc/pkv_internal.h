@@ -36,7 +36,17 @@ bool tc_eligible(pkv_dtype dt, int D, int bs);
 // Fills *plan; returns false for sizes no kernel handles.
 bool make_plan(int B, int H, int KVH, int D, int bs, int max_blocks, int max_context_len,
                int partition_size, pkv_dtype dt, int num_sms, size_t smem_optin, bool aligned16,
-               DecodePlan *plan, bool allow_wide = true);
+               DecodePlan *plan, bool allow_wide = true, int force_kernel = -1);
+// Every host-side check of a decode call except the workspace's, then the
+// plan (force_kernel: -1 automatic, else the kernel number of
+// DecodePlan::kernel).  *empty: B == 0, nothing to enqueue.
+pkv_status decode_check_and_plan(const void *out, const void *q, const void *k_cache,
+                                 const void *v_cache, const int32_t *block_tables,
+                                 const int32_t *context_lens, int B, int H, int num_kv_heads,
+                                 int head_dim, int block_size, int max_blocks, int64_t num_blocks,
+                                 pkv_dtype dt, int max_context_len, int partition_size,
+                                 bool xpacked, int force_kernel, DecodePlan *plan, int *num_sms,
+                                 bool *empty);
 size_t workspace_bytes_for(int B, int H, int D, int max_parts);
 // Bytes at the start of the workspace that must be zero before a call (the
 // work queue and the per-(sequence, head group) counters).

@@ -12,7 +12,10 @@
 // The array below lives for as long as the library is loaded, on every GPU
 // the library is used on.  Host code cannot use its name as a device
 // address, so the first call on each device looks the address up with
-// cudaGetSymbolAddress (with that device current) and keeps it.
+// cudaGetSymbolAddress (with that device current) and keeps it, together
+// with the identity of the device's context: after cudaDeviceReset the
+// context is new, the module is loaded again and the address is looked up
+// again.  Devices past the cache's range look it up on every call.
 #include "pkv_device.cuh"
 #include "pkv_internal.h"
 
@@ -23,19 +26,60 @@ constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_pkv_scratch[kStaticScratchBytes];
 
-void *g_scratch_addr[kMaxDevices] = {nullptr};
+struct ScratchEntry {
+  unsigned long long ctx_id;   // the context the address belongs to (0: none yet)
+  void *addr;
+};
+ScratchEntry g_scratch[kMaxDevices] = {};
 
-// Device address of g_pkv_scratch on the current device (looked up once).
+typedef CUresult (*CtxGetCurrentFn)(CUcontext *);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long *);
+
+// Identity of the current context (0 if it cannot be read: then the address
+// is looked up on every call).
+unsigned long long current_context_id() {
+  static CtxGetCurrentFn get_current = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<CtxGetCurrentFn>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<CtxGetIdFn>(p);
+    tried = true;
+  }
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr ||
+      get_id(ctx, &id) != CUDA_SUCCESS)
+    return 0;
+  return id;
+}
+
+// Device address of g_pkv_scratch in the current device's context.
 pkv_status scratch_address(void **addr) {
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return PKV_ERR_CUDA;
-  if (!g_scratch_addr[dev]) {
-    void *p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_pkv_scratch) != cudaSuccess || p == nullptr)
-      return PKV_ERR_CUDA;
-    g_scratch_addr[dev] = p;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return PKV_ERR_CUDA;
+  // the runtime makes the device's context current (and loads the module)
+  // when the symbol is looked up; the context's identity is read after that
+  void *p = nullptr;
+  const unsigned long long id = dev < kMaxDevices ? current_context_id() : 0;
+  if (dev < kMaxDevices && id != 0 && g_scratch[dev].ctx_id == id) {
+    *addr = g_scratch[dev].addr;
+    return PKV_OK;
   }
-  *addr = g_scratch_addr[dev];
+  if (cudaGetSymbolAddress(&p, g_pkv_scratch) != cudaSuccess || p == nullptr) return PKV_ERR_CUDA;
+  if (dev < kMaxDevices) {
+    const unsigned long long now = current_context_id();
+    g_scratch[dev].ctx_id = now;
+    g_scratch[dev].addr = p;
+  }
+  *addr = p;
   return PKV_OK;
 }
 
@@ -46,29 +90,23 @@ extern "C" PKV_API pkv_status pkv_decode_attention_static(
     const int32_t *block_tables, const int32_t *context_lens, int B, int H, int num_kv_heads,
     int head_dim, int block_size, int max_blocks, int64_t num_blocks, float scale, pkv_dtype dt,
     int max_context_len, int partition_size, int *err_flags, pkv_stream_t stream) {
-  if (B < 0 || H <= 0 || num_kv_heads <= 0 || H % num_kv_heads != 0 || head_dim <= 0 ||
-      block_size <= 0 || max_blocks < 0 || max_context_len < 0 || partition_size < 0 ||
-      partition_size % 16 != 0)
-    return PKV_ERR_INVALID_ARG;
-  if (B == 0) return PKV_OK;
-  void *scratch = nullptr;
-  pkv_status st = scratch_address(&scratch);
-  if (st != PKV_OK) return st;
-  int dev = 0, sms = 0, optin = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
-    return PKV_ERR_CUDA;
-  // The same plan pkv_decode_attention will make: how much scratch it needs.
-  const void *ptrs[4] = {out, q, k_cache, v_cache};
-  bool aligned16 = true;
-  for (const void *p : ptrs) aligned16 = aligned16 && (reinterpret_cast<uintptr_t>(p) % 16 == 0);
+  // Every argument check of pkv_decode_attention first, so that a rejected
+  // call enqueues nothing (in particular no clearing of the shared array,
+  // which another call may still be using on another stream).
   pkv::DecodePlan plan;
-  if (!pkv::make_plan(B, H, num_kv_heads, head_dim, block_size, max_blocks, max_context_len,
-                      partition_size, dt, sms, (size_t)optin, aligned16, &plan))
-    return PKV_ERR_INVALID_ARG;
+  int sms = 0;
+  bool empty = false;
+  pkv_status st = pkv::decode_check_and_plan(out, q, k_cache, v_cache, block_tables, context_lens,
+                                             B, H, num_kv_heads, head_dim, block_size, max_blocks,
+                                             num_blocks, dt, max_context_len, partition_size,
+                                             false, -1, &plan, &sms, &empty);
+  if (st != PKV_OK || empty) return st;
+  // The scratch this plan needs (the same plan pkv_decode_attention makes).
   const size_t need = pkv::workspace_bytes_for(B, H, head_dim, plan.max_parts);
   if (need > kStaticScratchBytes) return PKV_ERR_WORKSPACE;  // beyond the fixed maximum
+  void *scratch = nullptr;
+  st = scratch_address(&scratch);
+  if (st != PKV_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   // The merge counters must start at zero; the array keeps whatever the
   // previous call left, so clear them on this call's stream.

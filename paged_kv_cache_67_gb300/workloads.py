@@ -128,6 +128,12 @@ def _lengths(cfg: DecodeConfig, g: torch.Generator) -> torch.Tensor:
     return torch.cat([n, torch.zeros(cfg.pad_seqs, dtype=torch.int64)])
 
 
+def draw_lengths(cfg: DecodeConfig, seed: int) -> torch.Tensor:
+    """The context lengths make_decode_inputs(cfg, seed) draws (its first
+    draw), without the rest of the batch: to size a run before making it."""
+    return _lengths(cfg, torch.Generator().manual_seed(seed)).to(torch.int32)
+
+
 def _garbage_tail(cfg: DecodeConfig, shape, num_blocks: int, g: torch.Generator) -> torch.Tensor:
     if cfg.tail == "99999":
         return torch.full(shape, 99999, dtype=torch.int32)
@@ -153,7 +159,7 @@ def make_decode_inputs(cfg: DecodeConfig, seed: int, device="cpu",
     every cache row no sequence uses (unassigned blocks and the tail of each
     last block) with NaN, so that any read of them shows in the output."""
     g = torch.Generator().manual_seed(seed)
-    lens = _lengths(cfg, g)
+    lens = _lengths(cfg, g)   # the first draw (draw_lengths gives the same)
     # room to grow for per-step runs: step s appends the token at position n + s
     total_len = lens + (cfg.steps if cfg.steps > 1 else 0)
     total_len[cfg.B - cfg.pad_seqs:] = 0

@@ -54,3 +54,31 @@ def gpu_decode(q, k_cache, v_cache, tables, lens, scale, partition_size=0, max_c
 def oracle_decode(q, k_cache, v_cache, tables, lens, scale, seqs=None):
     c = lambda t: t.detach().cpu().contiguous()
     return oracle.decode(c(q), c(k_cache), c(v_cache), c(tables), c(lens), scale, seqs=seqs)
+
+
+def oracle_decode_parallel(q, k_cache, v_cache, tables, lens, scale, seqs=None, threads=None):
+    """The oracle's decode of the given sequences (all by default), one task
+    per (sequence, KV head's query heads) on a thread pool (the oracle is C
+    called through ctypes, which releases the GIL).  Rows of other sequences
+    are zero."""
+    import os
+    from concurrent.futures import ThreadPoolExecutor
+
+    c = lambda t: t.detach().cpu().contiguous()
+    q, k_cache, v_cache, tables, lens = map(c, (q, k_cache, v_cache, tables, lens))
+    B, H, _ = q.shape
+    kvh = k_cache.shape[2]
+    G = H // kvh
+    out = torch.zeros_like(q)
+    seqs = range(B) if seqs is None else seqs
+    tasks = [(b, g) for b in seqs for g in range(kvh)]
+    lib = oracle.load()
+
+    def one(task):
+        b, g = task
+        oracle.decode(q, k_cache, v_cache, tables, lens, scale, seqs=(b, b + 1),
+                      heads=(g * G, (g + 1) * G), out=out, lib=lib)
+
+    with ThreadPoolExecutor(max_workers=threads or max(1, min(os.cpu_count() or 1, 32))) as ex:
+        list(ex.map(one, tasks))
+    return out

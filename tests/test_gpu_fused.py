@@ -223,34 +223,6 @@ def test_argument_errors():
     assert call(ks=132) == 1               # stride not a multiple of 16 bytes
 
 
-def test_full_size_llama8b_step_sampled():
-    """The 8B-shaped batch at full size in the bench's configuration (new
-    token = last position of each context, automatic partitions): caches
-    bit-exact at every written row and unchanged elsewhere; outputs of a
-    sample of sequences against the oracle; all outputs bit-identical to
-    the two-launch sequence."""
-    cfg = wl.CONFIGS["llama8b_bf16"]
-    inp = wl.make_decode_inputs(cfg, seed=1234, device=DEV)
-    positions = [int(n) - 1 for n in inp.context_lens]
-    wb = wl.make_write_batch(inp, positions, seed=4321, device=DEV)
-    tables, lens = inp.block_tables.to(DEV), inp.context_lens.to(DEV)
-    kc2, vc2 = inp.k_cache.clone(), inp.v_cache.clone()
-    pkv.pkv_write(kc2, vc2, wb.k, wb.v, wb.slot_mapping)
-    out2, err2 = gpu_decode(inp.q, kc2, vc2, tables, lens, inp.scale, max_context_len=cfg.len_hi)
-    assert err2 == 0
-    out, err = fused(inp.q, wb.k, wb.v, wb.slot_mapping, inp.k_cache, inp.v_cache, tables, lens,
-                     inp.scale, max_context_len=cfg.len_hi)
-    assert err == 0
-    assert torch.equal(bits(out), bits(out2))
-    assert torch.equal(bits(inp.k_cache), bits(kc2)) and torch.equal(bits(inp.v_cache), bits(vc2))
-    c = lambda t: t.cpu()
-    q_c, kc_c, vc_c = c(inp.q), c(inp.k_cache), c(inp.v_cache)
-    for b in (0, 17, 40, 63):
-        want = oracle_decode(q_c, kc_c, vc_c, inp.block_tables, inp.context_lens, inp.scale,
-                             seqs=(b, b + 1))
-        assert_close(out[b], want[b], cfg.dtype, f"sequence {b}")
-
-
 @pytest.mark.parametrize("name", ["step", "mqa"])
 def test_step_loop_fused_in_cuda_graph(name):
     """The per-step loop with the fused launch: every step's launch captured

@@ -119,28 +119,3 @@ def test_relaunch_and_graph_replay():
         torch.cuda.synchronize()
         assert int(err.item()) == 0
         assert_close(out, want, torch.bfloat16, "graph replay")
-
-
-def test_full_size_mqa_sampled():
-    """The MQA workload at its full size, in the bench's launch configuration,
-    checked on sampled sequences (the longest and shortest included)."""
-    cfg = wl.CONFIGS["mqa_bf16"]
-    inp = wl.make_decode_inputs(cfg, seed=1234, device=DEV)
-    max_ctx = cfg.len_hi + cfg.steps
-    assert pkv.pkv_decode_plan(cfg.B, cfg.H, cfg.KVH, cfg.D, cfg.bs, cfg.table_width, max_ctx)[2] == 2
-    ws = pkv.DecodeWorkspace(cfg.B, cfg.H, cfg.KVH, cfg.D, cfg.bs, cfg.table_width, max_ctx, 0,
-                             device=DEV)
-    out = torch.empty_like(inp.q)
-    err = torch.zeros(1, dtype=torch.int32, device=DEV)
-    tables, lens = inp.block_tables.to(DEV), inp.context_lens.to(DEV)
-    pkv.pkv_decode_attention(out, inp.q, inp.k_cache, inp.v_cache, tables, lens, inp.scale,
-                             max_context_len=max_ctx, workspace=ws, err_flags=err)
-    torch.cuda.synchronize()
-    assert int(err.item()) == 0
-    L = inp.context_lens
-    picks = sorted({int(L.argmax()), int(L.argmin()), 0, 1, cfg.B // 2, cfg.B - 1})
-    q_c, kc, vc = inp.q.cpu(), inp.k_cache.cpu(), inp.v_cache.cpu()
-    for b in picks:
-        want = oracle_decode(q_c, kc, vc, inp.block_tables, inp.context_lens, inp.scale,
-                             seqs=(b, b + 1))
-        assert_close(out[b:b + 1], want[b:b + 1], cfg.dtype, f"sequence {b} (n={int(L[b])})")
