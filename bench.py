@@ -83,23 +83,32 @@ def config_block(workload=WORKLOAD, mode="fused", dec_bytes=None, wr_bytes=None,
     return c
 
 
+TRAFFIC_RECORDS = os.path.join("profiles", "decode_traffic.txt")
+
+
 def decode_traffic(kernel, workload):
     """DRAM bytes per launch of `kernel` on `workload` from the committed ncu
-    capture, or None when there is none for them or the kernel's sources
-    have changed since it was taken."""
-    path = os.path.join(ROOT, "profiles", "decode_traffic.txt")
+    captures (one record per kernel and workload, `kernel | workload |
+    sources_sha256 | bytes_per_launch`), or None when there is none for them
+    or the kernel's sources have changed since it was taken."""
+    path = os.path.join(ROOT, TRAFFIC_RECORDS)
     try:
-        rec = {}
-        for line in open(path):
-            if line.strip() and not line.startswith("#"):
-                key, val = line.split(None, 1)
-                rec[key] = val.strip()
-        if (sources_sha256() != rec["sources_sha256"] or rec["kernel"] != kernel
-                or rec["workload"] != workload):
-            return None
-        return int(rec["bytes_per_launch"])
-    except Exception:
+        lines = open(path).read().splitlines()
+    except OSError:
         return None
+    for line in lines:
+        if not line.strip() or line.lstrip().startswith("#"):
+            continue
+        parts = [x.strip() for x in line.split("|")]
+        if len(parts) != 4 or parts[0] != kernel or parts[1] != workload:
+            continue
+        try:
+            if parts[2] != sources_sha256(kernel):
+                return None
+            return int(parts[3])
+        except (ValueError, OSError):
+            return None
+    return None
 
 
 def code_only(text):
@@ -112,15 +121,24 @@ def code_only(text):
     return " ".join(text.split())
 
 
-def sources_sha256():
-    """Digest of what the decode kernels' launches are built from: the
-    tensor-core kernel's file, the shared device header and the plan
-    (partition choice) in the API file, comments left out."""
+KERNEL_SOURCES = {
+    "pkv_decode_tc_kernel": ("pkv_decode_tc.cu", "pkv_device.cuh"),
+    "pkv_decode_wide_kernel": ("pkv_decode_wide.cu", "pkv_device.cuh", "pkv_tcgen05.cuh"),
+    "pkv_decode_simt_kernel": ("pkv_decode_simt.cu", "pkv_device.cuh"),
+    "pkv_decode_xpacked_kernel": ("pkv_decode_xpacked.cu", "pkv_device.cuh"),
+}
+
+
+def sources_sha256(kernel="pkv_decode_tc_kernel"):
+    """Digest of what a decode kernel's launches are built from: its own
+    file, the shared device headers it uses and the plan (partition
+    choice) in the API file, comments left out."""
     import hashlib
     import re
     csrc = os.path.join(ROOT, "paged_kv_cache_67_gb300", "csrc")
+    family = kernel.split("<")[0]
     h = hashlib.sha256()
-    for f in ("pkv_decode_tc.cu", "pkv_device.cuh"):
+    for f in KERNEL_SOURCES[family]:
         with open(os.path.join(csrc, f), encoding="utf-8") as fh:
             h.update(code_only(fh.read()).encode())
     with open(os.path.join(csrc, "pkv_api.cu"), encoding="utf-8") as fh:
@@ -463,11 +481,8 @@ class DecodeRun:
                                       self.max_ctx, 0, device=dev)
         self.kname = (kernel_name(cfg, mode, kernel) if layout == "token-major" else
                       f"pkv_decode_xpacked_kernel<{cfg.D}, bf16>")
-        wide = layout == "token-major" and self.kname.startswith("pkv_decode_wide")
-        # launches per step: the fused entry is one, except on the wide-group
-        # kernel (pkv_write, then the decode as its programmatic dependent)
-        self.launches_per_step = 1 if self.fused and not wide else 2
-        self.wide_fused = self.fused and wide
+        # launches per step: the fused entry is one
+        self.launches_per_step = 1 if self.fused else 2
 
     def entry(self, i):
         c, s = self.order[i % len(self.order)]
@@ -607,15 +622,17 @@ def config_entry(run, args, stream, world, sampler, peak, flush):
         del buf
     kb = statistics.mean(run.kernel_bytes(i) for i in range(args.steps))
     achieved = kb / (kern_ms * 1e-3) / 1e9
+    traffic = decode_traffic(run.kname, run.name)
+    if traffic is not None and len(run.sets) > 1:
+        # the record is of the first input set: scaled to the cycle's mean bytes
+        traffic = round(traffic * kb / run.kernel_bytes(0))
     return {
         "workload": f"{run.name}: {WORKLOAD_TEXT[run.name]}",
-        "step": ("pkv_write_decode_attention" if run.fused else "pkv_write + pkv_decode_attention")
-                + (" (on this kernel: pkv_write, then the decode as its programmatic dependent; "
-                   "both in the timed span)" if run.wide_fused else ""),
+        "step": "pkv_write_decode_attention" if run.fused else "pkv_write + pkv_decode_attention",
         "kernel": run.kname, "kernel_us": round(kern_ms * 1e3, 2),
         "bytes_per_launch": round(kb), "achieved": round(achieved, 1), "unit": "GB/s",
         "peak": peak, "frac": round(achieved / peak, 4), "bound": "hbm",
-        "traffic": decode_traffic(run.kname, run.name),
+        "traffic": traffic,
         "ms_per_step": round(elapsed * 1e3 / args.steps, 4), "timing": timing,
         "gpu_launches": args.steps * run.launches_per_step, "clocks": clocks,
     }
@@ -643,6 +660,42 @@ def measure_copy(pkv, dev, stream):
         res[name] = round(2 * src.numel() / (ms * 1e-3) / 1e9, 1)
     del src, dst
     return res
+
+
+def measure_gather(pkv, run, stream):
+    """In-run read bandwidth of the batch's own access pattern without the
+    arithmetic: every cache block the first input set's sequences use (K
+    then V), whole, in table order, read by pkv_hbm_gather_read; best of 10."""
+    inp, cfg = run.inp, run.cfg
+    lens = [int(x) for x in inp.context_lens]
+    blocks = [blk for b, n in enumerate(lens) for blk in inp.owned[b][:-(-n // cfg.bs)]]
+    idx = torch.tensor(blocks, dtype=torch.int32, device=run.dev)
+    block_bytes = cfg.bs * cfg.KVH * cfg.D * run.elem
+    sink = torch.zeros(1, dtype=torch.int64, device=run.dev)
+    pkv.pkv_hbm_gather_read(inp.k_cache, idx, block_bytes, block_bytes, sink, stream=stream)
+
+    def both():
+        for cache in (inp.k_cache, inp.v_cache):
+            pkv.pkv_hbm_gather_read(cache, idx, block_bytes, block_bytes, sink, stream=stream,
+                                    check_bounds=False)
+
+    for _ in range(3):
+        both()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(10)]
+    for a, b in evs:
+        a.record(stream)
+        both()
+        b.record(stream)
+    torch.cuda.synchronize()
+    ms = min(a.elapsed_time(b) for a, b in evs)
+    nbytes = 2 * len(blocks) * block_bytes
+    return {"gbs": round(nbytes / (ms * 1e-3) / 1e9, 1), "bytes": nbytes, "blocks": len(blocks),
+            "what": (f"every cache block the {cfg.name} batch uses ({len(blocks)} blocks of "
+                     f"{block_bytes} B, K then V), whole, in table order, by the library's "
+                     f"gather-read kernel (pkv_hbm_gather_read): the batch's access pattern "
+                     f"without the arithmetic; best of 10")}
 
 
 def run_gpu(args, world, rank, local):
@@ -693,6 +746,8 @@ def _run_gpu(args, world, rank, dev, stream, peak, peak_kind, sampler, pkv):
                              "what": "bulk fill: every context token of the workload, random order"}
         del bulk  # the pool now holds the bulk-fill values; the decode reads those
         copy = measure_copy(pkv, dev, stream)
+        if args.layout == "token-major":
+            extra["gather_read_in_run"] = measure_gather(pkv, run, stream)
         extra["hbm_copy_gbs_in_run"] = copy["pkv_hbm_copy"]
         extra["hbm_copy_in_run"] = {"pkv_hbm_copy_gbs": copy["pkv_hbm_copy"],
                                     "torch_copy_gbs": copy["torch_copy"],
@@ -736,10 +791,11 @@ def _run_gpu(args, world, rank, dev, stream, peak, peak_kind, sampler, pkv):
                      "frac": round(achieved / peak, 4),
                      "traffic": decode_traffic(run.kname, args.workload),
                      "kernel": run.kname, "bytes_per_launch": round(kern_bytes),
-                     **({"timed_span": "pkv_write + " + run.kname} if run.wide_fused else {}),
                      "peak_source": ("measured (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
                                      else "fallback 6.8 TB/s"),
-                     "kernel_us": round(dec_ms * 1e3, 2)},
+                     "kernel_us": round(dec_ms * 1e3, 2),
+                     **({"frac_of_gather_read": round(achieved / extra["gather_read_in_run"]["gbs"], 4)}
+                        if "gather_read_in_run" in extra else {})},
         **extra,
         "e2e": e2e,
         "gpu_launches": args.steps * run.launches_per_step,

@@ -285,11 +285,10 @@ PKV_API pkv_status pkv_decode_attention_with_kernel(
  * first part and raises PKV_FLAG_APPEND_MISMATCH when it does not hold.
  * The launch that reads position n-1 takes the new token's K/V from k/v
  * directly, so it does not wait for its own cache write; one CTA per
- * (sequence, KV head) writes the cache row.  (Shapes that run the
- * wide-group kernel -- see pkv_decode_attention -- make this two launches:
- * pkv_write's kernel, then that decode kernel, which checks the slots; the
- * decode is launched as the write's programmatic dependent, so its set-up
- * overlaps the write and only its cache reads wait for it.)  The
+ * (sequence, KV head) writes the cache row.  (On the wide-group kernel --
+ * see pkv_decode_attention -- the row read at position n-1 is replaced in
+ * shared memory by the new token's once the tile has landed; still one
+ * launch.)  The
  * cache ends bit-identical to pkv_write's; the output is bit-identical to
  * pkv_write + pkv_decode_attention with the same partition size.
  * Additional requirements: k, v, k_cache, v_cache 16-byte aligned;
@@ -400,6 +399,24 @@ PKV_API int pkv_decode_plan(int B, int H, int num_kv_heads, int head_dim, int bl
  * overlap, NULL), PKV_ERR_CUDA.  bytes == 0 enqueues nothing.
  */
 PKV_API pkv_status pkv_hbm_copy(void *dst, const void *src, size_t bytes, pkv_stream_t stream);
+
+/*
+ * pkv_hbm_gather_read -- reads nchunks chunks of chunk_bytes bytes, chunk i
+ * starting at base + chunk_index[i] * chunk_stride_bytes (device pointers;
+ * base 16-byte aligned, chunk_bytes and chunk_stride_bytes multiples of 16;
+ * every chunk inside the caller's buffer -- the indices are not checked),
+ * and XORs the 16-byte words read into *sink (a device uint64; the XOR of
+ * the two 64-bit halves of every word, folded in, so no read is dead).  The
+ * yardstick for the decode kernels' access pattern: the bandwidth reads of
+ * randomly placed whole cache blocks reach on this GPU (bytes read =
+ * nchunks * chunk_bytes), taken in the same run.  The pages have no
+ * counterpart.  Errors: PKV_ERR_INVALID_ARG, PKV_ERR_CUDA.  nchunks == 0 or
+ * chunk_bytes == 0 enqueues nothing.
+ */
+PKV_API pkv_status pkv_hbm_gather_read(const void *base, const int32_t *chunk_index,
+                                       int64_t nchunks, int64_t chunk_stride_bytes,
+                                       int64_t chunk_bytes, unsigned long long *sink,
+                                       pkv_stream_t stream);
 
 /* A static, human-readable name for a status code. */
 PKV_API const char *pkv_status_string(pkv_status status);

@@ -35,6 +35,7 @@ from ._binding import (  # noqa: F401
     pkv_decode_plan,
     pkv_decode_workspace_size,
     pkv_hbm_copy,
+    pkv_hbm_gather_read,
     pkv_prefill_attention,
     pkv_status_string,
     pkv_version,

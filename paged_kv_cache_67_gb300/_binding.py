@@ -110,6 +110,8 @@ def load_library():
         lib.pkv_bm_block_refcount.restype = c_int
         lib.pkv_hbm_copy.argtypes = [vp, vp, c_size, vp]
         lib.pkv_hbm_copy.restype = c_int
+        lib.pkv_hbm_gather_read.argtypes = [vp, vp, i64, i64, i64, vp, vp]
+        lib.pkv_hbm_gather_read.restype = c_int
         lib.pkv_status_string.argtypes = [c_int]
         lib.pkv_status_string.restype = ctypes.c_char_p
         lib.pkv_version.argtypes = []
@@ -350,6 +352,30 @@ def pkv_hbm_copy(dst, src, stream=None) -> None:
              "both tensors must be on the same CUDA device")
     _check(lib.pkv_hbm_copy(_ptr(dst), _ptr(src), nbytes, _stream_handle(stream, src.device)),
            "pkv_hbm_copy")
+
+
+def pkv_hbm_gather_read(base, chunk_index, chunk_stride_bytes: int, chunk_bytes: int, sink,
+                        stream=None, check_bounds: bool = True) -> None:
+    """Read chunk_bytes at base + chunk_index[i] * chunk_stride_bytes for
+    every i, XOR-folding the 16-byte words into sink (a 1-element int64
+    device tensor): the library's yardstick for reads of randomly placed
+    cache blocks.  Every chunk must lie inside ``base``'s storage
+    (``check_bounds`` verifies it, at the cost of a device synchronisation)."""
+    lib = load_library()
+    _require(chunk_index.dtype == torch.int32 and chunk_index.dim() == 1 and chunk_index.is_contiguous(),
+             "chunk_index must be contiguous int32 [n]")
+    _require(sink.dtype == torch.int64 and sink.numel() == 1, "sink must be one int64")
+    dev = base.device
+    _require(dev.type == "cuda" and chunk_index.device == dev and sink.device == dev,
+             "all tensors must be on the same CUDA device")
+    n = chunk_index.numel()
+    if n and check_bounds:
+        span = base.numel() * base.element_size()
+        hi = int(chunk_index.max()) * chunk_stride_bytes + chunk_bytes
+        _require(int(chunk_index.min()) >= 0 and hi <= span, "a chunk lies outside base")
+    _check(lib.pkv_hbm_gather_read(_ptr(base), _ptr(chunk_index), n, int(chunk_stride_bytes),
+                                   int(chunk_bytes), _ptr(sink), _stream_handle(stream, dev)),
+           "pkv_hbm_gather_read")
 
 
 PKV_ERR_OUT_OF_BLOCKS = 5

@@ -294,7 +294,6 @@ static pkv_status decode_entry(void *out, const void *q, const void *k_cache, co
       block_size, max_blocks, num_blocks, dt, max_context_len, partition_size, xpacked,
       force_kernel, &plan, &sms, &empty);
   if (chk != PKV_OK || empty) return chk;
-  const uintptr_t el = (uintptr_t)elem_size(dt);
 
   DecodeArgs a;
   memset(&a, 0, sizeof a);
@@ -346,19 +345,7 @@ static pkv_status decode_entry(void *out, const void *q, const void *k_cache, co
   }
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (xpacked) return launch_decode_xpacked(a, plan, dt, s);
-  if (plan.kernel == 2) {
-    // the fused step on this kernel: the new rows are written first (one
-    // launch), the decode then reads them from the cache and checks each
-    // slot against position n - 1
-    if (app) {
-      const pkv_status st = launch_write(const_cast<void *>(k_cache), const_cast<void *>(v_cache),
-                                         app->k, app->v, app->slots, B,
-                                         app->k_stride, app->v_stride, num_blocks, block_size,
-                                         num_kv_heads, head_dim, (int)el, err_flags, s);
-      if (st != PKV_OK) return st;
-    }
-    return launch_decode_wide(a, dt, sms, partition_size == 0, app != nullptr, s);
-  }
+  if (plan.kernel == 2) return launch_decode_wide(a, dt, sms, partition_size == 0, s);
   return plan.kernel ? launch_decode_tc(a, plan, dt, s) : launch_decode_simt(a, plan, dt, s);
 }
 

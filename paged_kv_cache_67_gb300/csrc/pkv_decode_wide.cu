@@ -30,7 +30,7 @@
 // SM) and CTAs claim items from a counter in device memory: every full
 // partition first (the latest partitions, which only long contexts have,
 // first), then the partial ones by tile count, most first -- long contexts
-// spread over SMs early and the last claims are the smallest.  7 warps:
+// spread over SMs early and the last claims are the smallest.  8 warps:
 //   warp 6     scheduler: claims items (the next once the producer reaches
 //              the current item's last tile), publishes each to the CTA
 //              through a two-slot ring, loads the item's 16 query rows (TMA,
@@ -40,13 +40,17 @@
 //              to 128 tokens of one cache block x 64 columns, 128-byte
 //              swizzle; block-table entries read four tiles ahead) into one
 //              ring of K-or-V slots, in the order K0, K1, V0, K2, V1, ... so
-//              keys run a tile ahead of values; in the fused step it waits
-//              for the write kernel (this launch's programmatic primary)
-//              before its first cache read;
+//              keys run a tile ahead of values;
 //   warp 1     MMA issuer (one thread): S^T of the item's first two tiles,
 //              then per tile, once its P^T is written: O^T += V^T . P^T and
 //              the S^T two tiles ahead into the freed score buffer; frees
 //              the tensor memory at the end;
+//   warp 7     append (fused step, one launch): per item that ends its
+//              context, the new token's K and V rows -- written to the cache
+//              row by head chunk 0's item, and written over row n - 1 of the
+//              last tile's K and V in shared memory once they land, before
+//              the MMA thread may read them (so no read waits for the cache
+//              write: bit-identical to writing first, then reading);
 //   warps 2-5  softmax, thread = token lane: scores from tensor memory,
 //              running max and per-lane weight sums per head, P^T written to
 //              shared memory; after the item's last tile the per-head sums
@@ -69,10 +73,12 @@ namespace pkv {
 
 constexpr int kWdTile = 128;             // tokens per KV tile (M of S^T)
 constexpr int kWdHeads = 16;             // query heads per item (N)
-constexpr int kWdWarps = 7;
+constexpr int kWdWarps = 8;
 constexpr int kWdThreads = 32 * kWdWarps;
 constexpr int kWdSchedWarp = 6;
-constexpr int kWdReaders = 2 + 4;        // producer, MMA thread, one lane per softmax warp
+constexpr int kWdAppendWarp = 7;
+constexpr int kWdReaders = 3 + 4;        // producer, MMA thread, append warp, one lane per softmax warp
+constexpr int kWdPatchOff = 1952;        // misc area: the four append counters
 constexpr int kWdSchedSlots = 1024;      // work counters, one per launch in flight
 constexpr int kWdRingBytes = 192 * 1024; // K-or-V slots
 
@@ -95,13 +101,15 @@ struct WdShape {
   static constexpr int kPOff = kQOff + kQBytes;                 // [2]
   static constexpr int kOOff = kPOff + 2 * kPBytes;             // [16][D] fp32 (finishing)
   static constexpr int kMiscOff = kOOff + kWdHeads * D * 4;
-  static constexpr int kMiscBytes = 2048;   // barriers, item ring, reductions, claim tables
+  static constexpr int kMiscBytes = 2048;   // barriers, item ring, reductions, claim tables,
+                                            // append counters
   static constexpr int kSmem = kMiscOff + kMiscBytes + 1024;    // + alignment slack
   // tensor memory: two S^T buffers (16 columns each), O^T (D / 128 blocks
   // of 16 columns)
   static constexpr uint32_t kTmemCols = 64;
   static_assert(kSlots >= 3 && kSlots <= 6, "the ring has three to six slots");
-  static_assert(1168 + 3 * 65 * 4 <= kMiscBytes, "shared-memory misc area");
+  static_assert(1168 + 3 * 65 * 4 <= kWdPatchOff && kWdPatchOff + 16 <= kMiscBytes,
+                "shared-memory misc area");
   static_assert(kSmem <= 232448, "shared memory per block");
   static_assert(32 + 16 * (D / 128) <= (int)kTmemCols, "tensor memory");
 };
@@ -111,7 +119,10 @@ struct __align__(16) WdItem {
   int kind, b, kvh, hc;    // sequence, KV head, 16-head chunk of its group
   int part, nparts;        // partition and partitions of the sequence
   int t0, t1;              // the partition's tokens
-  int n, ntiles, pad0, pad1;
+  int n, ntiles;
+  int patch_row;           // fused step: row of position n - 1 in the item's last tile
+                           // (the item ends the context), else -1
+  int pad1;
 };
 static_assert(sizeof(WdItem) == 48, "three 16-byte words");
 
@@ -120,10 +131,9 @@ struct WdArgs {
   unsigned *sched;     // this launch's (next, done) counters
   int hchunks;         // 16-head chunks per KV head (G / 16)
   int units;           // B * KVH * hchunks
-  int check_append;    // new_slots given: check each slot against position n - 1
+  int check_append;    // fused step (new_slots given): write each new token, read it at n - 1
   int box_tok;         // tokens per K/V box: 16, 32, 64 or 128, dividing bs and P
   int auto_items;      // the partition size is the plan's own: items may be larger
-  int after_write;     // launched as the programmatic dependent of the step's pkv_write
 };
 
 // Whether the phase with the given parity has completed (never waits).
@@ -137,6 +147,26 @@ __device__ __forceinline__ bool wd_test_wait(uint64_t *bar, uint32_t parity) {
       : "r"(smem_u32(bar)), "r"(parity)
       : "memory");
   return ok != 0;
+}
+
+// Monotonic event counters in shared memory, written by one thread with
+// release and read with acquire (no phase parity: a waiter can never
+// mistake an old event for the one it waits for).
+__device__ __forceinline__ void wd_count_store(int *p, int v) {
+  asm volatile("st.release.cta.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(p)), "r"(v) : "memory");
+}
+__device__ __forceinline__ int wd_count_load(const int *p) {
+  int v;
+  asm volatile("ld.acquire.cta.shared::cta.b32 %0, [%1];" : "=r"(v) : "r"(smem_u32(p)) : "memory");
+  return v;
+}
+// Wait until *p >= v; false after kWaitLimitNs.
+__device__ __forceinline__ bool wd_count_wait(const int *p, int v) {
+  if (wd_count_load(p) >= v) return true;
+  const unsigned long long t0 = global_timer_ns();
+  while (wd_count_load(p) < v)
+    if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+  return true;
 }
 
 // A barrier of the 128 softmax threads on an mbarrier, with the bounded
@@ -214,6 +244,7 @@ __device__ __forceinline__ WdItem wd_make_item(const WdArgs &w, int u, int part,
   const DecodeArgs &a = w.d;
   WdItem it;
   memset(&it, 0, sizeof it);
+  it.patch_row = -1;
   it.b = u / (a.KVH * w.hchunks);
   it.kvh = (u / w.hchunks) % a.KVH;
   it.hc = u % w.hchunks;
@@ -228,6 +259,7 @@ __device__ __forceinline__ WdItem wd_make_item(const WdArgs &w, int u, int part,
   }
   it.kind = 1;
   it.ntiles = (it.t1 - it.t0 + kWdTile - 1) / kWdTile;
+  it.patch_row = (w.check_append && it.t1 == n) ? n - 1 - (it.t0 + (it.ntiles - 1) * kWdTile) : -1;
   return it;
 }
 
@@ -480,6 +512,10 @@ __global__ void __launch_bounds__(kWdThreads, 1)
   float *s_l = s_m + kWdHeads;                                      // [16]
   int *s_scratch = reinterpret_cast<int *>(s_l + kWdHeads);         // [1 + 2 * 16]
   float *s_o = reinterpret_cast<float *>(sm + Sh::kOOff);           // [16][D]
+  // fused step, per item that ends its context (counted in item order):
+  // [0] / [1] the producer has issued the last tile's K / V load, [2] / [3]
+  // the append warp has written the new token's row over its row n - 1
+  int *patch_cnt = reinterpret_cast<int *>(sm + Sh::kMiscOff + kWdPatchOff);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
@@ -502,6 +538,7 @@ __global__ void __launch_bounds__(kWdThreads, 1)
     mbar_init(grp_bar, 128);
     mbar_init(prod_done, 1);
     mbar_init(tmem_done, 128);
+    for (int i = 0; i < 4; ++i) patch_cnt[i] = 0;
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -532,15 +569,30 @@ __global__ void __launch_bounds__(kWdThreads, 1)
     // the checks of the whole batch, once, by CTA 0 after its first item is
     // out: lengths, the host's bound on them, and (fused step) each new
     // token's slot against position n - 1
+    // (fused step) the new rows of contexts the launch does not reach to
+    // their end -- cut by the host's bound or the table -- are written here:
+    // no item holds their position n - 1
     auto batch_checks = [&]() {
       const long long reach = (long long)a.max_parts * a.P;
       int over = 0;
-      for (int bb = lane; bb < a.B; bb += 32) {
-        const int n = checked_len(a, bb, true);
-        over |= (long long)n > reach;
-        if (w.check_append) {
-          const long long slot = __ldg(a.new_slots + bb);
-          if (slot >= 0) append_check(a, bb, 0, slot, n);
+      for (int b0 = 0; b0 < a.B; b0 += 32) {
+        const int bb = b0 + lane;
+        bool cut = false;
+        long long slot = -1;
+        if (bb < a.B) {
+          const int n = checked_len(a, bb, true);
+          over |= (long long)n > reach;
+          if (w.check_append) {
+            slot = __ldg(a.new_slots + bb);
+            cut = slot >= 0 && wd_clamp_len(w, __ldg(a.lens + bb)) != max(__ldg(a.lens + bb), 0);
+          }
+        }
+        for (unsigned m = __ballot_sync(0xffffffffu, cut); m; m &= m - 1) {
+          const int src = __ffs(m) - 1;
+          const int b = b0 + src;
+          const long long sl = __shfl_sync(0xffffffffu, slot, src);
+          const int n = checked_len(a, b, false);
+          for (int kv = 0; kv < a.KVH; ++kv) append_write_row<T>(a, b, kv, sl, n, lane);
         }
       }
       if (__any_sync(0xffffffffu, over) && lane == 0) raise_flag(a.err, PKV_FLAG_CONTEXT_OVER_HINT);
@@ -794,12 +846,8 @@ __global__ void __launch_bounds__(kWdThreads, 1)
       prefetch_tensormap(&tmK);
       prefetch_tensormap(&tmV);
     }
-    int it = 0, loads = 0;
+    int it = 0, loads = 0, npatch = 0;
     bool ok = true;
-    // in the fused step this launch may start while the write kernel still
-    // runs (everything up to here, and the scheduler's claims, read only
-    // lengths, tables and queries): the cache rows are read after it is done
-    if (w.after_write) asm volatile("griddepcontrol.wait;" ::: "memory");
     while (ok) {
       const int slot = it & 1;
       ok = __all_sync(0xffffffffu, mbar_wait_bounded(&item_full[slot], (it >> 1) & 1));
@@ -863,6 +911,13 @@ __global__ void __launch_bounds__(kWdThreads, 1)
                     policy);
         }
         ++loads;
+        // the append warp may wait for the last tile's K (V) to land only
+        // once it is issued: its slot's earlier phases are complete then
+        if (item.patch_row >= 0 && j == nt - 1) {
+          __syncwarp();
+          if (lane == 0) wd_count_store(patch_cnt + v, npatch + 1);
+          if (v) ++npatch;
+        }
         // tile j's entries are done with once its values are on the way:
         // the lanes of its group read those of tile j + 4
         if (v && (lane >> 3) == (j & 3) && j + 4 < nt) ahead = entry_of(j + 4);
@@ -881,7 +936,7 @@ __global__ void __launch_bounds__(kWdThreads, 1)
       const uint32_t idesc_s = umma_idesc_f16(128, kWdHeads, bf16, false);       // K, Q: K-major
       const uint32_t idesc_o = umma_idesc_f16_mn(128, kWdHeads, bf16, true, false);  // V MN-major
       const uint32_t q_base = smem_u32(sm + Sh::kQOff), p_base = smem_u32(sm + Sh::kPOff);
-      int it = 0, loads = 0, st = 0, pt = 0, iq = 0;
+      int it = 0, loads = 0, st = 0, pt = 0, iq = 0, npk = 0, npv = 0;  // patches waited for
       bool ok = true;
       while (ok) {
         const int slot = it & 1;
@@ -900,6 +955,9 @@ __global__ void __launch_bounds__(kWdThreads, 1)
         auto issue_s = [&](int j) -> bool {
           const int l = L0 + wd_kidx(j), s = l % Sh::kSlots;
           if (!mbar_wait_bounded(&slot_full[s], (l / Sh::kSlots) & 1)) return false;
+          // fused step: the last tile's K row n - 1 is the new token's
+          if (j == item.ntiles - 1 && item.patch_row >= 0 && !wd_count_wait(patch_cnt + 2, ++npk))
+            return false;
           tc_fence_after();
           const int buf = st & 1;
           const uint32_t kb = smem_u32(sm + s * Sh::kTileBytes);
@@ -921,6 +979,8 @@ __global__ void __launch_bounds__(kWdThreads, 1)
           if (!ok) break;
           const int l = L0 + wd_vidx(j, item.ntiles), s = l % Sh::kSlots;
           ok = mbar_wait_bounded(&slot_full[s], (l / Sh::kSlots) & 1);
+          if (ok && j == item.ntiles - 1 && item.patch_row >= 0)
+            ok = wd_count_wait(patch_cnt + 3, ++npv);  // the new token's V row
           if (!ok) break;
           tc_fence_after();
           // O^T (+)= V^T . P^T, per block of 128 of the D values
@@ -951,6 +1011,76 @@ __global__ void __launch_bounds__(kWdThreads, 1)
     mbar_wait_bounded(tmem_done, 0);
     tc_fence_after();
     tmem_dealloc(tmem, Sh::kTmemCols);
+  } else if (warp == kWdAppendWarp) {
+    // ------------------------------------------------------------ append
+    // Fused step only (no items carry a patch row otherwise).  Per item that
+    // ends its context: the new token's K and V rows of the item's KV head
+    // are loaded; the item of head chunk 0 writes them to the cache row
+    // (after the slot checks); once the last tile's K (then V) has landed
+    // its row n - 1 is overwritten with the new row in shared memory (so
+    // nothing waits for the cache write, and whatever a load read of that
+    // row is replaced) and the MMA thread is released.  Empty contexts with
+    // a new token are written (and flagged) here too.
+    constexpr int kRowVecs = D / 8;        // 16-byte vectors of one head's row (<= 32)
+    int it = 0, loads = 0, npatch = 0;
+    bool ok = true;
+    while (true) {
+      const int slot = it & 1;
+      ok = __all_sync(0xffffffffu, mbar_wait_bounded(&item_full[slot], (it >> 1) & 1));
+      if (!ok) break;
+      const WdItem item = items[slot];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&item_empty[slot]);
+      ++it;
+      if (item.kind < 0) break;
+      const long long snew = w.check_append ? append_slot(a, item.b) : -1LL;
+      if (item.kind == 2) {  // empty context: no rows read; the token is still written (flagged)
+        if (snew >= 0 && item.hc == 0) append_write_row<T>(a, item.b, item.kvh, snew, 0, lane);
+        continue;
+      }
+      if (item.kind != 1) continue;
+      const int L0 = loads;
+      loads += 2 * item.ntiles;
+      if (item.patch_row < 0) continue;
+      // a context cut short by the host's bound never reaches here with its
+      // true length (the batch checks write its row)
+      const bool has = snew >= 0 && max(__ldg(a.lens + item.b), 0) == item.n;
+      uint4 kv = make_uint4(0, 0, 0, 0), vv = kv;
+      if (has && lane < kRowVecs) {
+        kv = __ldg(append_src<T>(a, false, item.b, item.kvh) + lane);
+        vv = __ldg(append_src<T>(a, true, item.b, item.kvh) + lane);
+      }
+      if (has && item.hc == 0) {
+        int wr = 0;
+        if (lane == 0) wr = append_check(a, item.b, item.kvh, snew, item.n);
+        if (__shfl_sync(0xffffffffu, wr, 0) && lane < kRowVecs)
+          append_store<T>(a, item.kvh, snew, lane, kv, vv);
+      }
+      const int r = item.patch_row;
+      ++npatch;
+      // 16-byte column lane & 7 of the 64-value region lane >> 3, row r,
+      // 128-byte swizzle (the tile's regions are 1024-byte aligned)
+      const uint32_t off = (uint32_t)((lane >> 3) * Sh::kRegionBytes + r * 128 +
+                                      (((lane & 7) ^ (r & 7)) << 4));
+      for (int v = 0; v < 2 && ok; ++v) {
+        const int l = L0 + (v ? wd_vidx(item.ntiles - 1, item.ntiles) : wd_kidx(item.ntiles - 1));
+        if (has) {
+          // issued (so the slot holds no older load), then landed
+          ok = __all_sync(0xffffffffu, wd_count_wait(patch_cnt + v, npatch)) &&
+               __all_sync(0xffffffffu,
+                          mbar_wait_bounded(&slot_full[l % Sh::kSlots], (l / Sh::kSlots) & 1)) &&
+               !aborted();
+          if (!ok) break;
+          if (lane < kRowVecs)
+            st_shared_v4(smem_u32(sm + (l % Sh::kSlots) * Sh::kTileBytes) + off, v ? vv : kv);
+          fence_proxy_async_shared();  // the row before the product reads it
+          __syncwarp();
+        }
+        if (lane == 0) wd_count_store(patch_cnt + 2 + v, npatch);
+      }
+      if (!ok) break;
+    }
+    if (!ok && lane == 0) abort_cta();
   } else {
     // ------------------------------------------------------------ softmax
     const int q4 = warp & 3;                       // tensor-memory lane quarter
@@ -1254,17 +1384,12 @@ static pkv_status launch_wide_t(const WdArgs &w, const CUtensorMap &mq, const CU
   cfg.blockDim = dim3(kWdThreads);
   cfg.dynamicSmemBytes = WdShape<D>::kSmem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = w.after_write ? 1 : 0;
   if (cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, w) != cudaSuccess) return PKV_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
 pkv_status launch_decode_wide(const DecodeArgs &a, pkv_dtype dt, int num_sms, bool auto_items,
-                              bool after_write, cudaStream_t stream) {
+                              cudaStream_t stream) {
   CUtensorMap mq, mk, mv;
   const int box_tok = wd_box_tokens(a.bs, a.P);
   if (!encode_query_group_map(&mq, a.q, dt, a.B, a.H, a.D) ||
@@ -1286,7 +1411,6 @@ pkv_status launch_decode_wide(const DecodeArgs &a, pkv_dtype dt, int num_sms, bo
   w.check_append = a.new_slots != nullptr;
   w.box_tok = box_tok;
   w.auto_items = auto_items;
-  w.after_write = after_write;
   // one persistent CTA per SM, never more than the items there can be
   const long long items = (long long)w.units * a.max_parts;
   const int ctas = (int)std::min<long long>(items, num_sms > 0 ? num_sms : 1);

@@ -105,6 +105,6 @@ pkv_status launch_decode_tc(const DecodeArgs &a, const DecodePlan &plan, pkv_dty
 // persistent tensor-core decode with tokens as the product's M.
 size_t wide_smem_bytes(int D);
 pkv_status launch_decode_wide(const DecodeArgs &a, pkv_dtype dt, int num_sms, bool auto_items,
-                              bool after_write, cudaStream_t stream);
+                              cudaStream_t stream);
 
 }  // namespace pkv

@@ -29,22 +29,34 @@ def test_code_edits_change_the_code():
 
 
 def test_traffic_record_lookup(tmp_path, monkeypatch):
-    # a record is reported for its kernel and workload while the sources hash
-    # to its digest, and for nothing else
+    # a record is reported for its kernel and workload while that kernel's
+    # sources hash to its digest, and for nothing else
     kern = "pkv_decode_tc_kernel<128, bf16, append>"
+    wide = "pkv_decode_wide_kernel<256, bf16>"
     (tmp_path / "profiles").mkdir()
     rec = tmp_path / "profiles" / "decode_traffic.txt"
+    digests = {k: bench.sources_sha256(k) for k in (kern, wide)}   # of the sources in this tree
+    assert digests[kern] != digests[wide]
 
-    def write(sha):
-        rec.write_text("# a capture\nkernel %s\nworkload llama8b_bf16\nsources_sha256 %s\n"
-                       "bytes_per_launch 714866688\n" % (kern, sha))
+    def write(sha_tc, sha_wide):
+        rec.write_text("# captures\n%s | llama8b_bf16 | %s | 714866688\n"
+                       "%s | mqa_bf16 | %s | 161000000\n" % (kern, sha_tc, wide, sha_wide))
 
-    digest = bench.sources_sha256()          # of the sources in this tree
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
-    monkeypatch.setattr(bench, "sources_sha256", lambda: digest)
-    write(digest)
+    monkeypatch.setattr(bench, "sources_sha256", lambda k="": digests[k])
+    write(digests[kern], digests[wide])
     assert bench.decode_traffic(kern, "llama8b_bf16") == 714866688
+    assert bench.decode_traffic(wide, "mqa_bf16") == 161000000
     assert bench.decode_traffic(kern, "long_bf16") is None
-    assert bench.decode_traffic("pkv_decode_wide_kernel<256, bf16>", "llama8b_bf16") is None
-    write("0" * 64)                          # taken on other sources
+    assert bench.decode_traffic(wide, "llama8b_bf16") is None
+    write("0" * 64, digests[wide])           # the tensor-core kernel changed since
     assert bench.decode_traffic(kern, "llama8b_bf16") is None
+    assert bench.decode_traffic(wide, "mqa_bf16") == 161000000
+
+
+def test_kernel_sources_cover_every_decode_kernel():
+    import os
+    for fam, files in bench.KERNEL_SOURCES.items():
+        for f in files:
+            assert os.path.exists(os.path.join(bench.ROOT, "paged_kv_cache_67_gb300", "csrc", f))
+        assert len(bench.sources_sha256(fam + "<x>")) == 64

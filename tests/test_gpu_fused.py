@@ -229,9 +229,10 @@ def test_step_loop_fused_in_cuda_graph(name):
     in one CUDA graph (each step its own slice of device-resident step
     inputs), replayed once; caches and every step's output against the
     oracle's write-then-decode sequence.  "mqa" runs the wide-group kernel,
-    whose decode is the write kernel's programmatic dependent and reads the
-    new rows from the cache: each step must see its own write (contexts up
-    to 2500 tokens, so some are split and merged)."""
+    which writes each new row to the cache and over row n - 1 of its landed
+    tiles in the same launch: each step must see its own token and the next
+    step its cache row (contexts up to 2500 tokens, so some are split and
+    merged)."""
     cfg = (wl.small_variant(wl.CONFIGS["step_bf16"], B=16, len_hi=300, steps=6) if name == "step" else
            wl.small_variant(wl.CONFIGS["mqa_bf16"], B=12, len_hi=2500, steps=5))
     inp = wl.make_decode_inputs(cfg, seed=97)
@@ -277,3 +278,64 @@ def test_step_loop_fused_in_cuda_graph(name):
         assert_close(outs[s], want, cfg.dtype, f"step {s}")
         assert bool((outs[s][B - cfg.pad_seqs:] == 0).all())
     assert torch.equal(kc.cpu(), kc_o) and torch.equal(vc.cpu(), vc_o)
+
+
+@pytest.mark.parametrize("H,KVH,D,bs", [(16, 1, 128, 16), (32, 2, 256, 32), (16, 1, 128, 32)])
+@pytest.mark.parametrize("partition_size", [0, 128, 256])
+def test_wide_group_fused_step_edges(H, KVH, D, bs, partition_size):
+    """The wide-group kernel's one-launch fused step (16 query heads per
+    head chunk; 1 or 2 KV heads; block sizes 16 and 32): the new
+    token at every edge of a 128-token tile and of a partition, against the
+    oracle's write-then-decode and bit-identical to the two launches."""
+    lens = [1, 2, 127, 128, 129, 255, 256, 257, 1000, 1024, 1025]
+    case = random_paged_case(D + H + bs + partition_size, lens, H=H, KVH=KVH, D=D, bs=bs,
+                             dtype=torch.bfloat16)
+    assert pkv.pkv_decode_plan(len(lens), H, KVH, D, bs, case["block_tables"].shape[1],
+                               partition_size=partition_size)[2] == 2
+    g = torch.Generator().manual_seed(D * H + bs)
+    k = torch.randn((len(lens), KVH, D), generator=g).to(torch.bfloat16)
+    v = torch.randn((len(lens), KVH, D), generator=g).to(torch.bfloat16)
+    slots = torch.tensor([wl.slot_of(case["owned"][b], n - 1, bs) for b, n in enumerate(lens)])
+    check_step(case["q"], k, v, slots, case["k_cache"], case["v_cache"], case["block_tables"],
+               case["context_lens"], 1.0 / math.sqrt(D), torch.bfloat16,
+               f"wide H={H} KVH={KVH} D={D} bs={bs} P={partition_size}", partition_size)
+
+
+@pytest.mark.parametrize("H,KVH,D,bs", [(16, 1, 256, 32), (8, 2, 128, 16)])
+def test_fused_step_odd_slots_and_cut_contexts(H, KVH, D, bs):
+    """On the wide-group kernel (16 heads per KV head) and the TMA +
+    mma.sync kernel: an empty context with a kept slot (written, flagged),
+    a slot of -1 (nothing written), a slot that is not position n - 1
+    (written where it says, flagged), and contexts longer than the host's
+    bound (cut, flagged; their new rows still written).  The caches must
+    equal the oracle's write bit for bit; the sequences with a regular
+    append must match the oracle's decode."""
+    lens = [0, 40, 300, 77, 900, 600]
+    case = random_paged_case(H + D + 3, [max(n, 1) for n in lens], H=H, KVH=KVH, D=D, bs=bs,
+                             dtype=torch.bfloat16, poison=False)
+    lens_t = torch.tensor(lens, dtype=torch.int32)
+    g = torch.Generator().manual_seed(H + D)
+    k = torch.randn((len(lens), KVH, D), generator=g).to(torch.bfloat16)
+    v = torch.randn((len(lens), KVH, D), generator=g).to(torch.bfloat16)
+    own = case["owned"]
+    slots = torch.tensor([wl.slot_of(own[0], 0, bs),          # empty context, kept slot
+                          -1,                                  # no new token
+                          wl.slot_of(own[2], 299, bs),        # regular
+                          wl.slot_of(own[3], 10, bs),         # not position n - 1
+                          wl.slot_of(own[4], 899, bs),        # cut by the bound below
+                          wl.slot_of(own[5], 599, bs)])       # regular
+    hint = 640   # sequence 4 (900 tokens) is longer: cut
+    kern = pkv.pkv_decode_plan(len(lens), H, KVH, D, bs, case["block_tables"].shape[1], hint)[2]
+    assert kern == (2 if H // KVH == 16 else 1)
+    kc, vc = case["k_cache"].to(DEV), case["v_cache"].to(DEV)
+    d = lambda t: t.to(DEV)
+    out, err = fused(d(case["q"]), d(k), d(v), d(slots), kc, vc, d(case["block_tables"]),
+                     d(lens_t), 0.11, max_context_len=hint)
+    assert err == pkv.FLAG_APPEND_MISMATCH | pkv.FLAG_CONTEXT_OVER_HINT, hex(err)
+    kc_o, vc_o = case["k_cache"].clone(), case["v_cache"].clone()
+    oracle.write(kc_o, vc_o, k, v, slots)
+    assert torch.equal(bits(kc.cpu()), bits(kc_o)) and torch.equal(bits(vc.cpu()), bits(vc_o))
+    want = oracle_decode(case["q"], kc_o, vc_o, case["block_tables"], lens_t, 0.11)
+    for b in (1, 2, 5):
+        assert_close(out[b], want[b], torch.bfloat16, f"sequence {b}")
+    assert bool((out[0] == 0).all())
