@@ -561,10 +561,12 @@ class DecodeRun:
         barrier(world)
         torch.cuda.synchronize()
         h0 = time.monotonic()
+        torch.cuda.nvtx.range_push("timed")
         t_start.record(stream)
         graph.replay()
         t_end.record(stream)
         torch.cuda.synchronize()
+        torch.cuda.nvtx.range_pop()
         h1 = time.monotonic()
         barrier(world)
         self.check_flags("in the timed region")
@@ -582,6 +584,7 @@ class DecodeRun:
         barrier(world)
         torch.cuda.synchronize()
         h0 = time.monotonic()
+        torch.cuda.nvtx.range_push("timed")
         t_start.record(stream)
         for i in range(steps):
             if flush is not None:
@@ -589,6 +592,7 @@ class DecodeRun:
             self.step(i, stream, evs[i])
         t_end.record(stream)
         torch.cuda.synchronize()
+        torch.cuda.nvtx.range_pop()
         h1 = time.monotonic()
         barrier(world)
         self.check_flags("in the timed region")
