@@ -626,6 +626,7 @@ def config_entry(run, args, stream, world, sampler, peak, flush):
         del buf
     kb = statistics.mean(run.kernel_bytes(i) for i in range(args.steps))
     achieved = kb / (kern_ms * 1e-3) / 1e9
+    gather = None if flush else measure_gather(run.pkv, run, stream)
     traffic = decode_traffic(run.kname, run.name)
     if traffic is not None and len(run.sets) > 1:
         # the record is of the first input set: scaled to the cycle's mean bytes
@@ -639,6 +640,10 @@ def config_entry(run, args, stream, world, sampler, peak, flush):
         "traffic": traffic,
         "ms_per_step": round(elapsed * 1e3 / args.steps, 4), "timing": timing,
         "gpu_launches": args.steps * run.launches_per_step, "clocks": clocks,
+        **({"gather_read_gbs": gather["gbs"],
+            "frac_of_gather_read": round(achieved / gather["gbs"], 4),
+            "gather_what": gather["what"] + ("; the first input set" if len(run.sets) > 1 else "")}
+           if gather else {}),
     }
 
 

@@ -57,7 +57,10 @@
 //              are reduced and the item is finished -- output rows, or the
 //              partition's partials counted by an atomic read at the next
 //              item's end, where the last partition of the sequence merges
-//              (log-sum-exp).
+//              (log-sum-exp).  The CTA's last merge waits for the roles to
+//              end and is run by all eight warps: twice the threads, half
+//              the rounds of partial loads, on the launch's tail (the whole
+//              CTA's: 35.2 -> 34.2 us on the MQA batch, three input sets).
 // Every wait on an mbarrier is bounded; on time-out the CTA raises
 // PKV_FLAG_TIMEOUT, lets its copies and products land (bounded) and exits.
 #include <string.h>
@@ -79,6 +82,7 @@ constexpr int kWdSchedWarp = 6;
 constexpr int kWdAppendWarp = 7;
 constexpr int kWdReaders = 3 + 4;        // producer, MMA thread, append warp, one lane per softmax warp
 constexpr int kWdPatchOff = 1952;        // misc area: the four append counters
+constexpr int kWdFinOff = 1968;          // misc area: the CTA's last merge, run by all threads
 constexpr int kWdSchedSlots = 1024;      // work counters, one per launch in flight
 constexpr int kWdRingBytes = 192 * 1024; // K-or-V slots
 
@@ -108,7 +112,8 @@ struct WdShape {
   // of 16 columns)
   static constexpr uint32_t kTmemCols = 64;
   static_assert(kSlots >= 3 && kSlots <= 6, "the ring has three to six slots");
-  static_assert(1168 + 3 * 65 * 4 <= kWdPatchOff && kWdPatchOff + 16 <= kMiscBytes,
+  static_assert(1168 + 3 * 65 * 4 <= kWdPatchOff && kWdPatchOff + 16 <= kWdFinOff &&
+                    kWdFinOff + 5 * 4 <= kMiscBytes,
                 "shared-memory misc area");
   static_assert(kSmem <= 232448, "shared memory per block");
   static_assert(32 + 16 * (D / 128) <= (int)kTmemCols, "tensor memory");
@@ -328,31 +333,37 @@ __device__ bool wd_publish(const DecodeArgs &a, int b, int head0, int part, int 
 }
 
 // The merge of a (sequence, head chunk) whose partitions have all arrived,
-// by the group whose count was the last:  M = max_p m_p,
+// by NT threads (the softmax group, or the whole CTA for its last item)
+// of the CTA whose count was the last:  M = max_p m_p,
 // L = sum_p l_p 2^(m_p - M),  out = sum_p o_p 2^(m_p - M) / L.  It sits at
-// the end of the work, so it is written for latency: warp w takes rows w,
-// w + 4, w + 8, w + 12 together (their m and l loads in one round trip when
-// nparts <= 32) and puts the weights in s_w (16 x nparts floats when they
-// fit in w_cap); then each thread takes four output vectors of four values at
-// a time with eight partitions' loads of each in flight.  The counter is put
-// back to zero for the next call.
-template <int D, typename T, typename Sync>
+// the end of the work, so it is written for latency: warp w of the NT / 32
+// takes rows w, w + NT / 32, ... together (their m and l loads in one round
+// trip when nparts <= 32) and puts the weights in s_w (16 x nparts floats
+// when they fit in w_cap); then each thread takes up to four output vectors
+// of four values at a time with eight partitions' loads of each in flight.
+// The counter is put back to zero for the next call.
+template <int D, typename T, int NT, typename Sync>
 __device__ void wd_merge(const DecodeArgs &a, int b, int head0, int nparts, float *s_w, int w_cap,
                          int *s_scratch, int *counter, int ts, Sync sync) {
   T *out = reinterpret_cast<T *>(a.out);
   const size_t row0 = (size_t)b * a.H + head0;
+  constexpr int kVecs = kWdHeads * D / 4;   // output vectors of four values
+  constexpr int kU = kVecs / NT < 4 ? kVecs / NT : 4;   // vectors per thread and step
+  static_assert(kU >= 1 && kVecs % (NT * kU) == 0, "whole steps of the threads");
   // the other partitions' partials: thread 0's count was an acquire-release
   // atomic that saw theirs, the group barrier passes that on, and the loads
   // below go to L2
   const int warp = ts >> 5, lane = ts & 31;
-  constexpr int kRows = kWdHeads / 4;
+  constexpr int kWarps = NT / 32;
+  constexpr int kRows = kWdHeads / kWarps;
+  static_assert(kRows * kWarps == kWdHeads, "rows per warp");
   const bool cached = kWdHeads * nparts <= w_cap;
   float *s_M = reinterpret_cast<float *>(s_scratch + 1), *s_invL = s_M + kWdHeads;
   const float *pm[kRows], *pl[kRows];
 #pragma unroll
   for (int j = 0; j < kRows; ++j) {
-    pm[j] = a.ws_m + (row0 + warp + 4 * j) * a.max_parts;
-    pl[j] = a.ws_l + (row0 + warp + 4 * j) * a.max_parts;
+    pm[j] = a.ws_m + (row0 + warp + kWarps * j) * a.max_parts;
+    pl[j] = a.ws_l + (row0 + warp + kWarps * j) * a.max_parts;
   }
   auto warp_max = [](float v) {
 #pragma unroll
@@ -381,7 +392,7 @@ __device__ void wd_merge(const DecodeArgs &a, int b, int head0, int nparts, floa
       M[j] = warp_max(mv[j]);
       const float e = mine ? fast_exp2(mv[j] - M[j]) : 0.f;
       inv_l[j] = 1.f / warp_sum(mine ? lv[j] * e : 0.f);
-      if (cached && mine) s_w[(warp + 4 * j) * nparts + lane] = e * inv_l[j];
+      if (cached && mine) s_w[(warp + kWarps * j) * nparts + lane] = e * inv_l[j];
     }
   } else {
     float L[kRows];
@@ -406,27 +417,24 @@ __device__ void wd_merge(const DecodeArgs &a, int b, int head0, int nparts, floa
       for (int p = lane; p < nparts; p += 32) {
 #pragma unroll
         for (int j = 0; j < kRows; ++j)
-          s_w[(warp + 4 * j) * nparts + p] = fast_exp2(__ldcg(pm[j] + p) - M[j]) * inv_l[j];
+          s_w[(warp + kWarps * j) * nparts + p] = fast_exp2(__ldcg(pm[j] + p) - M[j]) * inv_l[j];
       }
   }
   if (lane == 0) {
 #pragma unroll
     for (int j = 0; j < kRows; ++j) {
-      s_M[warp + 4 * j] = M[j];
-      s_invL[warp + 4 * j] = inv_l[j];
+      s_M[warp + kWarps * j] = M[j];
+      s_invL[warp + kWarps * j] = inv_l[j];
     }
   }
   sync();
-  constexpr int kVecs = kWdHeads * D / 4;   // output vectors of four values
-  constexpr int kU = 4;                     // vectors per thread and step
-  static_assert(kVecs % (128 * kU) == 0, "whole steps of the group");
-  for (int i0 = ts; i0 < kVecs; i0 += 128 * kU) {
+  for (int i0 = ts; i0 < kVecs; i0 += NT * kU) {
     int r[kU], d[kU];
     const float4 *po[kU];
     float4 acc[kU];
 #pragma unroll
     for (int u = 0; u < kU; ++u) {
-      const int i = i0 + 128 * u;
+      const int i = i0 + NT * u;
       r[u] = 4 * i / D;
       d[u] = 4 * i - r[u] * D;
       po[u] = reinterpret_cast<const float4 *>(a.ws_o + (row0 + r[u]) * a.max_parts * D + d[u]);
@@ -516,6 +524,9 @@ __global__ void __launch_bounds__(kWdThreads, 1)
   // [0] / [1] the producer has issued the last tile's K / V load, [2] / [3]
   // the append warp has written the new token's row over its row n - 1
   int *patch_cnt = reinterpret_cast<int *>(sm + Sh::kMiscOff + kWdPatchOff);
+  // the CTA's last item, if it was the last partition of its context: merge
+  // it (1 / 0), sequence, first head, partitions, counter index
+  int *fin = reinterpret_cast<int *>(sm + Sh::kMiscOff + kWdFinOff);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
@@ -539,6 +550,7 @@ __global__ void __launch_bounds__(kWdThreads, 1)
     mbar_init(prod_done, 1);
     mbar_init(tmem_done, 128);
     for (int i = 0; i < 4; ++i) patch_cnt[i] = 0;
+    fin[0] = 0;
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -1104,7 +1116,7 @@ __global__ void __launch_bounds__(kWdThreads, 1)
       if (ts == 0) s_scratch[0] = pend_prev == (unsigned)(pend_nparts - 1);
       group_sync();
       if (s_scratch[0])
-        wd_merge<D, T>(a, pend_b, pend_head0, pend_nparts, reinterpret_cast<float *>(sm + Sh::kPOff),
+        wd_merge<D, T, 128>(a, pend_b, pend_head0, pend_nparts, reinterpret_cast<float *>(sm + Sh::kPOff),
                        2 * Sh::kPBytes / 4, s_scratch, pend_cnt, ts, group_sync);
       group_sync();
       pend = false;
@@ -1269,11 +1281,23 @@ __global__ void __launch_bounds__(kWdThreads, 1)
     }
     tc_fence_before();
     mbar_arrive(tmem_done);  // no tensor-memory access after this
-    if (ok) settle();        // the last item's merge, if it was the last partition
+    // the last item's merge, if it was the last partition, is left to the
+    // whole CTA after the barrier below (the other roles are done by then):
+    // twice the threads, half the rounds of partial loads
+    if (ts == 0) {
+      fin[0] = ok && pend && pend_prev == (unsigned)(pend_nparts - 1);
+      fin[1] = pend_b;
+      fin[2] = pend_head0;
+      fin[3] = pend_nparts;
+      fin[4] = pend ? (int)(pend_cnt - a.ws_cnt) : 0;
+    }
     if (!ok && lane == 0) abort_cta();
   }
 
   __syncthreads();
+  if (fin[0])
+    wd_merge<D, T, kWdThreads>(a, fin[1], fin[2], fin[3], reinterpret_cast<float *>(sm + Sh::kPOff),
+                               2 * Sh::kPBytes / 4, s_scratch, a.ws_cnt + fin[4], tid, CtaSync());
   if (tid == 0) {
     // the last CTA of the launch puts the work counters back for the next
     // (every claim of this CTA was an atomic whose value it used before the
