@@ -21,6 +21,7 @@ from ._binding import (  # noqa: F401
     PKV_ERR_OUT_OF_BLOCKS,
     BlockManager,
     PkvError,
+    PreparedCall,
     DecodeWorkspace,
     exported_symbols,
     library_path,
@@ -42,4 +43,6 @@ from ._binding import (  # noqa: F401
     pkv_write,
     pkv_write_decode_attention,
     pkv_write_xpacked,
+    prepare_decode_attention,
+    prepare_write_decode_attention,
 )

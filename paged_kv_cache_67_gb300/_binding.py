@@ -266,6 +266,70 @@ def pkv_write_decode_attention(out, q, k, v, slot_mapping, k_cache, v_cache, blo
     return out
 
 
+class PreparedCall:
+    """One library call whose arguments were checked and marshalled once.
+
+    Calling it enqueues the call again on the same tensors' memory (their
+    storage must stay where it was: write new inputs into the same tensors,
+    as a serving loop that reuses its step buffers does) with the argument
+    list built at preparation, so each call costs one ctypes call and no
+    Python-side checks.  Raises PkvError on a status other than PKV_OK."""
+
+    __slots__ = ("_fn", "_args", "_what", "_keep")
+
+    def __init__(self, fn, args, what, keep):
+        self._fn, self._args, self._what, self._keep = fn, tuple(args), what, keep
+
+    def __call__(self):
+        status = self._fn(*self._args)
+        if status != 0:
+            raise PkvError(status, self._what)
+
+
+def prepare_write_decode_attention(out, q, k, v, slot_mapping, k_cache, v_cache, block_tables,
+                                   context_lens, scale: float, max_context_len: int = 0,
+                                   partition_size: int = 0, workspace=None, err_flags=None,
+                                   stream=None) -> PreparedCall:
+    """pkv_write_decode_attention, checked and marshalled once: returns a
+    callable that enqueues the step on the same buffers (see PreparedCall)."""
+    lib = load_library()
+    dev = _decode_checks(out, q, k_cache, v_cache, block_tables, context_lens)
+    B, H, D = q.shape
+    nb, bs, kvh, _ = k_cache.shape
+    _require(k.dim() == 3 and v.shape == k.shape and k.shape == (B, kvh, D), "k, v must be [B, KVH, D]")
+    _require(k.stride(2) == 1 and k.stride(1) == D and v.stride(2) == 1 and v.stride(1) == D,
+             "each token's [KVH, D] row must be contiguous")
+    _require(k.dtype == v.dtype == q.dtype, "dtype mismatch")
+    _require(slot_mapping.dtype == torch.int64 and slot_mapping.is_contiguous()
+             and slot_mapping.shape == (B,), "slot_mapping must be contiguous int64 [B]")
+    _require(all(t.device == dev for t in (k, v, slot_mapping)), "all tensors must be on the same CUDA device")
+    ws_ptr, ws_bytes = _workspace_arg(workspace)
+    args = (_ptr(out), _ptr(q), _ptr(k), _ptr(v), k.stride(0) if B > 0 else kvh * D,
+            v.stride(0) if B > 0 else kvh * D, _ptr(slot_mapping), _ptr(k_cache), _ptr(v_cache),
+            _ptr(block_tables), _ptr(context_lens), B, H, kvh, D, bs, block_tables.shape[1], nb,
+            float(scale), _DT[q.dtype], int(max_context_len), int(partition_size), ws_ptr, ws_bytes,
+            _ptr(err_flags), _stream_handle(stream, dev))
+    keep = (out, q, k, v, slot_mapping, k_cache, v_cache, block_tables, context_lens, workspace, err_flags)
+    return PreparedCall(lib.pkv_write_decode_attention, args, "pkv_write_decode_attention", keep)
+
+
+def prepare_decode_attention(out, q, k_cache, v_cache, block_tables, context_lens, scale: float,
+                             max_context_len: int = 0, partition_size: int = 0, workspace=None,
+                             err_flags=None, stream=None) -> PreparedCall:
+    """pkv_decode_attention, checked and marshalled once (see PreparedCall)."""
+    lib = load_library()
+    dev = _decode_checks(out, q, k_cache, v_cache, block_tables, context_lens)
+    B, H, D = q.shape
+    nb, bs, kvh, _ = k_cache.shape
+    ws_ptr, ws_bytes = _workspace_arg(workspace)
+    args = (_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(context_lens),
+            B, H, kvh, D, bs, block_tables.shape[1], nb, float(scale), _DT[q.dtype],
+            int(max_context_len), int(partition_size), ws_ptr, ws_bytes, _ptr(err_flags),
+            _stream_handle(stream, dev))
+    keep = (out, q, k_cache, v_cache, block_tables, context_lens, workspace, err_flags)
+    return PreparedCall(lib.pkv_decode_attention, args, "pkv_decode_attention", keep)
+
+
 def pkv_prefill_attention(out, q, k_cache, v_cache, block_tables, cu_seqlens_q, context_lens,
                           scale: float, max_q_len: int = 0, err_flags=None, stream=None):
     """Paged causal prefill attention into ``out`` [total_q, H, D] (returned):

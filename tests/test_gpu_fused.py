@@ -339,3 +339,38 @@ def test_fused_step_odd_slots_and_cut_contexts(H, KVH, D, bs):
     for b in (1, 2, 5):
         assert_close(out[b], want[b], torch.bfloat16, f"sequence {b}")
     assert bool((out[0] == 0).all())
+
+
+def test_prepared_call_matches_the_plain_call():
+    """prepare_write_decode_attention: checked once, then each call enqueues
+    the step on the same buffers; refilling the input tensors between calls
+    gives each step's own result, equal to the plain call's bit for bit."""
+    lens = [40, 1, 333, 128]
+    case = random_paged_case(91, lens, H=8, KVH=2, D=128, bs=16, dtype=torch.bfloat16, poison=False)
+    d = lambda t: t.to(DEV)
+    q, tables, lens_t = d(case["q"]), d(case["block_tables"]), d(case["context_lens"])
+    kc, vc = d(case["k_cache"]), d(case["v_cache"])
+    kc2, vc2 = kc.clone(), vc.clone()
+    g = torch.Generator().manual_seed(92)
+    k = torch.empty((4, 2, 128), dtype=torch.bfloat16, device=DEV)
+    v = torch.empty_like(k)
+    slots = torch.tensor([wl.slot_of(case["owned"][b], n - 1, 16) for b, n in enumerate(lens)],
+                         device=DEV)
+    out = torch.empty_like(q)
+    ws = pkv.DecodeWorkspace(4, 8, 2, 128, 16, tables.shape[1], device=DEV)
+    ws2 = pkv.DecodeWorkspace(4, 8, 2, 128, 16, tables.shape[1], device=DEV)
+    call = pkv.prepare_write_decode_attention(out, q, k, v, slots, kc, vc, tables, lens_t, 0.09,
+                                              workspace=ws)
+    for step in range(3):
+        k.copy_(torch.randn((4, 2, 128), generator=g).to(torch.bfloat16))
+        v.copy_(torch.randn((4, 2, 128), generator=g).to(torch.bfloat16))
+        q.copy_(torch.randn((4, 8, 128), generator=g).to(torch.bfloat16))
+        call()
+        want = pkv.pkv_write_decode_attention(torch.empty_like(q), q, k, v, slots, kc2, vc2, tables,
+                                              lens_t, 0.09, workspace=ws2)
+        torch.cuda.synchronize()
+        assert torch.equal(bits(out), bits(want)), f"step {step}"
+        assert torch.equal(bits(kc), bits(kc2)) and torch.equal(bits(vc), bits(vc2))
+    with pytest.raises(ValueError):  # checked at preparation
+        pkv.prepare_write_decode_attention(out, q, k[:1], v, slots, kc, vc, tables, lens_t, 0.09,
+                                           workspace=ws)
