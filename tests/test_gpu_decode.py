@@ -10,7 +10,7 @@ import torch
 import oracle
 import paged_kv_cache_67_gb300 as pkv
 from paged_kv_cache_67_gb300 import workloads as wl
-from gpu_helpers import assert_close, gpu_decode, oracle_decode
+from gpu_helpers import assert_close, bits, gpu_decode, oracle_decode
 from oracle_pins import random_paged_case
 
 pytestmark = pytest.mark.gpu
@@ -311,3 +311,39 @@ def test_step_loop_in_cuda_graph():
         assert bool((s_out[B - cfg.pad_seqs:] == 0).all())  # padded sequences
     assert torch.equal(kc.cpu(), kc_o) and torch.equal(vc.cpu(), vc_o)
     assert int((kc == wl.SENTINEL).sum()) == 0  # I1 across the loop
+
+
+def test_forced_kernels_agree_and_refuse_what_they_cannot_run():
+    """pkv_decode_attention_with_kernel: the CUDA-core and the TMA +
+    mma.sync kernels on the same bf16 batch both match the oracle (and the
+    plan's choice, -1, is pkv_decode_attention itself); a kernel that cannot
+    run the shape (the wide-group kernel at 4 heads per KV head, the
+    tensor-core kernels on fp32) answers PKV_ERR_UNSUPPORTED."""
+    lens = [1, 17, 300, 1000]
+    case = random_paged_case(71, lens, H=8, KVH=2, D=128, bs=16, dtype=torch.bfloat16)
+    d = [t.to(DEV) for t in (case["q"], case["k_cache"], case["v_cache"], case["block_tables"],
+                             case["context_lens"])]
+    want = oracle_decode(*[case[k] for k in ("q", "k_cache", "v_cache", "block_tables",
+                                             "context_lens")], 0.1)
+    ws = pkv.DecodeWorkspace(4, 8, 2, 128, 16, d[3].shape[1], device=DEV)
+    outs = {}
+    for kern in (pkv.KERNEL_AUTO, pkv.KERNEL_CUDA_CORE, pkv.KERNEL_TC):
+        out = torch.full_like(d[0], float("nan"))
+        pkv.pkv_decode_attention_with_kernel(out, *d, 0.1, kern, workspace=ws)
+        torch.cuda.synchronize()
+        assert_close(out, want, torch.bfloat16, f"kernel {kern}")
+        outs[kern] = out
+    plain, _ = gpu_decode(*d, 0.1)
+    assert torch.equal(bits(outs[pkv.KERNEL_AUTO]), bits(plain))
+    with pytest.raises(pkv.PkvError) as e:
+        pkv.pkv_decode_attention_with_kernel(torch.empty_like(d[0]), *d, 0.1, pkv.KERNEL_WIDE,
+                                             workspace=ws)
+    assert e.value.status == 2
+    f = [t.float() if t.is_floating_point() else t for t in d]
+    with pytest.raises(pkv.PkvError) as e:
+        pkv.pkv_decode_attention_with_kernel(torch.empty_like(f[0]), *f, 0.1, pkv.KERNEL_TC,
+                                             workspace=ws)
+    assert e.value.status == 2
+    with pytest.raises(pkv.PkvError) as e:
+        pkv.pkv_decode_attention_with_kernel(torch.empty_like(d[0]), *d, 0.1, 7, workspace=ws)
+    assert e.value.status == 1
