@@ -67,15 +67,20 @@ bool make_plan(int B, int H, int KVH, int D, int bs, int max_blocks, int max_con
   if (partition_size > 0) {
     p.P = partition_size;
   } else {
-    // About four CTAs per resident CTA slot: split each (sequence, head
-    // group) unit into enough partitions of the capacity, but never below
-    // 1024 tokens (each CTA pays a fixed start-up and merge cost) nor below
-    // the floor that bounds the partitions per sequence.  With enough units
-    // to fill the GPU nothing is split.
+    // About four CTAs per resident CTA slot (two for the tensor-core kernel
+    // when the units alone do not fill the slots: fewer, longer CTAs pay
+    // the per-CTA start-up and drain fewer times -- on the long-context
+    // batch, three seeds, 0.945 of the copy peak at two against 0.916 at
+    // four, 0.878-0.912 at 2.5-6): split each (sequence, head group) unit
+    // into enough partitions of the capacity, but never below 1024 tokens
+    // (each CTA pays a fixed start-up and merge cost) nor below the floor
+    // that bounds the partitions per sequence.  With enough units to fill
+    // the GPU nothing is split.
     const long long units = (long long)B * KVH * p.gchunks;
     const int per_sm = p.kernel ? (D <= 128 ? 2 : 1) : 4;
     const long long slots = (long long)(num_sms > 0 ? num_sms : 1) * per_sm;
-    long long parts = units > 0 ? (4 * slots + units - 1) / units : 1;
+    const long long per_slot = (p.kernel == 1 && units < slots) ? 2 : 4;
+    long long parts = units > 0 ? (per_slot * slots + units - 1) / units : 1;
     if (parts < 1) parts = 1;
     int P = round_up((cap + parts - 1) / parts, 16);
     const int floor_p = auto_partition_floor(cap);

@@ -43,7 +43,7 @@ def test_single_step_workload_full_size(name):
                                          max_ctx, dtype=cfg.dtype)
     assert kern == EXPECTED_KERNEL[name]
     if name == "long_bf16":
-        assert parts > 16  # the partitioned path and its merge, at full size
+        assert parts > 1  # the partitioned path and its merge, at full size
     kc0, vc0 = inp.k_cache.cpu(), inp.v_cache.cpu()
 
     # the library: two launches (write, then decode) on copies, then the
