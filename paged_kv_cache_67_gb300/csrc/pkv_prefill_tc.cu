@@ -658,7 +658,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                 if (global_timer_ns() - t0 > kWaitLimitNs) break;
               }
             }
-            ok = mbar_wait_bounded(&p_full[g], tcnt[g] & 1) && !aborted();
+            ok = mbar_wait_bounded(&p_full[g], tcnt[g] & 1);
             ++tcnt[g];
             if (!ok) break;
             if (!v_ready) {
@@ -668,6 +668,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             }
             tc_fence_after();
             issue_pv(g, ring, j > 0);
+            // the tile's last P . V: its V slot is free once that has run
+            if (g == kPfGroups - 1 || j >= item.nt[g + 1]) umma_commit(&v_empty[ring % kPfStages]);
             if (j + 1 < item.nt[g]) {
               if (!k_ready) {
                 ok = mbar_wait_bounded(&k_full[(ring + 1) % kPfStages], ((ring + 1) / kPfStages) & 1);
@@ -681,10 +683,10 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             }
           }
           if (!ok) break;
-          umma_commit(&v_empty[ring % kPfStages]);
           if (j + 1 < item.ntiles) umma_commit(&k_empty[(ring + 1) % kPfStages]);
         }
         ring0 = ring_next;
+        if (ok && aborted()) ok = false;
 #pragma unroll
         for (int g = 0; g < kPfGroups; ++g) ig[g] += item.nt[g] > 0;
       }
@@ -740,24 +742,30 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         tc_fence_after();
         const int t0 = j * kPfTile;
         const int ring = ring0 + j;
-        // pass 1: row max (scores raw when scale > 0: the max commutes)
+        // the row's 128 scores in registers: both loads in flight, one wait
+        // (scores raw when scale > 0: the max commutes with the scale)
+        uint32_t sa[64], sb[64];
+        tmem_ld64_nowait(tmem_sp, sa);
+        tmem_ld64_nowait(tmem_sp + 64, sb);
+        tmem_wait_ld_bind64(sa);
+        reg_bind64(sb);
+        float sc[128];
+#pragma unroll
+        for (int i = 0; i < 64; ++i) {
+          sc[i] = __uint_as_float(sa[i]);
+          sc[64 + i] = __uint_as_float(sb[i]);
+        }
+        if (!pos_scale) {
+#pragma unroll
+          for (int i = 0; i < 128; ++i) sc[i] *= sl2;
+        }
+        if (t0 + kPfTile - 1 > p_row) {
+#pragma unroll
+          for (int i = 0; i < 128; ++i) sc[i] = t0 + i <= p_row ? sc[i] : -INFINITY;
+        }
         float mx = -INFINITY;
 #pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-          const int tb = t0 + 64 * hf;
-          float s[64];
-          tmem_ld64(tmem_sp + 64 * hf, s);
-          if (!pos_scale) {
-#pragma unroll
-            for (int i = 0; i < 64; ++i) s[i] *= sl2;
-          }
-          if (tb + 63 > p_row) {
-#pragma unroll
-            for (int i = 0; i < 64; ++i) s[i] = tb + i <= p_row ? s[i] : -INFINITY;
-          }
-#pragma unroll
-          for (int i = 0; i < 64; i += 2) mx = max3f(mx, s[i], s[i + 1]);
-        }
+        for (int i = 0; i < 128; i += 2) mx = max3f(mx, sc[i], sc[i + 1]);
         if (pos_scale) mx *= sl2;
         // the reference max moves only when the row max exceeds it by 2^8
         const float m_new = (mx > m_used + 8.f) ? mx : m_used;
@@ -765,8 +773,31 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         const bool rescale = __any_sync(0xffffffffu, m_new != m_used) && j > 0;
         l *= alpha;
         m_used = m_new;
+        // P = 2^(s * scale * log2(e) - m), rounded to the input type, two
+        // tokens per column over the first 64 S columns; l sums the
+        // unrounded weights
+        float2 lsum = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          uint32_t pk[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const int c = 64 * hf + 2 * i;
+            float2 x = ffma2(make_float2(sc[c], sc[c + 1]), make_float2(mul, mul),
+                             make_float2(-m_used, -m_used));
+            x.x = fast_exp2(x.x);
+            x.y = fast_exp2(x.y);
+            lsum = fadd2(lsum, x);
+            pk[i] = PackPair<T>::pack(x.x, x.y);
+          }
+          tmem_st32u_nowait(tmem_sp + 32 * hf, pk);
+        }
+        tmem_wait_st();
+        l += lsum.x + lsum.y;
         // O is final for tile j-1 here: the commit that signalled S_g(j) also
-        // covers P_g(j-1) . V, issued before it
+        // covers P_g(j-1) . V, issued before it.  The rescale and the zeroed V
+        // rows come after P (the scores' registers are free by then) and
+        // before the arrive that lets P_g(j) . V_j go.
         if (rescale) {
 #pragma unroll
           for (int c = 0; c < D / 32; ++c) {
@@ -795,37 +826,6 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                 *reinterpret_cast<uint4 *>(vrow + rg * kKVRegion + c * 16) = make_uint4(0, 0, 0, 0);
           }
         }
-        // pass 2: P = 2^(s * scale * log2(e) - m), rounded to the input type,
-        // two tokens per column over S columns already read (P columns
-        // 32 hf .. +31 lie below S columns 64 hf read in this or the earlier
-        // step); l sums the unrounded weights
-        float2 lsum = make_float2(0.f, 0.f);
-#pragma unroll 1
-        for (int hf = 0; hf < 2; ++hf) {   // 64 tokens at a time: P columns 32 hf .. +31
-          const int tb = t0 + 64 * hf;
-          float s[64];
-          tmem_ld64(tmem_sp + 64 * hf, s);
-          if (!pos_scale) {
-#pragma unroll
-            for (int i = 0; i < 64; ++i) s[i] *= sl2;
-          }
-          if (tb + 63 > p_row) {
-#pragma unroll
-            for (int i = 0; i < 64; ++i) s[i] = tb + i <= p_row ? s[i] : -INFINITY;
-          }
-          uint32_t pk[32];
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            float2 x = ffma2(make_float2(s[2 * i], s[2 * i + 1]), make_float2(mul, mul),
-                             make_float2(-m_used, -m_used));
-            x.x = fast_exp2(x.x);
-            x.y = fast_exp2(x.y);
-            lsum = fadd2(lsum, x);
-            pk[i] = PackPair<T>::pack(x.x, x.y);
-          }
-          tmem_st32u(tmem_sp + 32 * hf, pk);
-        }
-        l += lsum.x + lsum.y;
         // the zeroed V rows (generic writes) before the product reads them
         if (past_end) fence_proxy_async_shared();
         tc_fence_before();
