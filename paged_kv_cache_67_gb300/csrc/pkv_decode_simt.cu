@@ -106,10 +106,11 @@ __global__ void __launch_bounds__(32 * kSimtWarps) pkv_decode_simt_kernel(const 
     // kU tokens of the warp per step: every row load of the step is issued
     // before any is used, so the step costs one memory round trip, not kU;
     // the tokens are still taken in the warp's order (same results).  Only
-    // for head_dim <= 64: with more values per lane the extra registers
-    // halve the resident CTAs, which cost more than the round trips saved
-    // (bf16, head_dim 128: 543 -> 829 us on the 8B-shaped batch at kU = 4).
-    constexpr int kU = EPL <= 2 ? 4 : 1;
+    // for head_dim <= 64 (four registers per token): with more values per
+    // lane the extra registers halve the resident CTAs, which cost more than
+    // the round trips saved (bf16, head_dim 128: 543 -> 829 us on the
+    // 8B-shaped batch at kU = 4).
+    constexpr int kU = EPL <= 2 ? 8 : 1;
     for (int tu = ta + w; tu < tb; tu += kSimtWarps * kU) {
       float kx[kU][EPL], vx[kU][EPL];
 #pragma unroll
