@@ -1054,20 +1054,25 @@ __global__ void __launch_bounds__(kWdThreads, 1)
       const int L0 = loads;
       loads += 2 * item.ntiles;
       if (item.patch_row < 0) continue;
-      // a context cut short by the host's bound never reaches here with its
-      // true length (the batch checks write its row)
-      const bool has = snew >= 0 && max(__ldg(a.lens + item.b), 0) == item.n;
+      // Every load the item needs is in flight at once (one round trip, not
+      // three): the new token's slot (above), the context's length, the new K and V
+      // rows (row b of the new-token inputs exists for every sequence), and
+      // for head chunk 0 the table entry of position n - 1 that the cache
+      // write is checked against.  The rows are patched into the landed
+      // tiles first -- the MMA thread waits for them -- and the cache row is
+      // written after (nothing in this launch reads it from the cache).
+      // A context cut short by the host's bound never reaches here with its
+      // true length (the batch checks write its row).
+      const int len_b = __ldg(a.lens + item.b);
       uint4 kv = make_uint4(0, 0, 0, 0), vv = kv;
-      if (has && lane < kRowVecs) {
+      if (lane < kRowVecs) {
         kv = __ldg(append_src<T>(a, false, item.b, item.kvh) + lane);
         vv = __ldg(append_src<T>(a, true, item.b, item.kvh) + lane);
       }
-      if (has && item.hc == 0) {
-        int wr = 0;
-        if (lane == 0) wr = append_check(a, item.b, item.kvh, snew, item.n);
-        if (__shfl_sync(0xffffffffu, wr, 0) && lane < kRowVecs)
-          append_store<T>(a, item.kvh, snew, lane, kv, vv);
-      }
+      const int phys_last = (item.hc == 0 && lane == 0)
+                                ? __ldg(a.tables + (size_t)item.b * a.max_blocks + (item.n - 1) / a.bs)
+                                : 0;
+      const bool has = snew >= 0 && max(len_b, 0) == item.n;
       const int r = item.patch_row;
       ++npatch;
       // 16-byte column lane & 7 of the 64-value region lane >> 3, row r,
@@ -1091,6 +1096,12 @@ __global__ void __launch_bounds__(kWdThreads, 1)
         if (lane == 0) wd_count_store(patch_cnt + 2 + v, npatch);
       }
       if (!ok) break;
+      if (has && item.hc == 0) {
+        int wr = 0;
+        if (lane == 0) wr = append_check_entry(a, item.kvh, snew, item.n, phys_last);
+        if (__shfl_sync(0xffffffffu, wr, 0) && lane < kRowVecs)
+          append_store<T>(a, item.kvh, snew, lane, kv, vv);
+      }
     }
     if (!ok && lane == 0) abort_cta();
   } else {
@@ -1217,20 +1228,22 @@ __global__ void __launch_bounds__(kWdThreads, 1)
           *reinterpret_cast<unsigned short *>(pb + h * 128 + ((c16 ^ (h & 7)) << 4)) = wd_bits<T>(p);
         }
         // the tile's V rows past the partition are zeroed (they may hold
-        // anything, and 0 * NaN would poison the product)
+        // anything, and 0 * NaN would poison the product): in each 64-value
+        // region they are one contiguous run of 128-byte rows, written by
+        // the 128 threads as consecutive 16-byte vectors (a row per thread
+        // put eight lanes of every store on the same banks: ~2 us a tile)
         const int vl = L0 + wd_vidx(j, item.ntiles);
         if (item.t0 + (j + 1) * kWdTile > item.t1) {
           const int vs = vl % Sh::kSlots;
           ok = __all_sync(0xffffffffu, mbar_wait_bounded(&slot_full[vs], (vl / Sh::kSlots) & 1));
           if (!ok) break;
-          if (!valid) {
-            uint8_t *vrow = sm + vs * Sh::kTileBytes + t * 128;
+          const int v_rows = item.t1 - (item.t0 + j * kWdTile);   // 1 .. 127
+          const int vecs = (kWdTile - v_rows) * 8;                // per region
+          uint8_t *vtail = sm + vs * Sh::kTileBytes + v_rows * 128;
 #pragma unroll
-            for (int r = 0; r < Sh::kRegions; ++r)
-#pragma unroll
-              for (int c = 0; c < 8; ++c)
-                *reinterpret_cast<uint4 *>(vrow + r * Sh::kRegionBytes + c * 16) = make_uint4(0, 0, 0, 0);
-          }
+          for (int r = 0; r < Sh::kRegions; ++r)
+            for (int i = ts; i < vecs; i += 128)
+              *reinterpret_cast<uint4 *>(vtail + r * Sh::kRegionBytes + i * 16) = make_uint4(0, 0, 0, 0);
         }
         fence_proxy_async_shared();  // P^T and zeroed rows before the product reads them
         tc_fence_before();

@@ -413,18 +413,25 @@ __device__ __forceinline__ const uint4 *append_src(const DecodeArgs &a, bool is_
 // n-1 lives -- the physical block the table gives for it, row (n-1) % bs --
 // and inside the pool.  Flags are raised for KV head 0 only.  Returns
 // whether the row may be written.
-__device__ __forceinline__ bool append_check(const DecodeArgs &a, int b, int kvh, long long slot,
-                                             int n) {
+// The same check given the table entry of position n - 1 (`phys`, read by
+// the caller; ignored when n == 0).
+__device__ __forceinline__ bool append_check_entry(const DecodeArgs &a, int kvh, long long slot,
+                                                   int n, int phys) {
   bool match = false;
   if (n > 0) {
     const int lb = (n - 1) / a.bs;
-    const int phys = __ldg(a.tables + (size_t)b * a.max_blocks + lb);
     match = (long long)phys * a.bs + (n - 1 - lb * a.bs) == slot;
   }
   if (!match && kvh == 0) raise_flag(a.err, PKV_FLAG_APPEND_MISMATCH);
   const bool in_pool = slot < a.num_blocks * (long long)a.bs;
   if (!in_pool && kvh == 0) raise_flag(a.err, PKV_FLAG_SLOT_OUT_OF_RANGE);
   return in_pool;
+}
+
+__device__ __forceinline__ bool append_check(const DecodeArgs &a, int b, int kvh, long long slot,
+                                             int n) {
+  const int phys = n > 0 ? __ldg(a.tables + (size_t)b * a.max_blocks + (n - 1) / a.bs) : 0;
+  return append_check_entry(a, kvh, slot, n, phys);
 }
 
 // 16-byte vector j of the K and V rows of KV head kvh at cache row `slot`.
