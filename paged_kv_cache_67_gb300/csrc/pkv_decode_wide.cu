@@ -282,25 +282,30 @@ __device__ __forceinline__ uint32_t wd_pack2(float lo, float hi) {
 }
 
 // The end of one item, by the 128 softmax threads (thread ts, barrier
-// `sync`), given per head r: s_m[r] running max (log2 units), s_l[r] sum of
-// 2^(score - s_m[r]), s_o[r * D + d] the weighted V sum.  One partition:
-// the output rows s_o / s_l.  Otherwise the partials go to the workspace and
+// `sync`), given per head r: s_m[r] running max (log2 units), the sum of
+// 2^(score - s_m[r]) as four partial sums s_lw[w * 16 + r] (one per softmax
+// warp, added here by each thread that needs them), s_o[r * D + d] the
+// weighted V sum.  One partition:
+// the output rows s_o / l.  Otherwise the partials go to the workspace and
 // thread 0 counts the partition with an acquire-release atomic whose result
 // it reads only later (at the next item's end, where the last partition
 // merges): the atomic's round trip is not waited for.  Returns whether a
 // count is pending.
 template <int D, typename T, typename Sync>
 __device__ bool wd_publish(const DecodeArgs &a, int b, int head0, int part, int nparts,
-                           const float *s_m, const float *s_l, const float *s_o, int *counter,
+                           const float *s_m, const float *s_lw, const float *s_o, int *counter,
                            int ts, Sync sync, unsigned *prev) {
   T *out = reinterpret_cast<T *>(a.out);
   const size_t row0 = (size_t)b * a.H + head0;
+  auto l_of = [&](int r) {
+    return (s_lw[r] + s_lw[kWdHeads + r]) + (s_lw[2 * kWdHeads + r] + s_lw[3 * kWdHeads + r]);
+  };
   if (nparts == 1) {
     // eight outputs per thread and step: one 16-byte store
     for (int i = ts; i < kWdHeads * D / 8; i += 128) {
       const float4 x0 = *reinterpret_cast<const float4 *>(s_o + 8 * i);
       const float4 x1 = *reinterpret_cast<const float4 *>(s_o + 8 * i + 4);
-      const float inv_l = 1.f / s_l[8 * i / D];
+      const float inv_l = 1.f / l_of(8 * i / D);
       uint4 v;
       v.x = wd_pack2<T>(x0.x * inv_l, x0.y * inv_l);
       v.y = wd_pack2<T>(x0.z * inv_l, x0.w * inv_l);
@@ -312,7 +317,7 @@ __device__ bool wd_publish(const DecodeArgs &a, int b, int head0, int part, int 
   }
   if (ts < kWdHeads) {
     a.ws_m[(row0 + ts) * a.max_parts + part] = s_m[ts];
-    a.ws_l[(row0 + ts) * a.max_parts + part] = s_l[ts];
+    a.ws_l[(row0 + ts) * a.max_parts + part] = l_of(ts);
   }
   for (int i = ts; i < kWdHeads * D / 4; i += 128) {
     const int r = 4 * i / D, d = 4 * i - r * D;
@@ -517,8 +522,7 @@ __global__ void __launch_bounds__(kWdThreads, 1)
   float *s_red = reinterpret_cast<float *>(bars + 44);              // [2][4 warps][16]
   int *s_vote = reinterpret_cast<int *>(s_red + 2 * 4 * kWdHeads);  // [2][4]
   float *s_m = reinterpret_cast<float *>(s_vote + 8);               // [16]
-  float *s_l = s_m + kWdHeads;                                      // [16]
-  int *s_scratch = reinterpret_cast<int *>(s_l + kWdHeads);         // [1 + 2 * 16]
+  int *s_scratch = reinterpret_cast<int *>(s_m + 2 * kWdHeads);     // [1 + 2 * 16] (16 floats unused before)
   float *s_o = reinterpret_cast<float *>(sm + Sh::kOOff);           // [16][D]
   // fused step, per item that ends its context (counted in item order):
   // [0] / [1] the producer has issued the last tile's K / V load, [2] / [3]
@@ -1121,15 +1125,16 @@ __global__ void __launch_bounds__(kWdThreads, 1)
     int *pend_cnt = nullptr;
     unsigned pend_prev = 0;
     // the pending count's result: the last partition merges (the weights go
-    // to the P^T buffers, free between items)
+    // to the P^T buffers, free between items).  Thread 0 posts whether to
+    // merge (s_scratch[0]) before the item end's first barrier; settle runs
+    // after it.
     auto settle = [&]() {
       if (!pend) return;
-      if (ts == 0) s_scratch[0] = pend_prev == (unsigned)(pend_nparts - 1);
-      group_sync();
-      if (s_scratch[0])
+      if (s_scratch[0]) {
         wd_merge<D, T, 128>(a, pend_b, pend_head0, pend_nparts, reinterpret_cast<float *>(sm + Sh::kPOff),
                        2 * Sh::kPBytes / 4, s_scratch, pend_cnt, ts, group_sync);
-      group_sync();
+        group_sync();
+      }
       pend = false;
     };
     bool ok = true;
@@ -1172,11 +1177,16 @@ __global__ void __launch_bounds__(kWdThreads, 1)
           need |= x[h] > m_used[h] + 8.f;
         }
         // does any score of the tile pass its head's running max by 2^8?
+        // (always on an item's first tile, whose running maxima are -inf: no
+        // vote there)
         const int par = tg & 1;
-        const int need_w = __any_sync(0xffffffffu, need);
-        if (lane == 0) s_vote[par * 4 + (warp - 2)] = need_w;
-        group_sync();
-        const bool any = s_vote[par * 4] | s_vote[par * 4 + 1] | s_vote[par * 4 + 2] | s_vote[par * 4 + 3];
+        bool any = true;
+        if (j > 0) {
+          const int need_w = __any_sync(0xffffffffu, need);
+          if (lane == 0) s_vote[par * 4 + (warp - 2)] = need_w;
+          group_sync();
+          any = s_vote[par * 4] | s_vote[par * 4 + 1] | s_vote[par * 4 + 2] | s_vote[par * 4 + 3];
+        }
         if (any) {
           // per-head max of the tile over the 128 token lanes
 #pragma unroll
@@ -1275,14 +1285,12 @@ __global__ void __launch_bounds__(kWdThreads, 1)
       if (ts == 0) {
 #pragma unroll
         for (int h = 0; h < kWdHeads; ++h) s_m[h] = m_used[h];
+        if (pend) s_scratch[0] = pend_prev == (unsigned)(pend_nparts - 1);
       }
-      group_sync();
-      if (ts < kWdHeads)
-        s_l[ts] = (s_red[ts] + s_red[kWdHeads + ts]) + (s_red[2 * kWdHeads + ts] + s_red[3 * kWdHeads + ts]);
       group_sync();
       settle();  // the previous item's merge, if it was the last partition
       int *cnt = a.ws_cnt + (size_t)item.b * (a.KVH * w.hchunks) + item.kvh * w.hchunks + item.hc;
-      if (wd_publish<D, T>(a, item.b, head0, item.part, item.nparts, s_m, s_l, s_o, cnt, ts,
+      if (wd_publish<D, T>(a, item.b, head0, item.part, item.nparts, s_m, s_red, s_o, cnt, ts,
                            group_sync, &pend_prev)) {
         pend = true;
         pend_b = item.b;
