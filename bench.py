@@ -601,6 +601,14 @@ class DecodeRun:
                 sampler.window(h0, h1))
 
 
+def flop_per_byte(cfg):
+    """Decode arithmetic per byte of K/V read: per key and value row of D
+    elements, 2 * D flops of scores and 2 * D of weighted sum for each of
+    the G = H / KVH query heads, over 2 * D * element bytes."""
+    el = torch.empty((), dtype=cfg.dtype).element_size()
+    return round(2 * (cfg.H // cfg.KVH) / el, 2)
+
+
 def config_entry(run, args, stream, world, sampler, peak, flush):
     """One workload of the `configs` block: its decode kernel timed at the
     run's K and W, against the HBM peak.  Without `flush` the timed steps
@@ -637,7 +645,7 @@ def config_entry(run, args, stream, world, sampler, peak, flush):
         "kernel": run.kname, "kernel_us": round(kern_ms * 1e3, 2),
         "bytes_per_launch": round(kb), "achieved": round(achieved, 1), "unit": "GB/s",
         "peak": peak, "frac": round(achieved / peak, 4), "bound": "hbm",
-        "traffic": traffic,
+        "traffic": traffic, "flop_per_byte": flop_per_byte(run.cfg),
         "ms_per_step": round(elapsed * 1e3 / args.steps, 4), "timing": timing,
         "gpu_launches": args.steps * run.launches_per_step, "clocks": clocks,
         **({"gather_read_gbs": gather["gbs"],
@@ -669,6 +677,36 @@ def measure_copy(pkv, dev, stream):
         res[name] = round(2 * src.numel() / (ms * 1e-3) / 1e9, 1)
     del src, dst
     return res
+
+
+def measure_fma(pkv, dev, stream):
+    """In-run fp32 multiply-add rate of the CUDA cores (pkv_fp32_fma_peak:
+    eight blocks of 256 threads per SM, eight chains per thread), plain fmaf
+    and paired fma.rn.f32x2; TFLOP/s, best of 5 launches of ~1 ms."""
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    out = torch.empty(8 * sms, dtype=torch.float32, device=dev)
+    iters = 16384
+    flops = out.numel() * pkv.FMA_THREADS * pkv.FMA_CHAINS * iters * 2
+    res = {}
+    for name, paired in (("fmaf", False), ("fma_f32x2", True)):
+        for _ in range(3):
+            pkv.pkv_fp32_fma_peak(out, iters, 1.0, 1.0, paired=paired, stream=stream)
+        torch.cuda.synchronize()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(5)]
+        for a, b in evs:
+            a.record(stream)
+            pkv.pkv_fp32_fma_peak(out, iters, 1.0, 1.0, paired=paired, stream=stream)
+            b.record(stream)
+        torch.cuda.synchronize()
+        ms = min(a.elapsed_time(b) for a, b in evs)
+        res[name] = round(flops / (ms * 1e-3) / 1e12, 1)
+    if not torch.equal(out.cpu(), torch.full_like(out.cpu(), float(pkv.FMA_CHAINS * iters))):
+        raise RuntimeError("pkv_fp32_fma_peak: chains did not reach their exact value")
+    return {"fmaf_tflops": res["fmaf"], "fma_f32x2_tflops": res["fma_f32x2"],
+            "tflops": max(res.values()),
+            "what": f"pkv_fp32_fma_peak: {out.numel()} blocks x {pkv.FMA_THREADS} threads x "
+                    f"{pkv.FMA_CHAINS} chains x {iters} multiply-adds, best of 5"}
 
 
 def measure_gather(pkv, run, stream):
@@ -762,6 +800,7 @@ def _run_gpu(args, world, rank, dev, stream, peak, peak_kind, sampler, pkv):
                                     "torch_copy_gbs": copy["torch_copy"],
                                     "what": "1 GiB buffers, read + write bytes, best of 10, "
                                             "pkv_hbm_copy is the library's own copy kernel"}
+        extra["fma_fp32_in_run"] = measure_fma(pkv, dev, stream)
 
     run.warmup(args.warmup, stream)
     if args.graph:
@@ -802,7 +841,7 @@ def _run_gpu(args, world, rank, dev, stream, peak, peak_kind, sampler, pkv):
                      "kernel": run.kname, "bytes_per_launch": round(kern_bytes),
                      "peak_source": ("measured (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
                                      else "fallback 6.8 TB/s"),
-                     "kernel_us": round(dec_ms * 1e3, 2),
+                     "kernel_us": round(dec_ms * 1e3, 2), "flop_per_byte": flop_per_byte(cfg),
                      **({"frac_of_gather_read": round(achieved / extra["gather_read_in_run"]["gbs"], 4)}
                         if "gather_read_in_run" in extra else {})},
         **extra,

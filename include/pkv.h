@@ -418,6 +418,25 @@ PKV_API pkv_status pkv_hbm_gather_read(const void *base, const int32_t *chunk_in
                                        int64_t chunk_bytes, unsigned long long *sink,
                                        pkv_stream_t stream);
 
+/*
+ * pkv_fp32_fma_peak -- the CUDA-core yardstick: `blocks` blocks of 256
+ * threads, each thread running eight independent fp32 multiply-add chains
+ * x <- x * a + b from x = 0 for `iters` steps (fmaf, or with paired != 0 the
+ * two-lane fma.rn.f32x2 on four pairs): 2 * 8 * iters flops per thread.
+ * Thread 0 of block i stores the sum of its chains in out[i] (device
+ * float[blocks]); any other thread stores it only if it equals `never`, so
+ * no chain is dead code (pass a value no sum reaches).  With a = b = 1 every
+ * chain ends at exactly iters (iters < 2^24), which makes the result
+ * checkable.  The fp32 rate the CUDA cores reach in the same run, against
+ * which a decode's arithmetic (2 * G * D flops per key and per value row of
+ * D elements) is set when choosing tensor cores for a group of G query
+ * heads.  The pages have no counterpart.  Errors: PKV_ERR_INVALID_ARG
+ * (out NULL or not 4-byte aligned, blocks < 1 or > 2^20, iters < 0),
+ * PKV_ERR_CUDA.
+ */
+PKV_API pkv_status pkv_fp32_fma_peak(float *out, int blocks, int iters, float a, float b,
+                                     float never, int paired, pkv_stream_t stream);
+
 /* A static, human-readable name for a status code. */
 PKV_API const char *pkv_status_string(pkv_status status);
 

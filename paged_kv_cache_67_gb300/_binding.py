@@ -112,6 +112,9 @@ def load_library():
         lib.pkv_hbm_copy.restype = c_int
         lib.pkv_hbm_gather_read.argtypes = [vp, vp, i64, i64, i64, vp, vp]
         lib.pkv_hbm_gather_read.restype = c_int
+        lib.pkv_fp32_fma_peak.argtypes = [vp, c_int, c_int, ctypes.c_float, ctypes.c_float,
+                                          ctypes.c_float, c_int, vp]
+        lib.pkv_fp32_fma_peak.restype = c_int
         lib.pkv_status_string.argtypes = [c_int]
         lib.pkv_status_string.restype = ctypes.c_char_p
         lib.pkv_version.argtypes = []
@@ -440,6 +443,26 @@ def pkv_hbm_gather_read(base, chunk_index, chunk_stride_bytes: int, chunk_bytes:
     _check(lib.pkv_hbm_gather_read(_ptr(base), _ptr(chunk_index), n, int(chunk_stride_bytes),
                                    int(chunk_bytes), _ptr(sink), _stream_handle(stream, dev)),
            "pkv_hbm_gather_read")
+
+
+FMA_THREADS = 256   # threads per block of pkv_fp32_fma_peak
+FMA_CHAINS = 8      # independent multiply-add chains per thread
+
+
+def pkv_fp32_fma_peak(out, iters: int, a: float = 1.0, b: float = 1.0, never: float = -1.0,
+                      paired: bool = False, stream=None) -> None:
+    """The CUDA-core fp32 yardstick: out.numel() blocks of FMA_THREADS
+    threads, each running FMA_CHAINS multiply-add chains x <- x * a + b for
+    `iters` steps (2 * FMA_CHAINS * iters flops per thread); thread 0 of
+    block i stores the sum of its chains in out[i] (a contiguous float32
+    CUDA tensor).  ``paired`` uses the two-lane fma.rn.f32x2."""
+    lib = load_library()
+    _require(out.dtype == torch.float32 and out.is_contiguous() and out.device.type == "cuda",
+             "out must be a contiguous float32 CUDA tensor")
+    _require(int(iters) >= 0 and 1 <= out.numel() <= (1 << 20), "iters >= 0 and 1..2^20 blocks")
+    _check(lib.pkv_fp32_fma_peak(_ptr(out), out.numel(), int(iters), float(a), float(b), float(never),
+                                 int(bool(paired)), _stream_handle(stream, out.device)),
+           "pkv_fp32_fma_peak")
 
 
 PKV_ERR_OUT_OF_BLOCKS = 5

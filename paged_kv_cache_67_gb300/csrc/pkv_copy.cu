@@ -16,6 +16,11 @@
 // The gather: one warp per chunk at a time (chunks taken in list order,
 // grid-stride over warps), each lane with eight 16-byte loads in flight;
 // the words are folded by XOR into a checksum so that no load is dead.
+//
+//   pkv_fp32_fma_peak    the fp32 multiply-add rate of the CUDA cores: eight
+//                        independent chains per thread (enough, with eight
+//                        blocks of 256 threads per SM, to keep every lane's
+//                        FMA pipe busy), plain fmaf or paired fma.rn.f32x2.
 #include <algorithm>
 
 #include "pkv_device.cuh"
@@ -77,7 +82,47 @@ __global__ void __launch_bounds__(kGatherThreads) pkv_gather_read_kernel(
   if (lane == 0 && x != 0) atomicXor(sink, x);
 }
 
+constexpr int kFmaThreads = 256;
+constexpr int kFmaChains = 8;
+
+template <bool kPaired>
+__global__ void __launch_bounds__(kFmaThreads) pkv_fma_kernel(float *out, int iters, float a,
+                                                             float b, float never) {
+  float x[kFmaChains];
+#pragma unroll
+  for (int k = 0; k < kFmaChains; ++k) x[k] = 0.f;
+  if constexpr (kPaired) {
+    const float2 a2 = make_float2(a, a), b2 = make_float2(b, b);
+    float2 *x2 = reinterpret_cast<float2 *>(x);
+    for (int i = 0; i < iters; ++i) {
+#pragma unroll
+      for (int k = 0; k < kFmaChains / 2; ++k) x2[k] = ffma2(x2[k], a2, b2);
+    }
+  } else {
+    for (int i = 0; i < iters; ++i) {
+#pragma unroll
+      for (int k = 0; k < kFmaChains; ++k) x[k] = fmaf(x[k], a, b);
+    }
+  }
+  float s = 0.f;
+#pragma unroll
+  for (int k = 0; k < kFmaChains; ++k) s += x[k];
+  if (threadIdx.x == 0 || s == never) out[blockIdx.x] = s;
+}
+
 }  // namespace pkv
+
+extern "C" PKV_API pkv_status pkv_fp32_fma_peak(float *out, int blocks, int iters, float a, float b,
+                                                float never, int paired, pkv_stream_t stream) {
+  if (!out || reinterpret_cast<uintptr_t>(out) % 4 || blocks < 1 || blocks > (1 << 20) || iters < 0)
+    return PKV_ERR_INVALID_ARG;
+  const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (paired)
+    pkv::pkv_fma_kernel<true><<<blocks, pkv::kFmaThreads, 0, st>>>(out, iters, a, b, never);
+  else
+    pkv::pkv_fma_kernel<false><<<blocks, pkv::kFmaThreads, 0, st>>>(out, iters, a, b, never);
+  return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
 
 extern "C" PKV_API pkv_status pkv_hbm_gather_read(const void *base, const int32_t *chunk_index,
                                                   int64_t nchunks, int64_t chunk_stride_bytes,

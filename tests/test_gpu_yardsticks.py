@@ -3,7 +3,8 @@ copy bandwidth the kernels are set against) copies bit-exactly and rejects
 misaligned, ragged or overlapping ranges; pkv_hbm_gather_read (reads of
 listed chunks, the decode's access pattern without its arithmetic) reads
 exactly the listed chunks -- its XOR checksum equals one computed on the
-CPU over the same words."""
+CPU over the same words; pkv_fp32_fma_peak (the CUDA cores' fp32 rate) runs
+every chain to the exact value a = b = 1 gives, plain and paired."""
 import ctypes
 
 import numpy as np
@@ -58,3 +59,30 @@ def test_gather_reads_exactly_the_listed_chunks(chunk_bytes, stride):
     pkv.pkv_hbm_gather_read(pool.to(DEV), idx.to(DEV), stride, chunk_bytes, sink)
     torch.cuda.synchronize()
     assert int(sink.cpu().numpy().view(np.uint64)[0]) == want
+
+
+@pytest.mark.parametrize("paired", [False, True])
+@pytest.mark.parametrize("iters", [0, 1, 1000, 4097])
+def test_fma_chains_run_to_their_exact_value(paired, iters):
+    """x <- x * 1 + 1 from 0 is exactly iters after iters steps (iters <
+    2^24); thread 0 of every block stores the sum of its chains."""
+    out = torch.full((37,), -5.0, dtype=torch.float32, device=DEV)
+    pkv.pkv_fp32_fma_peak(out, iters, 1.0, 1.0, never=-1.0, paired=paired)
+    torch.cuda.synchronize()
+    assert torch.equal(out.cpu(), torch.full((37,), float(pkv.FMA_CHAINS * iters)))
+
+
+def test_fma_other_values_and_bad_args():
+    """a = 0.5, b = 1: a chain converges to 2 - 2^-iters (exact in fp32
+    for small iters); bad arguments are rejected before any launch."""
+    out = torch.zeros(4, dtype=torch.float32, device=DEV)
+    pkv.pkv_fp32_fma_peak(out, 10, 0.5, 1.0)
+    torch.cuda.synchronize()
+    assert torch.equal(out.cpu(), torch.full((4,), pkv.FMA_CHAINS * (2.0 - 2.0 ** -9)))
+    lib = pkv.load_library()
+    s = torch.cuda.current_stream().cuda_stream
+    p = out.data_ptr()
+    assert lib.pkv_fp32_fma_peak(ctypes.c_void_p(0), 4, 10, 1.0, 1.0, -1.0, 0, s) == 1
+    assert lib.pkv_fp32_fma_peak(ctypes.c_void_p(p + 2), 1, 10, 1.0, 1.0, -1.0, 0, s) == 1
+    assert lib.pkv_fp32_fma_peak(ctypes.c_void_p(p), 0, 10, 1.0, 1.0, -1.0, 0, s) == 1
+    assert lib.pkv_fp32_fma_peak(ctypes.c_void_p(p), 4, -1, 1.0, 1.0, -1.0, 0, s) == 1
