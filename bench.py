@@ -338,10 +338,22 @@ def cpu_baseline(inp, elem, seconds=10.0):
         if time.perf_counter() - t0 >= seconds:
             break
     dt = time.perf_counter() - t0
+    # the same units on one thread, a shorter sample
+    one_bytes, one_units, t1 = 0, 0, time.perf_counter()
+    while True:
+        b_u = order[(i + one_units) % len(order)]
+        run_oracle_units(oracle, cpu, [b_u], 1)
+        one_units += 1
+        one_bytes += unit_bytes(inp, b_u[0], elem)
+        if time.perf_counter() - t1 >= seconds / 3:
+            break
+    dt1 = time.perf_counter() - t1
     return {"value": done_bytes / dt / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
             "sample": (f"{done_units} (sequence, KV head) units of the {inp.cfg.name} workload "
                        f"({done_units / len(units):.2f} decode passes over its {len(units)} units), "
-                       f"fp64 C oracle, {dt:.1f} s on {threads} threads")}
+                       f"fp64 C oracle, {dt:.1f} s on {threads} threads"),
+            "single_thread": {"value": one_bytes / dt1 / 1e9, "unit": "GB/s",
+                              "sample": f"{one_units} units on one thread, {dt1:.1f} s"}}
 
 
 def run_reference(args, world, rank):
