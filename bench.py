@@ -721,22 +721,59 @@ def measure_fma(pkv, dev, stream):
                     f"{pkv.FMA_CHAINS} chains x {iters} multiply-adds, best of 5"}
 
 
+def gather_orders(pkv, dev, stream):
+    """The gather yardstick over the 8B-shaped batch's blocks in three
+    orders -- table order (the pages' random placement), sorted by physical
+    block, and one contiguous run of the pool -- K and V one launch each;
+    GB/s, best of 10.  Prints one JSON line."""
+    cfg = wl.CONFIGS["llama8b_bf16"]
+    inp = wl.make_decode_inputs(cfg, seed=1234, device=dev)
+    lens = [int(x) for x in inp.context_lens]
+    blocks = [blk for b, n in enumerate(lens) for blk in inp.owned[b][:-(-n // cfg.bs)]]
+    bb = cfg.bs * cfg.KVH * cfg.D * torch.empty((), dtype=cfg.dtype).element_size()
+    sink = torch.zeros(1, dtype=torch.int64, device=dev)
+    res = {"workload": "llama8b_bf16 (seed 1234)", "blocks": len(blocks),
+           "pool_blocks": int(inp.k_cache.shape[0]), "unit": "GB/s"}
+    for name, order in (("table_order", blocks), ("sorted", sorted(blocks)),
+                        ("contiguous", list(range(len(blocks))))):
+        idx = torch.tensor(order, dtype=torch.int32, device=dev)
+
+        def both():
+            for cache in (inp.k_cache, inp.v_cache):
+                pkv.pkv_hbm_gather_read(cache, idx, bb, bb, sink, stream=stream, check_bounds=False)
+
+        for _ in range(3):
+            both()
+        torch.cuda.synchronize()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(10)]
+        for a, b in evs:
+            a.record(stream)
+            both()
+            b.record(stream)
+        torch.cuda.synchronize()
+        ms = min(a.elapsed_time(b) for a, b in evs)
+        res[name] = round(2 * len(order) * bb / (ms * 1e-3) / 1e9, 1)
+    print(json.dumps(res), flush=True)
+
+
 def measure_gather(pkv, run, stream):
     """In-run read bandwidth of the batch's own access pattern without the
     arithmetic: every cache block the first input set's sequences use (K
-    then V), whole, in table order, read by pkv_hbm_gather_read; best of 10."""
+    then V), whole, in table order, read in one launch (as the decode reads
+    them) by pkv_hbm_gather_read_pair; best of 10."""
     inp, cfg = run.inp, run.cfg
     lens = [int(x) for x in inp.context_lens]
     blocks = [blk for b, n in enumerate(lens) for blk in inp.owned[b][:-(-n // cfg.bs)]]
     idx = torch.tensor(blocks, dtype=torch.int32, device=run.dev)
     block_bytes = cfg.bs * cfg.KVH * cfg.D * run.elem
     sink = torch.zeros(1, dtype=torch.int64, device=run.dev)
-    pkv.pkv_hbm_gather_read(inp.k_cache, idx, block_bytes, block_bytes, sink, stream=stream)
+    pkv.pkv_hbm_gather_read_pair(inp.k_cache, inp.v_cache, idx, block_bytes, block_bytes, sink,
+                                 stream=stream)
 
     def both():
-        for cache in (inp.k_cache, inp.v_cache):
-            pkv.pkv_hbm_gather_read(cache, idx, block_bytes, block_bytes, sink, stream=stream,
-                                    check_bounds=False)
+        pkv.pkv_hbm_gather_read_pair(inp.k_cache, inp.v_cache, idx, block_bytes, block_bytes, sink,
+                                     stream=stream, check_bounds=False)
 
     for _ in range(3):
         both()
@@ -753,7 +790,7 @@ def measure_gather(pkv, run, stream):
     return {"gbs": round(nbytes / (ms * 1e-3) / 1e9, 1), "bytes": nbytes, "blocks": len(blocks),
             "what": (f"every cache block the {cfg.name} batch uses ({len(blocks)} blocks of "
                      f"{block_bytes} B, K then V), whole, in table order, by the library's "
-                     f"gather-read kernel (pkv_hbm_gather_read): the batch's access pattern "
+                     f"gather-read kernel in one launch (pkv_hbm_gather_read_pair): the batch's access pattern "
                      f"without the arithmetic; best of 10")}
 
 
@@ -1113,6 +1150,9 @@ def main():
     ap.add_argument("--no-graph", dest="graph", action="store_false",
                     help="launch every timed step from the host, each decode launch between "
                          "its own CUDA events")
+    ap.add_argument("--gather-orders", action="store_true",
+                    help="only the gather yardstick over the 8B-shaped batch's blocks in table "
+                         "order, sorted and contiguous (one JSON line)")
     ap.add_argument("--layout", default="token-major", choices=["token-major", "xpacked"],
                     help="xpacked: the layout experiment (caches in vLLM's packed layout, "
                          "write + decode in two launches; with --only-decode)")
@@ -1127,7 +1167,15 @@ def main():
         ap.error("--kernel goes with --mode two-launch")
     world, rank, local = dist_setup()
     try:
-        if args.impl == "reference":
+        if args.gather_orders:
+            if rank == 0:
+                from paged_kv_cache_67_gb300 import build as libbuild
+                import paged_kv_cache_67_gb300 as pkv
+                libbuild.build()
+                torch.cuda.set_device(local)
+                dev = torch.device("cuda", local)
+                gather_orders(pkv, dev, torch.cuda.current_stream(dev))
+        elif args.impl == "reference":
             run_reference(args, world, rank)
         elif args.workload in wl.PREFILL_CONFIGS:
             run_prefill(args, world, rank, local)

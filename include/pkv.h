@@ -419,6 +419,20 @@ PKV_API pkv_status pkv_hbm_gather_read(const void *base, const int32_t *chunk_in
                                        pkv_stream_t stream);
 
 /*
+ * pkv_hbm_gather_read_pair -- the same reads over two buffers in one launch:
+ * every listed chunk of base_a, then every listed chunk of base_b (both
+ * 16-byte aligned, both holding every listed chunk), all folded into
+ * *sink.  Bytes read = 2 * nchunks * chunk_bytes.  The decode reads a
+ * batch's K and V blocks in one launch; so does this yardstick (two
+ * launches of half the size each pay their own ramp and tail).  Errors:
+ * PKV_ERR_INVALID_ARG (as pkv_hbm_gather_read, or base_b NULL), PKV_ERR_CUDA.
+ */
+PKV_API pkv_status pkv_hbm_gather_read_pair(const void *base_a, const void *base_b,
+                                            const int32_t *chunk_index, int64_t nchunks,
+                                            int64_t chunk_stride_bytes, int64_t chunk_bytes,
+                                            unsigned long long *sink, pkv_stream_t stream);
+
+/*
  * pkv_fp32_fma_peak -- the CUDA-core yardstick: `blocks` blocks of 256
  * threads, each thread running eight independent fp32 multiply-add chains
  * x <- x * a + b from x = 0 for `iters` steps (fmaf, or with paired != 0 the

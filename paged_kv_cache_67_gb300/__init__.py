@@ -37,6 +37,7 @@ from ._binding import (  # noqa: F401
     pkv_decode_workspace_size,
     pkv_hbm_copy,
     pkv_hbm_gather_read,
+    pkv_hbm_gather_read_pair,
     pkv_fp32_fma_peak,
     FMA_THREADS,
     FMA_CHAINS,

@@ -112,6 +112,8 @@ def load_library():
         lib.pkv_hbm_copy.restype = c_int
         lib.pkv_hbm_gather_read.argtypes = [vp, vp, i64, i64, i64, vp, vp]
         lib.pkv_hbm_gather_read.restype = c_int
+        lib.pkv_hbm_gather_read_pair.argtypes = [vp, vp, vp, i64, i64, i64, vp, vp]
+        lib.pkv_hbm_gather_read_pair.restype = c_int
         lib.pkv_fp32_fma_peak.argtypes = [vp, c_int, c_int, ctypes.c_float, ctypes.c_float,
                                           ctypes.c_float, c_int, vp]
         lib.pkv_fp32_fma_peak.restype = c_int
@@ -443,6 +445,30 @@ def pkv_hbm_gather_read(base, chunk_index, chunk_stride_bytes: int, chunk_bytes:
     _check(lib.pkv_hbm_gather_read(_ptr(base), _ptr(chunk_index), n, int(chunk_stride_bytes),
                                    int(chunk_bytes), _ptr(sink), _stream_handle(stream, dev)),
            "pkv_hbm_gather_read")
+
+
+def pkv_hbm_gather_read_pair(base_a, base_b, chunk_index, chunk_stride_bytes: int, chunk_bytes: int,
+                             sink, stream=None, check_bounds: bool = True) -> None:
+    """pkv_hbm_gather_read over two buffers (a batch's K and V caches) in
+    one launch: every listed chunk of base_a, then of base_b, XOR-folded
+    into sink."""
+    lib = load_library()
+    _require(chunk_index.dtype == torch.int32 and chunk_index.dim() == 1 and chunk_index.is_contiguous(),
+             "chunk_index must be contiguous int32 [n]")
+    _require(sink.dtype == torch.int64 and sink.numel() == 1, "sink must be one int64")
+    dev = base_a.device
+    _require(dev.type == "cuda" and base_b.device == dev and chunk_index.device == dev and sink.device == dev,
+             "all tensors must be on the same CUDA device")
+    n = chunk_index.numel()
+    if n and check_bounds:
+        hi = int(chunk_index.max()) * chunk_stride_bytes + chunk_bytes
+        for base in (base_a, base_b):
+            _require(int(chunk_index.min()) >= 0 and hi <= base.numel() * base.element_size(),
+                     "a chunk lies outside a base")
+    _check(lib.pkv_hbm_gather_read_pair(_ptr(base_a), _ptr(base_b), _ptr(chunk_index), n,
+                                        int(chunk_stride_bytes), int(chunk_bytes), _ptr(sink),
+                                        _stream_handle(stream, dev)),
+           "pkv_hbm_gather_read_pair")
 
 
 FMA_THREADS = 256   # threads per block of pkv_fp32_fma_peak

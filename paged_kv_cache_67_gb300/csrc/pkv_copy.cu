@@ -5,7 +5,8 @@
 //   pkv_hbm_gather_read  reads of whole chunks at listed places (the
 //                        bandwidth reads of randomly placed cache blocks
 //                        reach -- the decode's own access pattern, without
-//                        its arithmetic).
+//                        its arithmetic); pkv_hbm_gather_read_pair reads the
+//                        listed chunks of two buffers (K and V) in one launch.
 //
 // The copy: one 256-thread block per contiguous run of 1024 16-byte
 // vectors, each thread with its four loads in flight before its stores (a
@@ -52,15 +53,21 @@ constexpr int kGatherThreads = 256;
 constexpr int kGatherBlocksPerSm = 8;
 constexpr int kGatherInFlight = 8;
 
+// Chunk c < nchunks of the list is read from base, chunk nchunks + c (with
+// a second base) from base2: one launch over both.
 __global__ void __launch_bounds__(kGatherThreads) pkv_gather_read_kernel(
-    const uint8_t *__restrict__ base, const int32_t *__restrict__ index, int64_t nchunks,
-    int64_t stride, int64_t vecs, unsigned long long *sink) {
+    const uint8_t *__restrict__ base, const uint8_t *__restrict__ base2,
+    const int32_t *__restrict__ index, int64_t nchunks, int64_t stride, int64_t vecs,
+    unsigned long long *sink) {
   const int lane = threadIdx.x & 31;
   const int64_t warps = (int64_t)gridDim.x * (kGatherThreads / 32);
+  const int64_t total = base2 ? 2 * nchunks : nchunks;
   uint4 acc = make_uint4(0, 0, 0, 0);
-  for (int64_t c = (int64_t)blockIdx.x * (kGatherThreads / 32) + (threadIdx.x >> 5); c < nchunks;
+  for (int64_t c = (int64_t)blockIdx.x * (kGatherThreads / 32) + (threadIdx.x >> 5); c < total;
        c += warps) {
-    const uint4 *src = reinterpret_cast<const uint4 *>(base + (int64_t)__ldg(index + c) * stride);
+    const bool second = c >= nchunks;
+    const uint4 *src = reinterpret_cast<const uint4 *>((second ? base2 : base) +
+                                                       (int64_t)__ldg(index + (second ? c - nchunks : c)) * stride);
     int64_t v = lane;
     for (; v + 32 * (kGatherInFlight - 1) < vecs; v += 32 * kGatherInFlight) {
       uint4 r[kGatherInFlight];
@@ -124,27 +131,46 @@ extern "C" PKV_API pkv_status pkv_fp32_fma_peak(float *out, int blocks, int iter
   return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
-extern "C" PKV_API pkv_status pkv_hbm_gather_read(const void *base, const int32_t *chunk_index,
-                                                  int64_t nchunks, int64_t chunk_stride_bytes,
-                                                  int64_t chunk_bytes, unsigned long long *sink,
-                                                  pkv_stream_t stream) {
+static pkv_status gather_read(const void *base, const void *base2, const int32_t *chunk_index,
+                              int64_t nchunks, int64_t chunk_stride_bytes, int64_t chunk_bytes,
+                              unsigned long long *sink, pkv_stream_t stream) {
   if (nchunks < 0 || chunk_stride_bytes < 0 || chunk_bytes < 0) return PKV_ERR_INVALID_ARG;
   if (nchunks == 0 || chunk_bytes == 0) return PKV_OK;
   if (!base || !chunk_index || !sink || chunk_bytes % 16 || chunk_stride_bytes % 16 ||
-      reinterpret_cast<uintptr_t>(base) % 16 || reinterpret_cast<uintptr_t>(chunk_index) % 4 ||
-      reinterpret_cast<uintptr_t>(sink) % 8)
+      reinterpret_cast<uintptr_t>(base) % 16 || reinterpret_cast<uintptr_t>(base2) % 16 ||
+      reinterpret_cast<uintptr_t>(chunk_index) % 4 || reinterpret_cast<uintptr_t>(sink) % 8)
     return PKV_ERR_INVALID_ARG;
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
     return PKV_ERR_CUDA;
-  const int64_t want = (nchunks + pkv::kGatherThreads / 32 - 1) / (pkv::kGatherThreads / 32);
+  const int64_t total = base2 ? 2 * nchunks : nchunks;
+  const int64_t want = (total + pkv::kGatherThreads / 32 - 1) / (pkv::kGatherThreads / 32);
   const int blocks = (int)std::min<int64_t>(want, (int64_t)sms * pkv::kGatherBlocksPerSm);
   pkv::pkv_gather_read_kernel<<<blocks, pkv::kGatherThreads, 0,
                                 reinterpret_cast<cudaStream_t>(stream)>>>(
-      static_cast<const uint8_t *>(base), chunk_index, nchunks, chunk_stride_bytes,
-      chunk_bytes / 16, sink);
+      static_cast<const uint8_t *>(base), static_cast<const uint8_t *>(base2), chunk_index, nchunks,
+      chunk_stride_bytes, chunk_bytes / 16, sink);
   return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+extern "C" PKV_API pkv_status pkv_hbm_gather_read(const void *base, const int32_t *chunk_index,
+                                                  int64_t nchunks, int64_t chunk_stride_bytes,
+                                                  int64_t chunk_bytes, unsigned long long *sink,
+                                                  pkv_stream_t stream) {
+  return gather_read(base, nullptr, chunk_index, nchunks, chunk_stride_bytes, chunk_bytes, sink,
+                     stream);
+}
+
+extern "C" PKV_API pkv_status pkv_hbm_gather_read_pair(const void *base_a, const void *base_b,
+                                                       const int32_t *chunk_index, int64_t nchunks,
+                                                       int64_t chunk_stride_bytes,
+                                                       int64_t chunk_bytes,
+                                                       unsigned long long *sink,
+                                                       pkv_stream_t stream) {
+  if (!base_b) return PKV_ERR_INVALID_ARG;
+  return gather_read(base_a, base_b, chunk_index, nchunks, chunk_stride_bytes, chunk_bytes, sink,
+                     stream);
 }
 
 extern "C" PKV_API pkv_status pkv_hbm_copy(void *dst, const void *src, size_t bytes,

@@ -86,3 +86,21 @@ def test_fma_other_values_and_bad_args():
     assert lib.pkv_fp32_fma_peak(ctypes.c_void_p(p + 2), 1, 10, 1.0, 1.0, -1.0, 0, s) == 1
     assert lib.pkv_fp32_fma_peak(ctypes.c_void_p(p), 0, 10, 1.0, 1.0, -1.0, 0, s) == 1
     assert lib.pkv_fp32_fma_peak(ctypes.c_void_p(p), 4, -1, 1.0, 1.0, -1.0, 0, s) == 1
+
+
+def test_gather_pair_reads_both_buffers_in_one_launch():
+    """The pair gather's checksum is the XOR of the two single gathers'."""
+    g = torch.Generator().manual_seed(7)
+    stride = chunk = 4096
+    a = torch.randint(-2**62, 2**62, (200 * stride // 8,), dtype=torch.int64, generator=g)
+    b = torch.randint(-2**62, 2**62, (200 * stride // 8,), dtype=torch.int64, generator=g)
+    idx = torch.randperm(200, generator=g)[:77].to(torch.int32)
+    wa, wb = a.numpy().view(np.uint64), b.numpy().view(np.uint64)
+    want = 0
+    for i in idx.tolist():
+        want ^= _xor_fold(wa[i * stride // 8:(i * stride + chunk) // 8])
+        want ^= _xor_fold(wb[i * stride // 8:(i * stride + chunk) // 8])
+    sink = torch.zeros(1, dtype=torch.int64, device=DEV)
+    pkv.pkv_hbm_gather_read_pair(a.to(DEV), b.to(DEV), idx.to(DEV), stride, chunk, sink)
+    torch.cuda.synchronize()
+    assert int(sink.cpu().numpy().view(np.uint64)[0]) == want
