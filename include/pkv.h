@@ -193,6 +193,14 @@ PKV_API size_t pkv_decode_workspace_size(int B, int H, int num_kv_heads, int hea
  * mma.sync kernel; every other supported shape runs the CUDA-core kernel.
  * An explicit partition_size is used as given.  The output does not depend
  * on the partitioning beyond fp32 rounding order.
+ * Inside a stream capture the tensor-core kernels launch as programmatic
+ * dependents of the kernel before them (their start-up overlaps that
+ * kernel's end in the graph): they read q, block_tables, context_lens and
+ * (fused step) the new rows and slots before waiting for that kernel, and
+ * the caches, the workspace and out only after.  So a kernel captured just
+ * before them that releases its dependents early (griddepcontrol.
+ * launch_dependents) must not write those inputs; this library's kernels
+ * never do, and any other kernel is waited for in full.
  * Errors: PKV_ERR_INVALID_ARG, PKV_ERR_UNSUPPORTED, PKV_ERR_WORKSPACE,
  * PKV_ERR_CUDA.  B == 0 enqueues nothing.
  */

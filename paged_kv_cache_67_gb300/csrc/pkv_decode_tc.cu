@@ -188,6 +188,11 @@ __global__ void __launch_bounds__(32 * kTcWarps, 1)
   int *s_scratch = reinterpret_cast<int *>(s_l + kTcHeads);
 
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  // Launched as a programmatic dependent of the previous kernel on the
+  // stream, a CTA reads only inputs (lengths, slots, tables, new rows)
+  // before griddep_wait; K/V loads and every write come after it.  The next
+  // launch may be scheduled once every CTA of this grid has started.
+  griddep_launch_dependents();
   // grid (max_parts, head chunks, B), or with part_major (head chunks, B,
   // max_parts): every unit's first partitions launch first and the short or
   // empty last ones at the end of the launch
@@ -209,6 +214,7 @@ __global__ void __launch_bounds__(32 * kTcWarps, 1)
   }
   if (n == 0) {
     if (part == 0) {
+      griddep_wait();
       zero_rows<T>(a, b, head0, nh);
       if (s_new >= 0 && gc == 0 && w == 0) append_write_row<T>(a, b, kvh, s_new, n, lane);
     }
@@ -281,6 +287,10 @@ __global__ void __launch_bounds__(32 * kTcWarps, 1)
     }
     if (cache_writer && lane == 0) new_ok = append_check(a, b, kvh, s_new, n);
   }
+  // The warp's first table entries are read before the wait (the tables are
+  // inputs); the K/V loads, the cache write and every other write after it.
+  if (nch_w > 0) (void)phys_of(0);
+  griddep_wait();
   // Start the warp's first fetches before staging Q: the copies are in
   // flight while the query tile is loaded.
   const int npro = min(S, nch_w);
@@ -528,7 +538,20 @@ static pkv_status launch_tc_k(const DecodeArgs &a, const DecodePlan &plan, const
   if (plan.max_parts > 65535) args.part_major = 0;  // past the grid's z extent: unit-major
   const dim3 grid = args.part_major ? dim3(a.KVH * plan.gchunks, a.B, plan.max_parts)
                                     : dim3(plan.max_parts, a.KVH * plan.gchunks, a.B);
-  kern<<<grid, 32 * kTcWarps, plan.smem_bytes, stream>>>(mk, mv, args);
+  // a programmatic dependent of the previous kernel on the stream: its CTAs'
+  // start-up overlaps that kernel's last CTAs (see the kernel's griddep_wait)
+  cudaLaunchConfig_t cfg;
+  memset(&cfg, 0, sizeof cfg);
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(32 * kTcWarps);
+  cfg.dynamicSmemBytes = plan.smem_bytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = launch_as_dependent(stream) ? 1 : 0;
+  if (cudaLaunchKernelEx(&cfg, kern, mk, mv, args) != cudaSuccess) return PKV_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 

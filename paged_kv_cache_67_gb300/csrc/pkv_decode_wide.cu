@@ -498,6 +498,13 @@ __global__ void __launch_bounds__(kWdThreads, 1)
                            const __grid_constant__ CUtensorMap tmV, const WdArgs w) {
   using Sh = WdShape<D>;
   const DecodeArgs &a = w.d;
+  // Launched as a programmatic dependent of the previous kernel on the
+  // stream, a CTA reads only inputs (lengths, tables, queries, new rows)
+  // and works out its schedule before griddep_wait; every access the
+  // previous grid may conflict with (K/V loads, cache, workspace and output
+  // writes) comes after it.  All CTAs are resident at once (at most one per
+  // SM), so the next launch may be scheduled as soon as they are.
+  griddep_launch_dependents();
   extern __shared__ uint8_t smem_raw[];
   uint8_t *sm = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -822,7 +829,10 @@ __global__ void __launch_bounds__(kWdThreads, 1)
       }
       __syncwarp();
       ++it;
-      if (it == 1 && blockIdx.x == 0) batch_checks();
+      if (it == 1 && blockIdx.x == 0) {
+        griddep_wait();
+        batch_checks();
+      }
       if (item.kind < 0) break;
       if (item.kind == 1) {
         // the item's 16 query rows, once the last S^T of the previous is done
@@ -863,7 +873,7 @@ __global__ void __launch_bounds__(kWdThreads, 1)
       prefetch_tensormap(&tmV);
     }
     int it = 0, loads = 0, npatch = 0;
-    bool ok = true;
+    bool ok = true, dep_done = false;
     while (ok) {
       const int slot = it & 1;
       ok = __all_sync(0xffffffffu, mbar_wait_bounded(&item_full[slot], (it >> 1) & 1));
@@ -888,6 +898,10 @@ __global__ void __launch_bounds__(kWdThreads, 1)
         return __ldg(a.tables + trow + t / a.bs);
       };
       int ahead = (lane >> 3) < nt ? entry_of(lane >> 3) : 0;
+      if (!dep_done) {  // the previous grid's cache writes land before the first K/V load
+        griddep_wait();
+        dep_done = true;
+      }
       for (int idx = 0; idx < 2 * nt && ok; ++idx) {
         // which tile, K or V
         int j, v;
@@ -1040,6 +1054,7 @@ __global__ void __launch_bounds__(kWdThreads, 1)
     constexpr int kRowVecs = D / 8;        // 16-byte vectors of one head's row (<= 32)
     int it = 0, loads = 0, npatch = 0;
     bool ok = true;
+    griddep_wait();  // it writes cache rows
     while (true) {
       const int slot = it & 1;
       ok = __all_sync(0xffffffffu, mbar_wait_bounded(&item_full[slot], (it >> 1) & 1));
@@ -1110,6 +1125,7 @@ __global__ void __launch_bounds__(kWdThreads, 1)
     if (!ok && lane == 0) abort_cta();
   } else {
     // ------------------------------------------------------------ softmax
+    griddep_wait();  // output rows, partials and counters of the workspace
     const int q4 = warp & 3;                       // tensor-memory lane quarter
     const int t = 32 * q4 + lane;                  // token lane of the tile; D lane of O^T
     const int ts = (warp - 2) * 32 + lane;         // thread of the softmax group
@@ -1316,6 +1332,7 @@ __global__ void __launch_bounds__(kWdThreads, 1)
   }
 
   __syncthreads();
+  griddep_wait();  // (returned already for the roles that touch global memory)
   if (fin[0])
     wd_merge<D, T, kWdThreads>(a, fin[1], fin[2], fin[3], reinterpret_cast<float *>(sm + Sh::kPOff),
                                2 * Sh::kPBytes / 4, s_scratch, a.ws_cnt + fin[4], tid, CtaSync());
@@ -1429,6 +1446,13 @@ static pkv_status launch_wide_t(const WdArgs &w, const CUtensorMap &mq, const CU
   cfg.blockDim = dim3(kWdThreads);
   cfg.dynamicSmemBytes = WdShape<D>::kSmem;
   cfg.stream = stream;
+  // a programmatic dependent of the previous kernel on the stream: its
+  // start-up overlaps that kernel's tail (see the kernel's griddep_wait)
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = launch_as_dependent(stream) ? 1 : 0;
   if (cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, w) != cudaSuccess) return PKV_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }

@@ -62,6 +62,16 @@ __device__ __forceinline__ unsigned long long global_timer_ns() {
   return t;
 }
 
+// Programmatic dependent launch.  launch_dependents: a grid launched after
+// this one with programmatic stream serialization may be scheduled once every
+// CTA of this grid has issued it (or exited).  griddep_wait: wait until the
+// grids this one depends on have completed and their memory operations are
+// visible (returns at once when launched without the attribute).
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // Blackwell paired fp32 arithmetic: two lanes of fma / add in one instruction.
 __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
   unsigned long long d;

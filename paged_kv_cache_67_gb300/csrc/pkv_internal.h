@@ -32,6 +32,16 @@ constexpr int kMaxAutoParts = 64;
 // device is queried).
 constexpr size_t kDefaultSmemOptin = 232448;
 
+// Whether a decode launch on `stream` goes out as a programmatic dependent
+// of the kernel before it: only while the stream is being captured into a
+// graph, where consecutive steps run back to back and one launch's start-up
+// can overlap the previous one's tail.  Launched eagerly (a step at a time,
+// synchronised), the attribute bought nothing and cost a little.
+inline bool launch_as_dependent(cudaStream_t stream) {
+  cudaStreamCaptureStatus st = cudaStreamCaptureStatusNone;
+  return cudaStreamIsCapturing(stream, &st) == cudaSuccess && st == cudaStreamCaptureStatusActive;
+}
+
 bool tc_eligible(pkv_dtype dt, int D, int bs);
 // Fills *plan; returns false for sizes no kernel handles.
 bool make_plan(int B, int H, int KVH, int D, int bs, int max_blocks, int max_context_len,
