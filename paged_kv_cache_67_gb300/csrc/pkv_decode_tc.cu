@@ -288,12 +288,20 @@ __global__ void __launch_bounds__(32 * kTcWarps, 1)
     if (cache_writer && lane == 0) new_ok = append_check(a, b, kvh, s_new, n);
   }
   // The warp's first table entries are read before the wait (the tables are
-  // inputs); the K/V loads, the cache write and every other write after it.
-  if (nch_w > 0) (void)phys_of(0);
+  // inputs), and its first chunks of K and V asked into L2 by TMA prefetches
+  // of the very boxes the loads will read (a line the previous grid still
+  // writes is updated in L2, which the loads read); the K/V loads, the cache
+  // write and every other write come after the wait.
+  const int npro = min(S, nch_w);
+  for (int i = 0; i < npro; ++i) {
+    const int phys = phys_of(i);
+    const int tok = t0 + kChunk * (w + kTcWarps * i);
+    const int row0 = bs_mask >= 0 ? (tok & bs_mask) : tok % a.bs;
+    if (lane < 2) tma_prefetch_5d(lane ? &tmV : &tmK, 0, row0, 0, kvh, phys);
+  }
   griddep_wait();
   // Start the warp's first fetches before staging Q: the copies are in
   // flight while the query tile is loaded.
-  const int npro = min(S, nch_w);
   for (int i = 0; i < npro; ++i) issue(i, i);
 
   // Q rows of the group (rows >= nh are zero) into padded shared rows.

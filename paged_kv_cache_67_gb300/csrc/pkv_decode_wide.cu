@@ -203,6 +203,15 @@ __device__ __forceinline__ void wd_tma_4d(void *dst, const CUtensorMap *map, uin
       : "memory");
 }
 
+// The same 4-D box asked into L2 only (no shared memory, no barrier).
+__device__ __forceinline__ void wd_tma_prefetch_4d(const CUtensorMap *map, int c0, int c1, int c2,
+                                                   int c3) {
+  asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+               : "memory");
+}
+
 __device__ __forceinline__ void wd_tma_3d(void *dst, const CUtensorMap *map, uint64_t *bar, int c0,
                                           int c1, int c2) {
   asm volatile(
@@ -899,6 +908,21 @@ __global__ void __launch_bounds__(kWdThreads, 1)
       };
       int ahead = (lane >> 3) < nt ? entry_of(lane >> 3) : 0;
       if (!dep_done) {  // the previous grid's cache writes land before the first K/V load
+        // Before waiting: the first item's first two tiles of K and V are
+        // asked into L2 by TMA prefetches of the very boxes the loads will
+        // read, so those loads find them there.  A line the previous grid
+        // still writes is updated in L2, which the loads after the wait read.
+        for (int j = 0; j < min(nt, 2); ++j) {
+          const int tok0 = item.t0 + j * kWdTile;
+          const int valid_chunks = min(nch, (item.t1 - tok0 + bt - 1) / bt);
+          const int phys = __shfl_sync(0xffffffffu, ahead, 8 * j + (bt >> 4) * chunk);
+          if (lane < per_tensor && chunk < valid_chunks && phys >= 0 && (long long)phys < a.num_blocks) {
+            const int t = tok0 + bt * chunk;
+            const int lb = t / a.bs;
+            wd_tma_prefetch_4d(&tmK, region * 64, item.kvh, t - lb * a.bs, phys);
+            wd_tma_prefetch_4d(&tmV, region * 64, item.kvh, t - lb * a.bs, phys);
+          }
+        }
         griddep_wait();
         dep_done = true;
       }

@@ -152,6 +152,15 @@ __device__ __forceinline__ void tma_load_4d(void *dst, const CUtensorMap *map, u
 }
 
 // Tiled 5-D TMA load global -> shared, completion counted on `bar`.
+// The same 5-D box asked into L2 only (no shared memory, no barrier).
+__device__ __forceinline__ void tma_prefetch_5d(const CUtensorMap *map, int c0, int c1, int c2,
+                                                int c3, int c4) {
+  asm volatile("cp.async.bulk.prefetch.tensor.5d.L2.global.tile [%0, {%1, %2, %3, %4, %5}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4)
+               : "memory");
+}
+
 __device__ __forceinline__ void tma_load_5d(void *dst, const CUtensorMap *map, uint64_t *bar,
                                             int c0, int c1, int c2, int c3, int c4,
                                             uint64_t policy) {
