@@ -33,6 +33,12 @@
 // At the end the 4 warp states are merged in shared memory and the
 // partition is finished by finish_partition (direct output, or partials +
 // log-sum-exp merge by the last CTA of the sequence).
+//
+// Launched into a captured graph, the kernel is a programmatic dependent of
+// the step before it: a CTA reads its length, slot and table entries and
+// asks L2 for its warps' first chunks (TMA prefetches of the boxes the
+// first loads read) before griddepcontrol.wait; K/V loads and every write
+// come after it.
 #include <string.h>
 
 #include "pkv_device.cuh"

@@ -61,6 +61,11 @@
 //              end and is run by all eight warps: twice the threads, half
 //              the rounds of partial loads, on the launch's tail (the whole
 //              CTA's: 35.2 -> 34.2 us on the MQA batch, three input sets).
+// Launched into a captured graph, the kernel is a programmatic dependent of
+// the step before it: a CTA works out its schedule, reads its first item's
+// table entries and asks L2 for that item's first two K/V tiles (TMA
+// prefetches of the boxes its loads will read) before griddepcontrol.wait;
+// K/V loads, cache, workspace and output writes come after.
 // Every wait on an mbarrier is bounded; on time-out the CTA raises
 // PKV_FLAG_TIMEOUT, lets its copies and products land (bounded) and exits.
 #include <string.h>
