@@ -1058,7 +1058,8 @@ def run_e2e(args, world, dev, pkv, run, stream, total_bytes):
     aligned offset) and go over in one copy into a device buffer that the
     kernels read through views, the way a serving loop stages a batch; the
     fused step is a prepared call on those views (its checks and argument
-    marshalling done once, as a loop that reuses its buffers would)."""
+    marshalling done once, as a loop that reuses its buffers would), and so
+    are the copy in and the copy out (pkv_copy_async)."""
     steps = run.sets[0]["steps"]
     inp, out, ws, err, max_ctx = run.inp, run.out, run.ws, run.err, run.max_ctx
     S = len(steps)
@@ -1094,8 +1095,11 @@ def run_e2e(args, world, dev, pkv, run, stream, total_bytes):
             dbuf["tables"], dbuf["lens"], inp.scale, max_context_len=max_ctx, workspace=ws,
             err_flags=err, stream=stream)
 
+    copy_in = [pkv.prepare_copy_async(dblob, hb, stream=stream) for hb in host]
+    copy_out = pkv.prepare_copy_async(h_out, out, stream=stream)
+
     def e2e_step(i):
-        dblob.copy_(host[i % S], non_blocking=True)
+        copy_in[i % S]()
         if fused_call is not None:
             fused_call()
         else:
@@ -1104,7 +1108,7 @@ def run_e2e(args, world, dev, pkv, run, stream, total_bytes):
             pkv.pkv_decode_attention(out, dbuf["q"], inp.k_cache, inp.v_cache, dbuf["tables"],
                                      dbuf["lens"], inp.scale, max_context_len=max_ctx,
                                      workspace=ws, err_flags=err, stream=stream)
-        h_out.copy_(out, non_blocking=True)
+        copy_out()
         stream.synchronize()  # the caller reads the result every step
 
     with torch.cuda.stream(stream):

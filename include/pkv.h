@@ -459,6 +459,21 @@ PKV_API pkv_status pkv_hbm_gather_read_pair(const void *base_a, const void *base
 PKV_API pkv_status pkv_fp32_fma_peak(float *out, int blocks, int iters, float a, float b,
                                      float never, int paired, pkv_stream_t stream);
 
+/*
+ * pkv_copy_async -- enqueues one copy of `bytes` bytes from src to dst on
+ * `stream`, between any two memories the GPU addresses (device memory,
+ * pinned or pageable host memory; the runtime tells which from the
+ * pointers).  It is how a serving loop built on this library moves a step's
+ * staged inputs in and its output out around a prepared step call, one
+ * call per copy, without a framework's tensor copy in between.  The ranges
+ * must not overlap.  Pinned host memory gives an asynchronous copy;
+ * pageable host memory is staged by the runtime and may return only once
+ * the copy is done.  Errors: PKV_ERR_INVALID_ARG (dst or src NULL with
+ * bytes > 0, overlapping ranges), PKV_ERR_CUDA (the runtime refused the
+ * copy).  bytes == 0 enqueues nothing.
+ */
+PKV_API pkv_status pkv_copy_async(void *dst, const void *src, size_t bytes, pkv_stream_t stream);
+
 /* A static, human-readable name for a status code. */
 PKV_API const char *pkv_status_string(pkv_status status);
 

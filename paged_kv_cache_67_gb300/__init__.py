@@ -35,6 +35,7 @@ from ._binding import (  # noqa: F401
     pkv_decode_attention_xpacked,
     pkv_decode_plan,
     pkv_decode_workspace_size,
+    pkv_copy_async,
     pkv_hbm_copy,
     pkv_hbm_gather_read,
     pkv_hbm_gather_read_pair,
@@ -47,6 +48,7 @@ from ._binding import (  # noqa: F401
     pkv_write,
     pkv_write_decode_attention,
     pkv_write_xpacked,
+    prepare_copy_async,
     prepare_decode_attention,
     prepare_write_decode_attention,
 )

@@ -110,6 +110,8 @@ def load_library():
         lib.pkv_bm_block_refcount.restype = c_int
         lib.pkv_hbm_copy.argtypes = [vp, vp, c_size, vp]
         lib.pkv_hbm_copy.restype = c_int
+        lib.pkv_copy_async.argtypes = [vp, vp, c_size, vp]
+        lib.pkv_copy_async.restype = c_int
         lib.pkv_hbm_gather_read.argtypes = [vp, vp, i64, i64, i64, vp, vp]
         lib.pkv_hbm_gather_read.restype = c_int
         lib.pkv_hbm_gather_read_pair.argtypes = [vp, vp, vp, i64, i64, i64, vp, vp]
@@ -407,6 +409,33 @@ def pkv_decode_attention_with_kernel(out, q, k_cache, v_cache, block_tables, con
         int(max_context_len), int(partition_size), ws_ptr, ws_bytes, _ptr(err_flags), int(kernel),
         _stream_handle(stream, dev)), "pkv_decode_attention_with_kernel")
     return out
+
+
+def _copy_args(dst, src, stream):
+    nbytes = src.numel() * src.element_size()
+    _require(dst.numel() * dst.element_size() == nbytes, "dst and src differ in size")
+    _require(src.is_contiguous() and dst.is_contiguous(), "tensors must be contiguous")
+    cuda = [t.device for t in (dst, src) if t.device.type == "cuda"]
+    _require(len(cuda) > 0 and all(d == cuda[0] for d in cuda),
+             "one tensor must be on a CUDA device (both on the same one)")
+    return _ptr(dst), _ptr(src), nbytes, _stream_handle(stream, cuda[0])
+
+
+def pkv_copy_async(dst, src, stream=None) -> None:
+    """Enqueue a copy of src's bytes into dst (same byte size, contiguous;
+    host or device, at least one on the GPU) on the stream: a step's staged
+    inputs in, or its output out.  Pinned host tensors give an asynchronous
+    copy."""
+    lib = load_library()
+    _check(lib.pkv_copy_async(*_copy_args(dst, src, stream)), "pkv_copy_async")
+
+
+def prepare_copy_async(dst, src, stream=None) -> PreparedCall:
+    """pkv_copy_async, checked and marshalled once (see PreparedCall): a
+    serving loop's per-step copy in or out of the same buffers."""
+    lib = load_library()
+    return PreparedCall(lib.pkv_copy_async, _copy_args(dst, src, stream), "pkv_copy_async",
+                        (dst, src))
 
 
 def pkv_hbm_copy(dst, src, stream=None) -> None:

@@ -475,6 +475,16 @@ PKV_API pkv_status pkv_prefill_attention(void *out, const void *q, const void *k
                            reinterpret_cast<cudaStream_t>(stream));
 }
 
+PKV_API pkv_status pkv_copy_async(void *dst, const void *src, size_t bytes, pkv_stream_t stream) {
+  if (bytes == 0) return PKV_OK;
+  if (!dst || !src) return PKV_ERR_INVALID_ARG;
+  const uintptr_t d0 = reinterpret_cast<uintptr_t>(dst), s0 = reinterpret_cast<uintptr_t>(src);
+  if (d0 < s0 + bytes && s0 < d0 + bytes) return PKV_ERR_INVALID_ARG;  // overlapping ranges
+  const cudaError_t e =
+      cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDefault, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
 PKV_API const char *pkv_status_string(pkv_status status) {
   switch (status) {
     case PKV_OK: return "ok";

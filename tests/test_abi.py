@@ -148,3 +148,18 @@ def test_host_side_argument_errors(pkv):
     assert fz(ks=100) == 1               # stride shorter than a row
     assert fz(ks=132) == 1               # stride not a multiple of 16 bytes
     assert fz(dt=9) == 1
+
+
+def test_copy_async_argument_errors(pkv):
+    """pkv_copy_async refuses NULL pointers and overlapping ranges on the host,
+    before any CUDA call; zero bytes enqueue nothing."""
+    lib = pkv.load_library()
+    buf = ctypes.create_string_buffer(4096)
+    p = ctypes.addressof(buf)
+    vp = ctypes.c_void_p
+    assert lib.pkv_copy_async(None, vp(p), 16, None) == 1
+    assert lib.pkv_copy_async(vp(p), None, 16, None) == 1
+    assert lib.pkv_copy_async(vp(p + 8), vp(p), 64, None) == 1   # overlap
+    assert lib.pkv_copy_async(vp(p), vp(p + 63), 64, None) == 1  # overlap
+    assert lib.pkv_copy_async(None, None, 0, None) == 0
+    assert lib.pkv_copy_async(vp(p), vp(p), 0, None) == 0

@@ -374,3 +374,68 @@ def test_prepared_call_matches_the_plain_call():
     with pytest.raises(ValueError):  # checked at preparation
         pkv.prepare_write_decode_attention(out, q, k[:1], v, slots, kc, vc, tables, lens_t, 0.09,
                                            workspace=ws)
+
+
+def test_staged_step_through_prepared_copies():
+    """A serving loop's step from host memory: the inputs staged in one pinned
+    host buffer go over in one pkv_copy_async into a device buffer whose
+    views the prepared fused call reads, and the output comes back by a
+    second copy into pinned host memory.  Each step's host result equals the
+    device-only call's bit for bit, and the caches are written the same."""
+    lens = [17, 200, 64, 1, 129]
+    B, H, KVH, D, bs = 5, 8, 2, 128, 16
+    case = random_paged_case(93, lens, H=H, KVH=KVH, D=D, bs=bs, dtype=torch.bfloat16, poison=False)
+    d = lambda t: t.to(DEV)
+    kc, vc = d(case["k_cache"]), d(case["v_cache"])
+    kc2, vc2 = kc.clone(), vc.clone()
+    slots = torch.tensor([wl.slot_of(case["owned"][b], n - 1, bs) for b, n in enumerate(lens)])
+    parts = {"q": case["q"], "k": torch.empty((B, KVH, D), dtype=torch.bfloat16),
+             "v": torch.empty((B, KVH, D), dtype=torch.bfloat16), "slots": slots,
+             "tables": case["block_tables"], "lens": case["context_lens"]}
+    offs, off = {}, 0
+    for name, t in parts.items():
+        offs[name] = off
+        off += (t.numel() * t.element_size() + 255) // 256 * 256
+
+    def views(buf):
+        return {n: buf[offs[n]:offs[n] + t.numel() * t.element_size()].view(t.dtype).view(t.shape)
+                for n, t in parts.items()}
+
+    h_in = torch.zeros(off, dtype=torch.uint8).pin_memory()
+    d_in = torch.zeros(off, dtype=torch.uint8, device=DEV)
+    hv, dv = views(h_in), views(d_in)
+    out = torch.empty((B, H, D), dtype=torch.bfloat16, device=DEV)
+    h_out = torch.empty((B, H, D), dtype=torch.bfloat16).pin_memory()
+    ws = pkv.DecodeWorkspace(B, H, KVH, D, bs, case["block_tables"].shape[1], device=DEV)
+    ws2 = pkv.DecodeWorkspace(B, H, KVH, D, bs, case["block_tables"].shape[1], device=DEV)
+    stream = torch.cuda.Stream()
+    copy_in = pkv.prepare_copy_async(d_in, h_in, stream=stream)
+    step = pkv.prepare_write_decode_attention(out, dv["q"], dv["k"], dv["v"], dv["slots"], kc, vc,
+                                              dv["tables"], dv["lens"], 0.09, workspace=ws,
+                                              stream=stream)
+    copy_out = pkv.prepare_copy_async(h_out, out, stream=stream)
+    g = torch.Generator().manual_seed(94)
+    for s in range(3):
+        for n, t in parts.items():
+            hv[n].copy_(t)
+        hv["q"].copy_(torch.randn((B, H, D), generator=g).to(torch.bfloat16))
+        hv["k"].copy_(torch.randn((B, KVH, D), generator=g).to(torch.bfloat16))
+        hv["v"].copy_(torch.randn((B, KVH, D), generator=g).to(torch.bfloat16))
+        copy_in()
+        step()
+        copy_out()
+        stream.synchronize()
+        want = pkv.pkv_write_decode_attention(torch.empty_like(out), d(hv["q"]), d(hv["k"]),
+                                              d(hv["v"]), d(slots), kc2, vc2,
+                                              d(case["block_tables"]), d(case["context_lens"]),
+                                              0.09, workspace=ws2)
+        torch.cuda.synchronize()
+        assert torch.equal(bits(h_out), bits(want.cpu())), f"step {s}"
+        assert torch.equal(bits(kc), bits(kc2)) and torch.equal(bits(vc), bits(vc2))
+    # device to device and pageable host memory go through the same call
+    back = torch.empty(off, dtype=torch.uint8)
+    d2 = torch.empty_like(d_in)
+    pkv.pkv_copy_async(d2, d_in)
+    pkv.pkv_copy_async(back, d2)
+    torch.cuda.synchronize()
+    assert torch.equal(back, h_in)
