@@ -156,7 +156,14 @@ PKV_API size_t pkv_decode_workspace_size(int B, int H, int num_kv_heads, int hea
  * tokens in fp32, weighted sum of V, cast to q's dtype.
  *
  *   out           [B, H, head_dim], dtype dt (written; rows of sequences with
- *                 context_lens[b] == 0 are set to zero)
+ *                 context_lens[b] == 0 are set to zero).  Device memory, or
+ *                 host memory the GPU addresses directly (pinned memory under
+ *                 unified addressing; any host memory where the system
+ *                 translates host addresses for the GPU): the kernels only
+ *                 store to out -- no reads, atomics or TMA -- so the result
+ *                 crosses to the host inside the launch and needs no copy
+ *                 after it.  Its rows are complete for the host once the
+ *                 stream is synchronised.
  *   q             [B, H, head_dim], dtype dt
  *   k_cache, v_cache  [num_blocks, block_size, num_kv_heads, head_dim], dtype dt
  *   block_tables  [B, max_blocks] int32; only the first ceil(n/bs) entries of
@@ -367,8 +374,8 @@ PKV_API pkv_status pkv_prefill_attention(void *out, const void *q, const void *k
  * errors; block_size must be 16, head_dim a multiple of 8, k and the
  * caches 16-byte aligned, token strides multiples of 8 elements).
  * pkv_decode_attention_xpacked -- pkv_decode_attention over packed caches
- * (same arguments, workspace and errors; head_dim 64, 128 or 256; returns
- * PKV_ERR_UNSUPPORTED for other shapes and for fp32).
+ * (same arguments, workspace and errors, out in device memory; head_dim 64,
+ * 128 or 256; returns PKV_ERR_UNSUPPORTED for other shapes and for fp32).
  */
 PKV_API pkv_status pkv_write_xpacked(void *k_cache_x, void *v_cache_x, const void *k, const void *v,
                                      const int64_t *slot_mapping, int64_t num_tokens,

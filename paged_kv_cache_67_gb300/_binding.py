@@ -230,9 +230,13 @@ def _decode_checks(out, q, k_cache, v_cache, block_tables, context_lens):
              "block_tables must be int32 [B, max_blocks]")
     _require(context_lens.dtype == torch.int32 and context_lens.shape == (B,), "context_lens must be int32 [B]")
     dev = q.device
-    _require(dev.type == "cuda" and all(t.device == dev for t in (out, k_cache, v_cache, block_tables,
+    _require(dev.type == "cuda" and all(t.device == dev for t in (k_cache, v_cache, block_tables,
                                                                    context_lens)),
              "all tensors must be on the same CUDA device")
+    # out may also be pinned host memory: the kernels only store to it, so
+    # the result crosses to the host inside the launch
+    _require(out.device == dev or (out.device.type == "cpu" and out.is_pinned()),
+             "out must be on q's CUDA device or in pinned host memory")
     return dev
 
 

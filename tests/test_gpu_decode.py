@@ -347,3 +347,36 @@ def test_forced_kernels_agree_and_refuse_what_they_cannot_run():
     with pytest.raises(pkv.PkvError) as e:
         pkv.pkv_decode_attention_with_kernel(torch.empty_like(d[0]), *d, 0.1, 7, workspace=ws)
     assert e.value.status == 1
+
+
+@pytest.mark.parametrize("kernel,H,KVH,D,dtype", [
+    (pkv.KERNEL_CUDA_CORE, 4, 2, 64, torch.float32),
+    (pkv.KERNEL_TC, 8, 2, 128, torch.bfloat16),
+    (pkv.KERNEL_WIDE, 16, 1, 128, torch.bfloat16),
+])
+def test_output_into_pinned_host_memory(kernel, H, KVH, D, dtype):
+    """out may be pinned host memory: every decode kernel only stores to it,
+    so the result lands on the host inside the launch.  Bit-identical to the
+    same call into device memory, over one-partition, merged (partition 128)
+    and empty contexts, on each kernel."""
+    lens = [300, 0, 129, 5, 1000, 64]
+    case = random_paged_case(71 + kernel, lens, H=H, KVH=KVH, D=D, bs=16, dtype=dtype)
+    d = lambda t: t.to(DEV)
+    args = (d(case["q"]), d(case["k_cache"]), d(case["v_cache"]), d(case["block_tables"]),
+            d(case["context_lens"]), 0.11)
+    for P in (0, 128):
+        ws = pkv.DecodeWorkspace(len(lens), H, KVH, D, 16, case["block_tables"].shape[1], 0, P,
+                                 device=DEV)
+        want = torch.full((len(lens), H, D), float("nan"), dtype=dtype, device=DEV)
+        pkv.pkv_decode_attention_with_kernel(want, *args, kernel=kernel, partition_size=P,
+                                             workspace=ws)
+        got = torch.full((len(lens), H, D), float("nan"), dtype=dtype).pin_memory()
+        err = torch.zeros(1, dtype=torch.int32, device=DEV)
+        pkv.pkv_decode_attention_with_kernel(got, *args, kernel=kernel, partition_size=P,
+                                             workspace=ws, err_flags=err)
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+        assert torch.equal(bits(got), bits(want.cpu())), f"partition {P}"
+        assert bool((got[1] == 0).all())
+    with pytest.raises(ValueError):  # pageable host memory is refused
+        pkv.pkv_decode_attention(torch.empty((len(lens), H, D), dtype=dtype), *args)

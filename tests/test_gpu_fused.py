@@ -432,6 +432,14 @@ def test_staged_step_through_prepared_copies():
         torch.cuda.synchronize()
         assert torch.equal(bits(h_out), bits(want.cpu())), f"step {s}"
         assert torch.equal(bits(kc), bits(kc2)) and torch.equal(bits(vc), bits(vc2))
+    # the same step with out in pinned host memory: no copy after the launch
+    h_out2 = torch.empty_like(h_out).pin_memory()
+    step2 = pkv.prepare_write_decode_attention(h_out2, dv["q"], dv["k"], dv["v"], dv["slots"], kc,
+                                               vc, dv["tables"], dv["lens"], 0.09, workspace=ws,
+                                               stream=stream)
+    step2()
+    stream.synchronize()
+    assert torch.equal(bits(h_out2), bits(h_out))
     # device to device and pageable host memory go through the same call
     back = torch.empty(off, dtype=torch.uint8)
     d2 = torch.empty_like(d_in)
