@@ -163,3 +163,16 @@ def test_copy_async_argument_errors(pkv):
     assert lib.pkv_copy_async(vp(p), vp(p + 63), 64, None) == 1  # overlap
     assert lib.pkv_copy_async(None, None, 0, None) == 0
     assert lib.pkv_copy_async(vp(p), vp(p), 0, None) == 0
+
+
+def test_copy_async_binding_checks_on_the_host(pkv):
+    """The binding refuses, before any CUDA call, a copy with no tensor on the
+    GPU, tensors of different byte sizes, and non-contiguous tensors."""
+    import torch
+    a = torch.zeros(64, dtype=torch.uint8)
+    with pytest.raises(ValueError):
+        pkv.pkv_copy_async(a, torch.zeros(64, dtype=torch.uint8))       # both on the host
+    with pytest.raises(ValueError):
+        pkv.pkv_copy_async(a, torch.zeros(32, dtype=torch.int16)[:16])  # 64 vs 32 bytes
+    with pytest.raises(ValueError):
+        pkv.prepare_copy_async(torch.zeros(8, 8)[:, 0], torch.zeros(8))  # not contiguous
