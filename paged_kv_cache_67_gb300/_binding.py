@@ -255,7 +255,8 @@ def pkv_write_decode_attention(out, q, k, v, slot_mapping, k_cache, v_cache, blo
     ([B, KVH, D]) at slot_mapping[b] (int64 [B], negative = none), then paged
     decode attention into ``out`` [B, H, D] (returned) over contexts that
     already count the new token (slot_mapping[b] must be the slot of position
-    context_lens[b] - 1)."""
+    context_lens[b] - 1).  ``out`` may be a pinned host tensor: the kernels
+    only store to it, so the result reaches the host inside the launch."""
     lib = load_library()
     dev = _decode_checks(out, q, k_cache, v_cache, block_tables, context_lens)
     B, H, D = q.shape
@@ -376,7 +377,8 @@ def pkv_prefill_attention(out, q, k_cache, v_cache, block_tables, cu_seqlens_q, 
 def pkv_decode_attention(out, q, k_cache, v_cache, block_tables, context_lens, scale: float,
                          max_context_len: int = 0, partition_size: int = 0, workspace=None,
                          err_flags=None, stream=None):
-    """Paged decode attention into ``out`` [B, H, D] (returned)."""
+    """Paged decode attention into ``out`` [B, H, D] (returned): on q's
+    device, or a pinned host tensor that the kernels store the result into."""
     lib = load_library()
     dev = _decode_checks(out, q, k_cache, v_cache, block_tables, context_lens)
     B, H, D = q.shape
